@@ -1,0 +1,220 @@
+/*
+ * q4adamw.h -- C ABI of the B300 (sm_103a) fused 4-bit AdamW optimizer step.
+ *
+ * The method: "Rounding in Preconditioner Space: Redesigning 4-bit AdamW
+ * Optimizer-State Quantization" (Li et al., arXiv:2610.12444).  Its listing
+ * page's Abstract and Table 2 define the two recipes:
+ *   ZIP-SR  -- NF4 first moment (RTN), zero-inclusive dynamic-exponent 4-bit
+ *              second moment with stochastic rounding whose probabilities are
+ *              chosen in preconditioner space r = 1/(sqrt(v_hat)+eps);
+ *   ZE-EDEN -- NF4 first moment (RTN), zero-excluding dynamic-exponent 4-bit
+ *              second moment (RTN) with an EDEN rescale of each block;
+ * both with NF4 stochastic rounding of the LM-head first moment during the
+ * final 10% of training (Table 2 note).  The AReno docs page "4-bit AdamW",
+ * section "State representation", adds the factored mode (Adafactor row and
+ * column means over [shape[0], -1] for rank >= 2, packed zero-excluding v for
+ * 1-D tensors) and fixes the 128-element parameter-local block.  The news page
+ * (paragraph 4) fixes the storage: 4-bit codes plus one FP32 scale per block
+ * and moment, 1.0625 bytes/param for m+v.
+ *
+ * Conventions for every entry point:
+ *   - All buffers are owned by the caller.  Device pointers point to memory
+ *     of the current CUDA device; `stream` is a cudaStream_t (NULL = legacy
+ *     default stream).  The library allocates no device memory.
+ *   - Calls that take a stream are asynchronous with respect to the host:
+ *     they validate, enqueue kernels and return.  A kernel error surfaces at
+ *     the caller's next synchronisation.
+ *   - Every call returns a q4_status; none aborts, throws or exits.  On any
+ *     validation error nothing is enqueued.  Q4_ECUDA means a CUDA runtime
+ *     call failed; q4adamw_last_cuda_error() returns its cudaError_t.
+ *   - Blocks are 128 consecutive elements of one tensor in row-major flat
+ *     order; block b covers elements [128b, min(128b+128, numel)).
+ *   - Codes are packed two per byte: element 2k of a block in the low nibble
+ *     of byte k, element 2k+1 in the high nibble.  Code c indexes the
+ *     codebook's levels sorted ascending.  Each block owns 64 code bytes even
+ *     when it is partial; nibbles past numel are written as 0.
+ */
+#ifndef Q4ADAMW_H
+#define Q4ADAMW_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define Q4ADAMW_BLOCK 128        /* elements per quantisation block */
+#define Q4ADAMW_STATE_FORMAT 1   /* version of the state layout below */
+#define Q4ADAMW_MAGIC 0x57413451u /* "Q4AW" little-endian */
+
+typedef enum q4_status {
+    Q4_OK = 0,
+    Q4_EINVAL = -1,     /* null pointer where one is required, n < 0, step < 1,
+                           beta outside [0,1), eps <= 0, non-finite lr / wd */
+    Q4_EALIGN = -2,     /* a pointer violates the alignment stated below */
+    Q4_ESHAPE = -3,     /* numel < 0; factored tensor with rows < 1 or rows
+                           not dividing numel; elem_offset not a multiple of
+                           128 */
+    Q4_ERECIPE = -4,    /* unknown recipe or codebook id */
+    Q4_EVERSION = -5,   /* state header does not match this library/recipe */
+    Q4_ECUDA = -6,      /* a CUDA runtime call failed */
+    Q4_EWORKSPACE = -7  /* workspace NULL, too small or not 256-B aligned */
+} q4_status;
+
+typedef enum q4_recipe {
+    Q4_RECIPE_ZIP_SR = 0,   /* listing page Table 2, row "ZIP-SR 4-bit" */
+    Q4_RECIPE_ZE_EDEN = 1,  /* listing page Table 2, row "ZE-EDEN 4-bit" */
+    Q4_RECIPE_FACTORED = 2  /* AReno docs, State representation */
+} q4_recipe;
+
+/* Per-tensor flags (q4adamw_tensor_t.flags). */
+#define Q4_T_LM_HEAD  0x1u  /* this tensor is the LM head: its m uses NF4
+                               stochastic rounding while Q4_LM_HEAD_SR_ACTIVE */
+#define Q4_T_FACTORED 0x2u  /* rank >= 2 tensor: under Q4_RECIPE_FACTORED its v
+                               is the factored row/column form; ignored by the
+                               other recipes */
+
+/* Per-call flags (q4adamw_step). */
+#define Q4_LM_HEAD_SR_ACTIVE 0x1u /* the final 10% phase of the schedule: the
+                                     caller sets it when step > 0.9 * total */
+
+/*
+ * One parameter tensor and its optimizer state.  All pointers are device
+ * pointers owned by the caller.
+ *   param       FP32 master weights, numel.                    in/out, 16-B aligned
+ *   grad        BF16 gradient (raw bits), numel.               in,     16-B aligned
+ *   param_bf16  BF16 copy of the updated weights, numel.       out,    16-B aligned, may be NULL
+ *   m_codes     NF4 codes of m, ceil(numel/128)*64 bytes.      in/out, 16-B aligned
+ *   m_scale     FP32 absmax scale of m per block.              in/out, 4-B aligned
+ *   v_codes     dynamic-exponent codes of v, as m_codes.       in/out, NULL for factored tensors
+ *   v_scale     FP32 scale of v per block.                     in/out, NULL for factored tensors
+ *   v_row       factored row factor R, rows floats.            in/out, factored tensors only
+ *   v_col       factored column factor C, numel/rows floats.   in/out, factored tensors only
+ *   numel       number of elements (0 allowed: nothing to do)
+ *   rows        shape[0] of the tensor ([rows, numel/rows] view); 1 for 1-D
+ *   elem_offset global index of element 0 within the full parameter, for a
+ *               data-parallel shard; a multiple of 128.  Random draws depend
+ *               only on (seed, step, tensor_id, elem_offset + index).
+ *   tensor_id   stable id of the parameter (a random-draw key component)
+ *   flags       Q4_T_* bits
+ */
+typedef struct q4adamw_tensor {
+    float* param;
+    const uint16_t* grad;
+    uint16_t* param_bf16;
+    uint8_t* m_codes;
+    float* m_scale;
+    uint8_t* v_codes;
+    float* v_scale;
+    float* v_row;
+    float* v_col;
+    int64_t numel;
+    int64_t rows;
+    uint64_t elem_offset;
+    uint32_t tensor_id;
+    uint32_t flags;
+} q4adamw_tensor_t;
+
+/*
+ * State header: what a checkpoint of the 4-bit state must carry so that it is
+ * resumed only by this optimizer in this representation (AReno docs,
+ * "Requirements and errors": a saved 4-bit state resumes only with the 4-bit
+ * optimizer; earlier representations are incompatible).  Host memory.
+ */
+typedef struct q4adamw_header {
+    uint32_t magic;       /* Q4ADAMW_MAGIC */
+    uint32_t format;      /* Q4ADAMW_STATE_FORMAT */
+    uint32_t recipe;      /* q4_recipe */
+    uint32_t block;       /* Q4ADAMW_BLOCK */
+    int64_t n_tensors;
+    int64_t numel_total;
+} q4adamw_header_t;
+
+/* State-format version of this library (Q4ADAMW_STATE_FORMAT). */
+int q4adamw_version(void);
+
+/* Static, NUL-terminated description of a q4_status (never NULL). */
+const char* q4adamw_strerror(int status);
+
+/* cudaError_t of the most recent Q4_ECUDA on the calling thread (0 if none). */
+int q4adamw_last_cuda_error(void);
+
+/*
+ * Storage of the persistent 4-bit state (AReno docs "Requirements and
+ * errors": adam4_quantized_state_bytes, adam4_scale_metadata_bytes,
+ * adam4_total_bytes).  Host-only; reads numel/rows/flags of t[0..n) only.
+ *   quantized   code bytes of m and v (64 B per block and packed moment)
+ *   scale_meta  FP32 block scales, plus R and C floats of factored tensors
+ *   total       quantized + scale_meta
+ * For packed tensors whose numel is a multiple of 128 this is exactly
+ * 1.0625 bytes/param (news page, paragraph 4).  Any output pointer may be NULL.
+ */
+int q4adamw_state_bytes(const q4adamw_tensor_t* t, int n, int recipe, int64_t* quantized, int64_t* scale_meta,
+                        int64_t* total);
+
+/* Device workspace q4adamw_step needs for this tensor list (host-only).  The
+ * workspace holds the descriptor table and, for factored tensors, the
+ * partial row/column sums.  It must be 256-B aligned. */
+int q4adamw_workspace_bytes(const q4adamw_tensor_t* t, int n, int recipe, int64_t* bytes);
+
+/*
+ * Zero-initialise the state of t[0..n): codes, scales and factored R, C.
+ * A zero scale decodes every code to 0, so the first step starts from
+ * m = v = 0 as AdamW does.  If header_out is not NULL it is filled for
+ * recipe.  Asynchronous on stream.
+ */
+int q4adamw_state_init(const q4adamw_tensor_t* t, int n, int recipe, q4adamw_header_t* header_out, void* stream);
+
+/* Q4_OK if h was written by q4adamw_state_init of this state format for
+ * recipe; Q4_EVERSION otherwise; Q4_EINVAL if h is NULL.  Host-only. */
+int q4adamw_header_check(const q4adamw_header_t* h, int recipe);
+
+/*
+ * One fused 4-bit AdamW step over the tensor list t[0..n), step number
+ * `step` (1-based), on `stream`.
+ *
+ * Per element (FP32, each operation correctly rounded; news page paragraph 2
+ * and listing page Abstract for AdamW with bias correction and decoupled
+ * weight decay):
+ *   m  = NF4[qm] * s_m;   v = V[qv] * s_v      (factored: R_i*C_j / mean(R))
+ *   m' = fma(beta1, m, (1-beta1) * g);   v' = fma(beta2, v, (1-beta2) * g*g)
+ *   r  = 1 / (sqrt(v') * c2 + eps),  c2 = 1/sqrt(1 - beta2^step)
+ *   param' = param * (1 - lr*wd) - (lr / (1 - beta1^step)) * (m' * r)
+ *   param_bf16 = round-to-nearest-even(param')
+ * Per 128-block: new scales s = max|m'|, max v'; m requantised NF4 RTN
+ * (LM head with Q4_LM_HEAD_SR_ACTIVE: NF4 state-space stochastic rounding);
+ * v requantised per recipe (ZIP-SR: Dyn4 with preconditioner-space SR;
+ * ZE-EDEN: Dyn4-NZ RTN and the EDEN scale |y|^2/<y,yhat> folded into s_v;
+ * factored: 1-D tensors Dyn4-NZ RTN, rank >= 2 tensors update R and C).
+ * Stochastic rounding draws Philox4x32-10 keyed by (seed, step, tensor_id,
+ * elem_offset + element index); results do not depend on launch geometry.
+ *
+ * workspace: device memory of at least q4adamw_workspace_bytes() bytes,
+ * 256-B aligned, not used concurrently by another call.  The host tensor
+ * array t is read during the call only.  Tensors must not overlap.
+ */
+int q4adamw_step(const q4adamw_tensor_t* t, int n, float lr, float beta1, float beta2, float eps, float weight_decay,
+                 int64_t step, uint64_t seed, int recipe, uint32_t flags, void* workspace, int64_t workspace_bytes,
+                 void* stream);
+
+/*
+ * Decode the state of one tensor into FP32 device buffers of numel floats
+ * (either may be NULL): m_out = NF4[qm]*s_m; v_out = V[qv]*s_v for packed v
+ * (V = Dyn4 for ZIP-SR, Dyn4-NZ otherwise) or R_i*C_j/mean(R) for a factored
+ * tensor.  Asynchronous on stream.
+ */
+int q4adamw_dequant_state(const q4adamw_tensor_t* t, int recipe, float* m_out, float* v_out, void* stream);
+
+/*
+ * The library's own codebook tables (host-only).  which: 0 = NF4, 1 = Dyn4
+ * (zero-inclusive), 2 = Dyn4-NZ (zero-excluding).  levels: 16 ascending FP32
+ * levels; thresholds: the 15 FP32 RTN decision points (rounded double
+ * midpoints).  Either pointer may be NULL.
+ */
+int q4adamw_codebook(int which, float* levels, float* thresholds);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* Q4ADAMW_H */

@@ -1,0 +1,230 @@
+"""Pins of the oracle's full step: the unquantised reduction to textbook AdamW,
+the step's composition (what gets quantised, with which scale), the EDEN
+closed form, the factored statistics, storage arithmetic and the
+independence of the random draws from sharding.
+"""
+import os
+
+import numpy as np
+import pytest
+import torch
+
+from oracle import oracle as O
+
+H = dict(lr=1e-3, beta1=0.9, beta2=0.999, eps=1e-8, wd=0.1)
+GOLD = os.path.join(os.path.dirname(__file__), "golden", "storage_numbers.txt")
+
+
+def _f32(x):
+    return np.float32(x)
+
+
+def _bf16(x):
+    return torch.from_numpy(np.asarray(x, np.float32)).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+
+
+def _from_bf16(h):
+    return (np.asarray(h, np.uint16).astype(np.uint32) << 16).view(np.float32)
+
+
+def test_unquantised_step_matches_torch_adamw():
+    rng = np.random.default_rng(0)
+    n = 3000
+    theta0 = rng.normal(0, 0.02, n).astype(np.float32)
+    p = torch.nn.Parameter(torch.from_numpy(theta0.copy()))
+    opt = torch.optim.AdamW([p], lr=_f32(H["lr"]).item(), betas=(_f32(0.9).item(), _f32(0.999).item()),
+                            eps=_f32(1e-8).item(), weight_decay=_f32(0.1).item(), foreach=False)
+    th = theta0.copy()
+    m = np.zeros(n, np.float32)
+    v = np.zeros(n, np.float32)
+    for t in range(1, 11):
+        g = rng.normal(0, 1e-3, n).astype(np.float32)
+        p.grad = torch.from_numpy(g.copy())
+        opt.step()
+        O.adamw_fp32(th, g, m, v, H["lr"], H["beta1"], H["beta2"], H["eps"], H["wd"], t)
+        ref = p.detach().numpy()
+        assert np.all(np.abs(th - ref) <= 1e-6 * np.maximum(1, np.abs(ref))), t
+
+
+def test_unquantised_step_matches_float64_closed_form():
+    rng = np.random.default_rng(1)
+    n = 500
+    th = rng.normal(0, 0.02, n).astype(np.float32)
+    th64 = th.astype(np.float64)
+    m = np.zeros(n, np.float32); v = np.zeros(n, np.float32)
+    m64 = np.zeros(n); v64 = np.zeros(n)
+    lr, b1, b2, eps, wd = (float(_f32(H[k])) for k in ("lr", "beta1", "beta2", "eps", "wd"))
+    for t in range(1, 21):
+        g = rng.normal(0, 1e-2, n).astype(np.float32)
+        O.adamw_fp32(th, g, m, v, H["lr"], H["beta1"], H["beta2"], H["eps"], H["wd"], t)
+        m64 = b1 * m64 + (1 - b1) * g
+        v64 = b2 * v64 + (1 - b2) * g.astype(np.float64) ** 2
+        mh = m64 / (1 - b1 ** t)
+        vh = v64 / (1 - b2 ** t)
+        th64 = th64 * (1 - lr * wd) - lr * mh / (np.sqrt(vh) + eps)
+    assert np.max(np.abs(th - th64)) < 2e-6
+
+
+def _one_tensor_steps(recipe, numel, steps, grads_fn, rows=1, flags=0, call_flags=0, first=1, seed=0):
+    rng = np.random.default_rng(42)
+    theta0 = rng.normal(0, 0.02, numel).astype(np.float32)
+    t = O.OracleTensor.zeros_state(theta0, tensor_id=5, rows=rows, flags=flags, recipe=recipe)
+    for k in range(steps):
+        t.step(grads_fn(k), H["lr"], H["beta1"], H["beta2"], H["eps"], H["wd"], first + k, seed, recipe,
+               call_flags)
+    return theta0, t
+
+
+@pytest.mark.parametrize("recipe", ["zip_sr", "ze_eden"])
+def test_first_step_update_is_textbook_adamw(recipe):
+    # From the zero state the first update uses exact moments, so theta after
+    # step 1 equals torch.optim.AdamW's first step.
+    rng = np.random.default_rng(7)
+    n = 1000
+    g = _bf16(rng.normal(0, 1e-3, n))
+    theta0, t = _one_tensor_steps(recipe, n, 1, lambda k: g)
+    p = torch.nn.Parameter(torch.from_numpy(theta0.copy()))
+    opt = torch.optim.AdamW([p], lr=_f32(1e-3).item(), betas=(_f32(0.9).item(), _f32(0.999).item()),
+                            eps=_f32(1e-8).item(), weight_decay=_f32(0.1).item(), foreach=False)
+    p.grad = torch.from_numpy(_from_bf16(g).copy())
+    opt.step()
+    ref = p.detach().numpy()
+    assert np.all(np.abs(t.param - ref) <= 1e-6 * np.maximum(1, np.abs(ref)))
+    assert np.array_equal(t.param_bf16, _bf16(t.param))
+
+
+def test_first_step_state_is_nearest_level_of_the_moments():
+    # After step 1: m' = (1-b1) g, v' = (1-b2) g^2 (float64 restatement); the
+    # stored m is the nearest NF4 level of m' at scale max|m'| per block, the
+    # stored v (ZE-EDEN) the nearest Dyn4-NZ level at scale max v'.
+    rng = np.random.default_rng(8)
+    n = 1000
+    g = _bf16(rng.normal(0, 1e-3, n))
+    gf = _from_bf16(g).astype(np.float64)
+    _, t = _one_tensor_steps("ze_eden", n, 1, lambda k: g)
+    h = O.host_scalars(H["lr"], H["beta1"], H["beta2"], H["wd"], 1)
+    m1 = np.float32(h["omb1"]) * gf
+    v1 = np.float32(h["omb2"]) * gf * gf
+    cb = O.codebooks()
+    for b in range(O.nblocks(n)):
+        sl = slice(128 * b, min(128 * b + 128, n))
+        sm = np.abs(m1[sl]).max()
+        assert abs(t.m_scale[b] - sm) <= 1e-6 * sm
+        qm = np.array([(t.m_codes[e >> 1] >> (4 * (e & 1))) & 15 for e in range(sl.start, sl.stop)])
+        dm = np.abs(m1[sl][:, None] - cb["nf4"][None, :].astype(np.float64) * sm)
+        assert np.all(dm[np.arange(qm.size), qm] <= dm.min(1) + 1e-6 * sm)
+        sv = v1[sl].max()
+        qv = np.array([(t.v_codes[e >> 1] >> (4 * (e & 1))) & 15 for e in range(sl.start, sl.stop)])
+        dv = np.abs(v1[sl][:, None] - cb["dyn4nz"][None, :].astype(np.float64) * sv)
+        assert np.all(dv[np.arange(qv.size), qv] <= dv.min(1) + 1e-6 * sv)
+        # EDEN: stored scale = s * |y|^2 / <y, L[q]>, y = v'/s (float64 closed form)
+        y = v1[sl] / sv
+        eden = sv * np.dot(y, y) / np.dot(y, cb["dyn4nz"][qv].astype(np.float64))
+        assert abs(t.v_scale[b] - eden) <= 2e-6 * eden
+
+
+def test_eden_scale_closed_form_and_identity():
+    L = O.codebooks()["dyn4nz"]
+    t = O.codebooks()["dyn4nz_t"]
+    rng = np.random.default_rng(4)
+    for trial in range(100):
+        n = int(rng.integers(1, 129))
+        v = (rng.random(n) ** 4).astype(np.float32) * np.float32(10.0 ** rng.uniform(-12, 3))
+        q, s = O.quant_block(L, t, v, "state_rtn")
+        got = O.eden_scale(v, q, L, s)
+        y = v.astype(np.float64) * float(np.float32(1) / s)
+        ref = float(s) * np.dot(y, y) / np.dot(y, L[q].astype(np.float64))
+        assert abs(got - ref) <= 2e-6 * ref
+    # values on levels at a power-of-two scale: EDEN factor exactly 1
+    for s in (1.0, 2.0 ** -30):
+        v = (L * np.float32(s)).astype(np.float32)
+        q, sc = O.quant_block(L, t, v, "state_rtn")
+        assert O.eden_scale(v, q, L, sc) == np.float32(s)
+    z = np.zeros(128, np.float32)
+    assert O.eden_scale(z, np.zeros(128, np.uint8), L, np.float32(0)) == 0
+
+
+def test_factored_statistics_brute_force():
+    rows, cols = 24, 40
+    rng = np.random.default_rng(5)
+    gs = [_bf16(rng.normal(0, 1e-2, rows * cols) * rng.random(rows * cols)) for _ in range(3)]
+    _, t = _one_tensor_steps("factored", rows * cols, 3, lambda k: gs[k], rows=rows, flags=O.T_FACTORED)
+    b2 = float(_f32(0.999))
+    R = np.zeros(rows); C = np.zeros(cols)
+    for g in gs:
+        g2 = _from_bf16(g).astype(np.float64).reshape(rows, cols) ** 2
+        R = b2 * R + (1 - b2) * g2.mean(1)
+        C = b2 * C + (1 - b2) * g2.mean(0)
+    assert np.allclose(t.v_row, R, rtol=1e-5, atol=0)
+    assert np.allclose(t.v_col, C, rtol=1e-5, atol=0)
+    assert t.v_codes is None
+
+
+def test_factored_rank1_reconstruction_is_exact():
+    # If g^2 is rank-1 (g_ij = a_i b_j) then R_i C_j / mean(R) = (1-b2) g_ij^2 after step 1.
+    rows, cols = 16, 32
+    a = 2.0 ** np.arange(-4, 12, dtype=np.float64)[:rows] * 1e-4
+    b = 2.0 ** (np.arange(cols) % 5 - 2.0)
+    g = _bf16((a[:, None] * b[None, :]).reshape(-1))
+    _, t = _one_tensor_steps("factored", rows * cols, 1, lambda k: g, rows=rows, flags=O.T_FACTORED)
+    vhat = t.v_dequant("factored").astype(np.float64)
+    ref = (1 - float(_f32(0.999))) * _from_bf16(g).astype(np.float64) ** 2
+    assert np.allclose(vhat, ref, rtol=2e-6, atol=0)
+
+
+def test_storage_is_1p0625_bytes_per_param():
+    gold = {}
+    for line in open(GOLD):
+        line = line.strip()
+        if line and not line.startswith("#"):
+            k, v = line.split()
+            gold[k] = float(v)
+    n = 128 * 1000
+    t = O.OracleTensor.zeros_state(np.zeros(n, np.float32), 0, recipe="zip_sr")
+    state = t.m_codes.nbytes + t.v_codes.nbytes + t.m_scale.nbytes + t.v_scale.nbytes
+    assert state / n == gold["bytes_per_param_4bit"]
+    assert O.BLOCK == gold["block_size"]
+    assert round(gold["bytes_per_param_fp32_two_buffers"] / (state / n), 2) == gold["reduction_factor"]
+
+
+@pytest.mark.parametrize("recipe", ["zip_sr", "ze_eden"])
+def test_draws_independent_of_sharding(recipe):
+    # A tensor split into two block-aligned shards (elem_offset) steps exactly
+    # like the whole tensor: draws depend only on the global element index.
+    rng = np.random.default_rng(9)
+    n, cut = 128 * 7 + 50, 128 * 3
+    theta0 = rng.normal(0, 0.02, n).astype(np.float32)
+    whole = O.OracleTensor.zeros_state(theta0, 3, flags=O.T_LM_HEAD, recipe=recipe)
+    a = O.OracleTensor.zeros_state(theta0[:cut], 3, flags=O.T_LM_HEAD, elem_offset=0, recipe=recipe)
+    b = O.OracleTensor.zeros_state(theta0[cut:], 3, flags=O.T_LM_HEAD, elem_offset=cut, recipe=recipe)
+    for k in range(1, 6):
+        g = _bf16(rng.normal(0, 1e-3, n))
+        for obj, gg in ((whole, g), (a, g[:cut]), (b, g[cut:])):
+            obj.step(gg, H["lr"], H["beta1"], H["beta2"], H["eps"], H["wd"], k, 123, recipe, O.LM_HEAD_SR_ACTIVE)
+    assert np.array_equal(whole.param, np.concatenate([a.param, b.param]))
+    assert np.array_equal(whole.m_codes, np.concatenate([a.m_codes, b.m_codes]))
+    assert np.array_equal(whole.v_codes, np.concatenate([a.v_codes, b.v_codes]))
+    assert np.array_equal(whole.v_scale, np.concatenate([a.v_scale, b.v_scale]))
+
+
+def test_lm_head_sr_only_when_active_and_flagged():
+    rng = np.random.default_rng(10)
+    n = 128 * 4
+    gs = [_bf16(rng.normal(0, 1e-3, n)) for _ in range(3)]
+    res = {}
+    for flags, cf in ((0, 0), (O.T_LM_HEAD, 0), (0, O.LM_HEAD_SR_ACTIVE), (O.T_LM_HEAD, O.LM_HEAD_SR_ACTIVE)):
+        _, t = _one_tensor_steps("zip_sr", n, 3, lambda k: gs[k], flags=flags, call_flags=cf)
+        res[(flags, cf)] = t.m_codes.copy()
+    base = res[(0, 0)]
+    assert np.array_equal(res[(O.T_LM_HEAD, 0)], base)
+    assert np.array_equal(res[(0, O.LM_HEAD_SR_ACTIVE)], base)
+    assert not np.array_equal(res[(O.T_LM_HEAD, O.LM_HEAD_SR_ACTIVE)], base)
+
+
+def test_partial_block_padding_codes_are_zero():
+    n = 128 + 37
+    rng = np.random.default_rng(11)
+    _, t = _one_tensor_steps("zip_sr", n, 2, lambda k: _bf16(rng.normal(0, 1e-3, n)))
+    codes_m = np.stack([t.m_codes & 15, t.m_codes >> 4], 1).reshape(-1)
+    codes_v = np.stack([t.v_codes & 15, t.v_codes >> 4], 1).reshape(-1)
+    assert np.all(codes_m[n:] == 0) and np.all(codes_v[n:] == 0)
