@@ -1,0 +1,408 @@
+#!/usr/bin/env python3
+"""Benchmark of the fused 4-bit AdamW optimizer step on B300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl ours|reference]
+
+Default workload: the Llama-style 8B parameter set (291 tensors,
+8,030,261,248 FP32 master weights, BF16 gradients, 4-bit ZIP-SR state, about
+73 GB resident in HBM).  One step = one q4adamw_step over every tensor.  The
+timed region holds exactly K steps, bracketed by a barrier and
+torch.cuda.synchronize(); each step's working set (113 GB) exceeds the 126 MB
+L2, so no flush is needed between steps.  Rank 0 prints one JSON line.
+
+Metric: optimizer-step parameters per second (whole job); the roofline object
+reports achieved HBM GB/s of the step kernel against the measured copy peak.
+Algorithmic bytes per parameter: 2 (BF16 grad read) + 4 + 4 (FP32 master read
+and write) + 2 (BF16 weight write) + 2 x 1.0625 (packed m+v codes and block
+scales, read and written) = 14.125.
+
+--impl reference times the CPU oracle (oracle/, single thread) on a bounded
+sample of the same workload: it is the reference arm of this benchmark.
+Multi-GPU (torchrun, one rank per GPU): every rank runs an independent replica
+of the workload on its own GPU (weak scaling; the step has no data-path
+collective).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+BYTES_PER_PARAM = 2 + 4 + 4 + 2 + 2 * 1.0625           # packed (non-factored) tensors
+BYTES_PER_PARAM_FACTORED = 2 + 4 + 4 + 2 + 2 * 0.53125  # rank >= 2 tensors, factored v (m only)
+NOMINAL_HBM_GBS = 8000.0
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--workload", default="llama8b_zipsr")
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--e2e-steps", type=int, default=3)
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=12.0, help="target oracle time of the CPU sample")
+    return ap.parse_args()
+
+
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    return 6400.0, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled every 200 ms."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+        self.thread = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        if self.thread:
+            self.thread.join(timeout=2)
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [x.strip() for x in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax.append(float(parts[2]))
+            except ValueError:
+                continue
+            for name, val in zip(names, parts[5:9]):
+                if val.lower().startswith("active"):
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def kernel_source_hash() -> str:
+    p = os.path.join(ROOT, "bit_quantized_adamw_q4adamw_b300", "csrc", "q4_step.cu")
+    with open(p, "rb") as f:
+        return hashlib.sha256(f.read()).hexdigest()[:16]
+
+
+def traffic_record(workload: str):
+    """DRAM bytes per parameter of the step kernel from a committed ncu summary
+    (profiles/step_kernel_traffic.json), valid only for the kernel source it was
+    taken on."""
+    p = os.path.join(ROOT, "profiles", "step_kernel_traffic.json")
+    if not os.path.exists(p):
+        return None
+    with open(p) as f:
+        d = json.load(f)
+    rec = d.get(workload)
+    if not rec or rec.get("kernel_sha") != kernel_source_hash():
+        return None
+    return rec
+
+
+# ---------------------------------------------------------------- workload setup
+def build_state(w, device):
+    import torch
+
+    import bit_quantized_adamw_q4adamw_b300 as q4
+    from bit_quantized_adamw_q4adamw_b300 import workloads as W
+    st = q4.Q4State(w.tensors, w.recipe, device=device)
+    for i, s in enumerate(w.tensors):
+        st.view(i, "param").copy_(W.init_param(s, i, device=device))
+        W.draw_grad(w, s, i, w.first_step, device=device, out=st.view(i, "grad"))
+    st.init()
+    torch.cuda.synchronize()
+    return st
+
+
+def algorithmic_bytes(st, recipe) -> float:
+    total = 0.0
+    for sl in st.slots:
+        if st.is_factored(sl):
+            total += sl.numel * BYTES_PER_PARAM_FACTORED + (sl.rows + sl.numel // sl.rows) * 8
+        else:
+            total += sl.numel * BYTES_PER_PARAM
+    return total
+
+
+def launches_per_step(st) -> int:
+    return 1 + (4 if any(st.is_factored(s) for s in st.slots) else 0)
+
+
+# ---------------------------------------------------------------- CPU oracle sample
+def oracle_sample(w, target_seconds: float, device_gen: str = "cpu"):
+    """Time the oracle on a bounded, block-aligned sample of the workload.
+
+    The sample takes whole-tensor prefixes (multiples of 128 elements) in
+    workload order, sized from a short probe so that the timed oracle work lasts
+    about target_seconds.  Inputs are drawn with the same generators on the CPU.
+    Returns (params_per_second, sample_description, params)."""
+    import numpy as np
+    import torch
+
+    from bit_quantized_adamw_q4adamw_b300 import workloads as W
+    from oracle import oracle as O
+    h = W.HYPER
+    flags = O.LM_HEAD_SR_ACTIVE if w.lm_head_sr else 0
+
+    def run(n_target):
+        done, secs, parts = 0, 0.0, []
+        for i, s in enumerate(w.tensors):
+            if done >= n_target:
+                break
+            take = min(s.numel, ((n_target - done + 127) // 128) * 128)
+            if st_factored(w, s):
+                take = s.numel  # factored statistics need the whole tensor
+            th = W.init_param(s, i, n=take).numpy()
+            g = W.draw_grad(w, s, i, w.first_step, n=take)
+            gb = g.view(torch.int16).numpy().view(np.uint16)
+            t = O.OracleTensor.zeros_state(th, i, rows=s.rows if take == s.numel else 1, flags=s.flags,
+                                           recipe=w.recipe)
+            t0 = time.perf_counter()
+            t.step(gb, h["lr"], h["beta1"], h["beta2"], h["eps"], h["weight_decay"], w.first_step, 0, w.recipe,
+                   flags)
+            secs += time.perf_counter() - t0
+            done += take
+            parts.append(f"{s.name}[:{take}]")
+        return done, secs, parts
+
+    def st_factored(w, s):
+        return w.recipe == "factored" and bool(s.flags & W.T_FACTORED)
+
+    n0, s0, _ = run(2_000_000)
+    rate = n0 / max(s0, 1e-9)
+    n_target = int(min(max(rate * target_seconds, 1_000_000), w.numel))
+    n, secs, parts = run(n_target)
+    desc = (f"first {n} of {w.numel} params of {w.name} in tensor order "
+            f"({len(parts)} tensor prefixes), one step t={w.first_step}")
+    return n / secs, desc, n, secs
+
+
+# ---------------------------------------------------------------- arms
+def run_reference(args, rank, world):
+    from bit_quantized_adamw_q4adamw_b300 import workloads as W
+    if rank != 0:
+        return
+    w = W.WORKLOADS[args.workload]
+    per_step = max(args.cpu_seconds / max(args.steps, 1), 0.5)
+    vals, secs_total, desc, n = [], 0.0, "", 0
+    for k in range(args.warmup + args.steps):
+        v, desc, n, secs = oracle_sample(w, per_step if k >= args.warmup else 0.2)
+        if k >= args.warmup:
+            vals.append(v)
+            secs_total += secs
+    value = len(vals) * n / secs_total if secs_total > 0 else 0.0
+    line = {
+        "impl": "reference", "metric": "optimizer-step params/sec", "value": value, "unit": "params/s",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": 1e3 * w.numel / value if value else None, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": {"workload": w.name, "params": w.numel, "tensors": len(w.tensors), "recipe": w.recipe},
+        "cpu_baseline": {"value": value, "unit": "params/s", "cores": 1, "kind": "oracle",
+                         "sample": f"each step: {desc}"},
+        "e2e": {"value": value, "unit": "params/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def run_ours(args, rank, world, local):
+    import torch
+    import torch.distributed as dist
+
+    from bit_quantized_adamw_q4adamw_b300 import workloads as W
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    w = W.WORKLOADS[args.workload]
+    h = W.HYPER
+    flags = 1 if w.lm_head_sr else 0
+    st = build_state(w, dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def one_step(t):
+        st.step(t, h["lr"], h["beta1"], h["beta2"], h["eps"], h["weight_decay"], seed=0, flags=flags, stream=stream)
+
+    t = w.first_step
+    for _ in range(args.warmup):
+        one_step(t)
+        t += 1
+    torch.cuda.synchronize()
+
+    sampler = ClockSampler(local) if rank == 0 else None
+    if sampler:
+        sampler.start()
+        time.sleep(0.5)
+    evs = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps + 1)]
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    evs[0].record(stream)
+    for k in range(args.steps):
+        one_step(t)
+        t += 1
+        evs[k + 1].record(stream)
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    clocks = sampler.stop() if sampler else None
+    per = [evs[k].elapsed_time(evs[k + 1]) for k in range(args.steps)]
+    total_ms = evs[0].elapsed_time(evs[-1])
+    if world > 1:
+        tt = torch.tensor([total_ms], device=dev)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        total_ms = float(tt.item())
+    ms_per_step = total_ms / args.steps
+    value = world * w.numel * args.steps / (total_ms / 1e3)
+
+    # end to end through the public API with host buffers
+    e2e = None
+    if not args.no_e2e and args.e2e_steps > 0:
+        e2e = run_e2e(args, st, w, dev, stream, t)
+        t += args.e2e_steps + 1
+
+    if rank != 0:
+        return
+    alg = algorithmic_bytes(st, w.recipe)
+    peak, peak_kind = peaks()
+    mean_ms = statistics.mean(per)
+    achieved = alg / (mean_ms / 1e3) / 1e9
+    tr = traffic_record(w.name)
+    line = {
+        "metric": "optimizer-step params/sec", "value": value, "unit": "params/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": {"workload": w.name, "params": w.numel, "tensors": len(w.tensors), "recipe": w.recipe,
+                   "lm_head_sr": w.lm_head_sr, "parallelism": f"replicas{world}",
+                   "l2": f"inputs larger than L2 ({alg / 1e9:.1f} GB per step)",
+                   "step_ms_median": statistics.median(per), "step_ms_p10": sorted(per)[len(per) // 10],
+                   "step_ms_p90": sorted(per)[min(len(per) - 1, (9 * len(per)) // 10)]},
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
+                     "peak_kind": f"{peak_kind} copy bandwidth (MEASURED_PEAKS.json hbm_gbs)"
+                     if peak_kind == "measured" else "fallback 6.4 TB/s",
+                     "traffic": (tr["dram_bytes_per_param"] * w.numel) if tr else None,
+                     "algorithmic_bytes": alg, "kernel": "step_kernel (one launch per step)",
+                     "frac_of_nominal_8tbs": achieved / NOMINAL_HBM_GBS},
+        "gpu_launches": launches_per_step(st) * args.steps,
+        "clocks": clocks,
+    }
+    if e2e:
+        line["e2e"] = e2e
+    if not args.no_cpu_baseline:
+        v, desc, n, secs = oracle_sample(w, args.cpu_seconds)
+        line["cpu_baseline"] = {"value": v, "unit": "params/s", "cores": 1, "kind": "oracle",
+                                "sample": f"{desc}; {secs:.1f} s single-threaded"}
+    print(json.dumps(line), flush=True)
+
+
+def run_e2e(args, st, w, dev, stream, t0):
+    """Same metric through the public API with host buffers: per step, copy the
+    BF16 gradients from pinned host memory, run q4adamw_step, copy the BF16
+    weights back to pinned host memory."""
+    import torch
+    h = W_HYPER()
+    n = st.grad.numel()
+    try:
+        g_host = torch.empty(n, dtype=torch.bfloat16, pin_memory=True)
+        out_host = torch.empty(n, dtype=torch.bfloat16, pin_memory=True)
+    except RuntimeError as e:
+        return {"value": None, "unit": "params/s", "error": f"pinned allocation failed: {e}"[:200]}
+    g_host.copy_(st.grad)
+    torch.cuda.synchronize()
+    flags = 1 if w.lm_head_sr else 0
+    t = t0
+    # one untimed round trip
+    st.grad.copy_(g_host, non_blocking=True)
+    st.step(t, h["lr"], h["beta1"], h["beta2"], h["eps"], h["weight_decay"], 0, flags, stream)
+    out_host.copy_(st.param_bf16, non_blocking=True)
+    torch.cuda.synchronize()
+    t += 1
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    ev0.record(stream)
+    for _ in range(args.e2e_steps):
+        st.grad.copy_(g_host, non_blocking=True)
+        st.step(t, h["lr"], h["beta1"], h["beta2"], h["eps"], h["weight_decay"], 0, flags, stream)
+        out_host.copy_(st.param_bf16, non_blocking=True)
+        t += 1
+    ev1.record(stream)
+    torch.cuda.synchronize()
+    ms = ev0.elapsed_time(ev1) / args.e2e_steps
+    return {"value": w.numel / (ms / 1e3), "unit": "params/s", "h2d_bytes_per_step": 2 * n,
+            "d2h_bytes_per_step": 2 * n, "ms_per_step": ms, "steps": args.e2e_steps}
+
+
+def W_HYPER():
+    from bit_quantized_adamw_q4adamw_b300 import workloads as W
+    return W.HYPER
+
+
+def main():
+    args = parse()
+    rank, world, local = dist_env()
+    if world > 1:
+        import torch.distributed as dist
+        backend = "gloo" if args.impl == "reference" else "nccl"
+        if backend == "nccl":
+            import torch
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend=backend)
+    try:
+        if args.impl == "reference":
+            run_reference(args, rank, world)
+        else:
+            run_ours(args, rank, world, local)
+    finally:
+        if world > 1:
+            import torch.distributed as dist
+            dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,381 @@
+// C ABI of the q4adamw library: validation, host scalars, workspace layout,
+// descriptor upload and kernel launches.  See include/q4adamw.h.
+#include <cuda_runtime.h>
+
+#include <cmath>
+#include <cstring>
+#include <mutex>
+#include <new>
+#include <vector>
+
+#include "q4_internal.h"
+
+namespace {
+
+using q4::DevTensor;
+
+thread_local int g_last_cuda = 0;
+
+int cuda_fail(cudaError_t e) {
+    g_last_cuda = (int)e;
+    return Q4_ECUDA;
+}
+
+bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
+
+int64_t nblocks(int64_t numel) { return (numel + q4::kBlock - 1) / q4::kBlock; }
+
+bool is_factored(const q4adamw_tensor_t& t, int recipe) {
+    return recipe == Q4_RECIPE_FACTORED && (t.flags & Q4_T_FACTORED);
+}
+
+int check_recipe(int recipe) {
+    return (recipe == Q4_RECIPE_ZIP_SR || recipe == Q4_RECIPE_ZE_EDEN || recipe == Q4_RECIPE_FACTORED)
+               ? Q4_OK
+               : Q4_ERECIPE;
+}
+
+// Shape-only checks (host-only entry points).
+int check_shape(const q4adamw_tensor_t& t, int recipe) {
+    if (t.numel < 0) return Q4_ESHAPE;
+    if (t.elem_offset % q4::kBlock) return Q4_ESHAPE;
+    if (is_factored(t, recipe)) {
+        if (t.rows < 1 || (t.numel > 0 && t.numel % t.rows)) return Q4_ESHAPE;
+    }
+    return Q4_OK;
+}
+
+// Full pointer checks for calls that touch device memory.
+int check_tensor(const q4adamw_tensor_t& t, int recipe, bool need_grad) {
+    int rc = check_shape(t, recipe);
+    if (rc) return rc;
+    if (t.numel == 0) return Q4_OK;
+    if (!t.param || !t.m_codes || !t.m_scale) return Q4_EINVAL;
+    if (need_grad && !t.grad) return Q4_EINVAL;
+    if (!aligned(t.param, 16) || !aligned(t.m_codes, 16) || !aligned(t.m_scale, 4)) return Q4_EALIGN;
+    if (t.grad && !aligned(t.grad, 16)) return Q4_EALIGN;
+    if (t.param_bf16 && !aligned(t.param_bf16, 16)) return Q4_EALIGN;
+    if (is_factored(t, recipe)) {
+        if (!t.v_row || !t.v_col) return Q4_EINVAL;
+        if (!aligned(t.v_row, 4) || !aligned(t.v_col, 4)) return Q4_EALIGN;
+    } else {
+        if (!t.v_codes || !t.v_scale) return Q4_EINVAL;
+        if (!aligned(t.v_codes, 16) || !aligned(t.v_scale, 4)) return Q4_EALIGN;
+    }
+    return Q4_OK;
+}
+
+int64_t round_up(int64_t x, int64_t a) { return (x + a - 1) / a * a; }
+
+// Workspace layout, all offsets 256-B aligned.
+struct Layout {
+    int64_t desc, pairs, rows, tiles, cols, fids;  // uploaded part
+    int64_t upload_bytes;
+    int64_t rbar, colpart;                         // device-only part
+    int64_t total;
+    int n_factored;
+    int64_t colpart_floats;
+};
+
+int64_t n_slabs(int64_t rows) { return (rows + q4::kSlabRows - 1) / q4::kSlabRows; }
+int64_t n_segs(int64_t cols) { return (cols + q4::kSegCols - 1) / q4::kSegCols; }
+
+Layout make_layout(const q4adamw_tensor_t* t, int n, int recipe) {
+    Layout L{};
+    int64_t off = 0;
+    L.desc = off;  off = round_up(off + (int64_t)n * (int64_t)sizeof(DevTensor), 256);
+    L.pairs = off; off = round_up(off + (int64_t)(n + 1) * 8, 256);
+    L.rows = off;  off = round_up(off + (int64_t)(n + 1) * 8, 256);
+    L.tiles = off; off = round_up(off + (int64_t)(n + 1) * 8, 256);
+    L.cols = off;  off = round_up(off + (int64_t)(n + 1) * 8, 256);
+    L.fids = off;  off = round_up(off + (int64_t)(n > 0 ? n : 1) * 4, 256);
+    L.upload_bytes = off;
+    L.rbar = off;  off = round_up(off + (int64_t)(n > 0 ? n : 1) * 4, 256);
+    L.colpart = off;
+    int64_t cp = 0;
+    for (int i = 0; i < n; ++i) {
+        if (is_factored(t[i], recipe) && t[i].numel > 0) {
+            L.n_factored++;
+            cp += n_slabs(t[i].rows) * (t[i].numel / t[i].rows);
+        }
+    }
+    L.colpart_floats = cp;
+    off = round_up(off + cp * 4, 256);
+    L.total = off;
+    return L;
+}
+
+// Host scalars of step t, each computed in double and rounded once to FP32.
+struct Scalars {
+    float c2, step_size, decay, omb1, omb2;
+};
+Scalars host_scalars(float lr, float beta1, float beta2, float wd, int64_t step) {
+    const double dlr = lr, d1 = beta1, d2 = beta2, dwd = wd;
+    const double bc1 = 1.0 - std::pow(d1, (double)step);
+    const double bc2 = 1.0 - std::pow(d2, (double)step);
+    Scalars s;
+    s.c2 = (float)(1.0 / std::sqrt(bc2));
+    s.step_size = (float)(dlr / bc1);
+    s.decay = (float)(1.0 - dlr * dwd);
+    s.omb1 = (float)(1.0 - d1);
+    s.omb2 = (float)(1.0 - d2);
+    return s;
+}
+
+q4::Tables* g_tabs[3] = {nullptr, nullptr, nullptr};
+std::once_flag g_tabs_once;
+
+void build_all_tables() {
+    for (int vb = 1; vb <= 2; ++vb) {
+        q4::Tables* t = new (std::nothrow) q4::Tables;
+        if (t && q4::build_tables(vb, t)) g_tabs[vb] = t;
+        else delete t;
+    }
+}
+
+// One immutable table set per v codebook (1 = Dyn4, 2 = Dyn4-NZ), built once.
+q4::Tables* tables_for(int recipe) {
+    std::call_once(g_tabs_once, build_all_tables);
+    return g_tabs[recipe == Q4_RECIPE_ZIP_SR ? 1 : 2];
+}
+
+DevTensor make_dev(const q4adamw_tensor_t& t, int recipe, uint32_t call_flags) {
+    DevTensor d{};
+    d.param = t.param;
+    d.grad = t.grad;
+    d.bf16 = t.param_bf16;
+    d.mc = t.m_codes;
+    d.ms = t.m_scale;
+    d.vc = t.v_codes;
+    d.vs = t.v_scale;
+    d.vrow = t.v_row;
+    d.vcol = t.v_col;
+    d.numel = t.numel;
+    d.rows = t.rows < 1 ? 1 : t.rows;
+    d.cols = (t.numel > 0) ? t.numel / d.rows : 0;
+    d.elem_offset = t.elem_offset;
+    d.tensor_id = t.tensor_id;
+    d.flags = 0;
+    if ((t.flags & Q4_T_LM_HEAD) && (call_flags & Q4_LM_HEAD_SR_ACTIVE)) d.flags |= q4::DF_M_SR;
+    if (is_factored(t, recipe)) d.flags |= q4::DF_FACTORED;
+    if (t.param_bf16) d.flags |= q4::DF_BF16;
+    return d;
+}
+
+}  // namespace
+
+extern "C" {
+
+int q4adamw_version(void) { return Q4ADAMW_STATE_FORMAT; }
+
+const char* q4adamw_strerror(int status) {
+    switch (status) {
+        case Q4_OK: return "ok";
+        case Q4_EINVAL: return "invalid argument";
+        case Q4_EALIGN: return "misaligned pointer";
+        case Q4_ESHAPE: return "invalid tensor shape";
+        case Q4_ERECIPE: return "unknown recipe or codebook";
+        case Q4_EVERSION: return "state header does not match this optimizer state format or recipe";
+        case Q4_ECUDA: return "CUDA runtime error";
+        case Q4_EWORKSPACE: return "workspace missing, too small or misaligned";
+        default: return "unknown status";
+    }
+}
+
+int q4adamw_last_cuda_error(void) { return g_last_cuda; }
+
+int q4adamw_state_bytes(const q4adamw_tensor_t* t, int n, int recipe, int64_t* quantized, int64_t* scale_meta,
+                        int64_t* total) {
+    if (n < 0 || (n > 0 && !t)) return Q4_EINVAL;
+    if (int rc = check_recipe(recipe)) return rc;
+    int64_t q = 0, s = 0;
+    for (int i = 0; i < n; ++i) {
+        if (int rc = check_shape(t[i], recipe)) return rc;
+        const int64_t nb = nblocks(t[i].numel);
+        q += nb * 64;  // m codes
+        s += nb * 4;   // m scales
+        if (is_factored(t[i], recipe)) {
+            if (t[i].numel > 0) s += (t[i].rows + t[i].numel / t[i].rows) * 4;
+        } else {
+            q += nb * 64;
+            s += nb * 4;
+        }
+    }
+    if (quantized) *quantized = q;
+    if (scale_meta) *scale_meta = s;
+    if (total) *total = q + s;
+    return Q4_OK;
+}
+
+int q4adamw_workspace_bytes(const q4adamw_tensor_t* t, int n, int recipe, int64_t* bytes) {
+    if (n < 0 || (n > 0 && !t) || !bytes) return Q4_EINVAL;
+    if (int rc = check_recipe(recipe)) return rc;
+    for (int i = 0; i < n; ++i)
+        if (int rc = check_shape(t[i], recipe)) return rc;
+    *bytes = make_layout(t, n, recipe).total;
+    return Q4_OK;
+}
+
+int q4adamw_header_check(const q4adamw_header_t* h, int recipe) {
+    if (!h) return Q4_EINVAL;
+    if (h->magic != Q4ADAMW_MAGIC || h->format != Q4ADAMW_STATE_FORMAT || h->block != Q4ADAMW_BLOCK ||
+        h->recipe != (uint32_t)recipe)
+        return Q4_EVERSION;
+    return Q4_OK;
+}
+
+int q4adamw_state_init(const q4adamw_tensor_t* t, int n, int recipe, q4adamw_header_t* header_out, void* stream) {
+    if (n < 0 || (n > 0 && !t)) return Q4_EINVAL;
+    if (int rc = check_recipe(recipe)) return rc;
+    for (int i = 0; i < n; ++i)
+        if (int rc = check_tensor(t[i], recipe, false)) return rc;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    int64_t total = 0;
+    for (int i = 0; i < n; ++i) {
+        const q4adamw_tensor_t& x = t[i];
+        total += x.numel;
+        if (x.numel == 0) continue;
+        const int64_t nb = nblocks(x.numel);
+        cudaError_t e = cudaMemsetAsync(x.m_codes, 0, (size_t)(nb * 64), s);
+        if (e == cudaSuccess) e = cudaMemsetAsync(x.m_scale, 0, (size_t)(nb * 4), s);
+        if (e == cudaSuccess) {
+            if (is_factored(x, recipe)) {
+                e = cudaMemsetAsync(x.v_row, 0, (size_t)(x.rows * 4), s);
+                if (e == cudaSuccess) e = cudaMemsetAsync(x.v_col, 0, (size_t)(x.numel / x.rows * 4), s);
+            } else {
+                e = cudaMemsetAsync(x.v_codes, 0, (size_t)(nb * 64), s);
+                if (e == cudaSuccess) e = cudaMemsetAsync(x.v_scale, 0, (size_t)(nb * 4), s);
+            }
+        }
+        if (e != cudaSuccess) return cuda_fail(e);
+    }
+    if (header_out) {
+        header_out->magic = Q4ADAMW_MAGIC;
+        header_out->format = Q4ADAMW_STATE_FORMAT;
+        header_out->recipe = (uint32_t)recipe;
+        header_out->block = Q4ADAMW_BLOCK;
+        header_out->n_tensors = n;
+        header_out->numel_total = total;
+    }
+    return Q4_OK;
+}
+
+int q4adamw_step(const q4adamw_tensor_t* t, int n, float lr, float beta1, float beta2, float eps, float weight_decay,
+                 int64_t step, uint64_t seed, int recipe, uint32_t flags, void* workspace, int64_t workspace_bytes,
+                 void* stream) {
+    if (n < 0 || (n > 0 && !t)) return Q4_EINVAL;
+    if (int rc = check_recipe(recipe)) return rc;
+    if (step < 1 || step > 0xFFFFFFFFll) return Q4_EINVAL;
+    if (!(beta1 >= 0.f && beta1 < 1.f) || !(beta2 >= 0.f && beta2 < 1.f)) return Q4_EINVAL;
+    if (!(eps > 0.f) || !std::isfinite(eps) || !std::isfinite(lr) || !std::isfinite(weight_decay)) return Q4_EINVAL;
+    for (int i = 0; i < n; ++i)
+        if (int rc = check_tensor(t[i], recipe, true)) return rc;
+    const Layout L = make_layout(t, n, recipe);
+    if (!workspace || !aligned(workspace, 256) || workspace_bytes < L.total) return Q4_EWORKSPACE;
+    q4::Tables* tabs = tables_for(recipe);
+    if (!tabs) return Q4_EINVAL;
+    if (n == 0) return Q4_OK;
+
+    // Host image of the uploaded part of the workspace.
+    thread_local std::vector<unsigned char> img;
+    img.assign((size_t)L.upload_bytes, 0);
+    DevTensor* desc = reinterpret_cast<DevTensor*>(img.data() + L.desc);
+    int64_t* pairs = reinterpret_cast<int64_t*>(img.data() + L.pairs);
+    int64_t* rows = reinterpret_cast<int64_t*>(img.data() + L.rows);
+    int64_t* tiles = reinterpret_cast<int64_t*>(img.data() + L.tiles);
+    int64_t* cols = reinterpret_cast<int64_t*>(img.data() + L.cols);
+    int32_t* fids = reinterpret_cast<int32_t*>(img.data() + L.fids);
+    char* ws = static_cast<char*>(workspace);
+    int64_t colpart_off = L.colpart;
+    int nf = 0;
+    pairs[0] = rows[0] = tiles[0] = cols[0] = 0;
+    for (int i = 0; i < n; ++i) {
+        desc[i] = make_dev(t[i], recipe, flags);
+        const int64_t nb = nblocks(t[i].numel);
+        pairs[i + 1] = pairs[i] + (nb + 1) / 2;
+        const bool f = (desc[i].flags & q4::DF_FACTORED) && t[i].numel > 0;
+        rows[i + 1] = rows[i] + (f ? desc[i].rows : 0);
+        cols[i + 1] = cols[i] + (f ? desc[i].cols : 0);
+        tiles[i + 1] = tiles[i] + (f ? n_slabs(desc[i].rows) * n_segs(desc[i].cols) : 0);
+        if (f) {
+            desc[i].rbar = reinterpret_cast<float*>(ws + L.rbar) + nf;
+            desc[i].colpart = reinterpret_cast<float*>(ws + colpart_off);
+            colpart_off += n_slabs(desc[i].rows) * desc[i].cols * 4;
+            fids[nf++] = i;
+        }
+    }
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    cudaError_t e = cudaMemcpyAsync(workspace, img.data(), (size_t)L.upload_bytes, cudaMemcpyHostToDevice, s);
+    if (e != cudaSuccess) return cuda_fail(e);
+
+    const Scalars hs = host_scalars(lr, beta1, beta2, weight_decay, step);
+    const DevTensor* d_desc = reinterpret_cast<const DevTensor*>(ws + L.desc);
+
+    if (nf > 0) {
+        q4::FactoredParams fp{};
+        fp.tensors = d_desc;
+        fp.row_prefix = reinterpret_cast<const int64_t*>(ws + L.rows);
+        fp.tile_prefix = reinterpret_cast<const int64_t*>(ws + L.tiles);
+        fp.col_prefix = reinterpret_cast<const int64_t*>(ws + L.cols);
+        fp.factored_ids = reinterpret_cast<const int32_t*>(ws + L.fids);
+        fp.n_tensors = n;
+        fp.n_factored = nf;
+        fp.total_rows = rows[n];
+        fp.total_tiles = tiles[n];
+        fp.total_cols = cols[n];
+        fp.beta2 = beta2;
+        fp.omb2 = hs.omb2;
+        if (int ce = q4::launch_factored(fp, stream)) return cuda_fail((cudaError_t)ce);
+    }
+
+    q4::StepParams p{};
+    p.tensors = d_desc;
+    p.pair_prefix = reinterpret_cast<const int64_t*>(ws + L.pairs);
+    p.total_pairs = pairs[n];
+    p.n_tensors = n;
+    p.recipe = recipe;
+    p.beta1 = beta1;
+    p.beta2 = beta2;
+    p.omb1 = hs.omb1;
+    p.omb2 = hs.omb2;
+    p.c2 = hs.c2;
+    p.eps = eps;
+    p.decay = hs.decay;
+    p.step_size = hs.step_size;
+    p.step = (uint32_t)step;
+    const uint32_t k0 = (uint32_t)seed, k1 = (uint32_t)(seed >> 32);
+    for (int r = 0; r < 10; ++r) {
+        p.round_keys[2 * r] = k0 + (uint32_t)r * 0x9E3779B9u;
+        p.round_keys[2 * r + 1] = k1 + (uint32_t)r * 0xBB67AE85u;
+    }
+    p.tab = *tabs;
+    if (p.total_pairs == 0) return Q4_OK;
+    int dev = 0;
+    if ((e = cudaGetDevice(&dev)) != cudaSuccess) return cuda_fail(e);
+    const int grid = q4::step_grid_size(dev, p.total_pairs);
+    if (int ce = q4::launch_step(p, grid, stream)) return cuda_fail((cudaError_t)ce);
+    return Q4_OK;
+}
+
+int q4adamw_dequant_state(const q4adamw_tensor_t* t, int recipe, float* m_out, float* v_out, void* stream) {
+    if (!t) return Q4_EINVAL;
+    if (int rc = check_recipe(recipe)) return rc;
+    if (int rc = check_tensor(*t, recipe, false)) return rc;
+    if (t->numel == 0 || (!m_out && !v_out)) return Q4_OK;
+    const DevTensor d = make_dev(*t, recipe, 0);
+    const q4::Codebook& nf4 = q4::codebook(0);
+    const q4::Codebook& vb = q4::codebook(recipe == Q4_RECIPE_ZIP_SR ? 1 : 2);
+    if (int ce = q4::launch_dequant(d, recipe, nf4.levels, vb.levels, m_out, v_out, stream))
+        return cuda_fail((cudaError_t)ce);
+    return Q4_OK;
+}
+
+int q4adamw_codebook(int which, float* levels, float* thresholds) {
+    if (which < 0 || which > 2) return Q4_ERECIPE;
+    const q4::Codebook& c = q4::codebook(which);
+    if (levels) std::memcpy(levels, c.levels, sizeof c.levels);
+    if (thresholds) std::memcpy(thresholds, c.thresholds, sizeof c.thresholds);
+    return Q4_OK;
+}
+
+}  // extern "C"

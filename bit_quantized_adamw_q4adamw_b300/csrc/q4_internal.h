@@ -1,0 +1,96 @@
+// Internal definitions of the q4adamw CUDA library (not part of the ABI).
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+
+#include "q4adamw.h"
+
+namespace q4 {
+
+constexpr int kBlock = 128;        // elements per quantisation block
+constexpr int kThreads = 256;      // threads per CTA of the step kernel
+constexpr int kWarps = kThreads / 32;
+constexpr int kVLut = 2048;        // entries of the log-bucket candidate tables
+
+// Per-tensor descriptor as the kernels read it (one 128-byte record).
+struct DevTensor {
+    float* param;
+    const uint16_t* grad;
+    uint16_t* bf16;
+    uint8_t* mc;
+    float* ms;
+    uint8_t* vc;
+    float* vs;
+    float* vrow;
+    float* vcol;
+    int64_t numel;
+    int64_t rows;
+    int64_t cols;
+    uint64_t elem_offset;
+    uint32_t tensor_id;
+    uint32_t flags;        // DF_* bits
+    float* rbar;           // factored: device scalar mean(R) of this step
+    float* colpart;        // factored: column partial sums [n_slabs][cols]
+};
+static_assert(sizeof(DevTensor) == 128, "descriptor must stay 128 bytes");
+
+enum : uint32_t { DF_M_SR = 1u, DF_FACTORED = 2u, DF_BF16 = 4u };
+
+// Codebooks and candidate tables (built on the host by q4_tables.cpp).
+struct Tables {
+    float nf4[16];      // NF4 levels, ascending
+    float nf4_t[16];    // NF4 RTN thresholds (index 15 unused)
+    float vl[16];       // v levels for this launch (Dyn4 or Dyn4-NZ)
+    float vt[16];       // v RTN thresholds (index 15 unused)
+    uint8_t lut_nf4_t[64];   // NF4 threshold candidate by linear bucket
+    uint8_t lut_nf4_l[64];   // NF4 level (cell) candidate by linear bucket
+    uint8_t lut_v_l[kVLut];  // v level (cell) candidate by log bucket
+    uint8_t lut_v_t[kVLut];  // v threshold candidate by log bucket
+};
+
+// Host-side tables: 0 = NF4, 1 = Dyn4, 2 = Dyn4-NZ.
+struct Codebook {
+    float levels[16];
+    float thresholds[15];
+};
+const Codebook& codebook(int which);
+// Fills t for the v codebook `vbook` (1 or 2).  Returns false if a candidate
+// table cannot be built (never for the shipped codebooks).
+bool build_tables(int vbook, Tables* t);
+
+struct StepParams {
+    const DevTensor* tensors;
+    const int64_t* pair_prefix;   // n+1 entries: first block-pair of each tensor
+    int64_t total_pairs;
+    int n_tensors;
+    int recipe;
+    float beta1, beta2, omb1, omb2, c2, eps, decay, step_size;
+    uint32_t step;
+    uint32_t round_keys[20];      // Philox key schedule: (k0, k1) for rounds 0..9
+    Tables tab;
+};
+
+struct FactoredParams {
+    const DevTensor* tensors;
+    const int64_t* row_prefix;    // n+1: factored rows of each tensor
+    const int64_t* tile_prefix;   // n+1: column tiles (slab x segment) of each tensor
+    const int64_t* col_prefix;    // n+1: factored columns of each tensor
+    const int32_t* factored_ids;  // tensor index of the k-th factored tensor
+    int n_tensors;
+    int n_factored;
+    int64_t total_rows, total_tiles, total_cols;
+    float beta2, omb2;
+};
+
+constexpr int kSlabRows = 64;      // rows per column-partial slab
+constexpr int kSegCols = 2048;     // columns per column tile (256 threads x 8)
+
+// Launchers (return cudaError_t as int).
+int launch_step(const StepParams& p, int grid, void* stream);
+int step_grid_size(int device, int64_t total_pairs);
+int launch_factored(const FactoredParams& p, void* stream);
+int launch_dequant(const DevTensor& d, int recipe, const float* nf4, const float* vl, float* m_out, float* v_out,
+                   void* stream);
+
+}  // namespace q4

@@ -144,10 +144,11 @@ def tensor_sigma(w: Workload, tensor_id: int, seed: int = 0) -> float:
     return math.exp(math.log(lo) + u * (math.log(hi) - math.log(lo)))
 
 
-def init_param(spec: TensorSpec, tensor_id: int, device="cpu", seed: int = 0, std: float = 0.02) -> torch.Tensor:
-    """FP32 master weights ~ N(0, std)."""
+def init_param(spec: TensorSpec, tensor_id: int, device="cpu", seed: int = 0, std: float = 0.02,
+               n: int | None = None) -> torch.Tensor:
+    """FP32 master weights ~ N(0, std); n draws only that many leading elements."""
     g = _gen(device, seed, 1, tensor_id)
-    return torch.randn(spec.numel, generator=g, device=device, dtype=torch.float32).mul_(std)
+    return torch.randn(spec.numel if n is None else n, generator=g, device=device, dtype=torch.float32).mul_(std)
 
 
 def zero_block_mask(w: Workload, spec: TensorSpec, tensor_id: int, device="cpu", seed: int = 0) -> torch.Tensor:
@@ -160,10 +161,13 @@ def zero_block_mask(w: Workload, spec: TensorSpec, tensor_id: int, device="cpu",
 
 
 def draw_grad(w: Workload, spec: TensorSpec, tensor_id: int, step: int, device="cpu", seed: int = 0,
-              out: torch.Tensor | None = None) -> torch.Tensor:
-    """BF16 gradient of tensor `tensor_id` at step `step` (flat, numel)."""
+              out: torch.Tensor | None = None, n: int | None = None) -> torch.Tensor:
+    """BF16 gradient of tensor `tensor_id` at step `step` (flat, numel; n: only
+    that many leading elements, drawn directly, for timing samples)."""
+    if n is not None and n < spec.numel and (w.grad == "row_scaled" or w.zero_block_frac > 0):
+        return draw_grad(w, spec, tensor_id, step, device, seed)[:n].contiguous()
     g = _gen(device, seed, 2, tensor_id, step)
-    n = spec.numel
+    n = spec.numel if n is None else n
     x = torch.randn(n, generator=g, device=device, dtype=torch.float32)
     if w.grad == "normal":
         x.mul_(w.sigma_range[0])

@@ -1,0 +1,163 @@
+"""GPU-versus-oracle parity of the fused step through the C ABI.
+
+Codes, scales, FP32 weights and BF16 weights must be bit-identical to the
+oracle (both sides evaluate the same FP32 operation sequence; decisions that
+turn floating point into codes are taken in FP32 on both).  The factored
+statistics R, C are FP32 tree sums on the GPU and float64 sums in the oracle:
+they are compared at 1e-5 relative, and the weights of factored tensors at
+the stated bound |dtheta| <= 1e-6 * max(1, |theta|).
+"""
+import numpy as np
+import pytest
+import torch
+
+from bit_quantized_adamw_q4adamw_b300 import workloads as W
+from parity_util import HYPER, Pair, grads_for
+
+pytestmark = pytest.mark.gpu
+
+
+def _assert_exact(res, step):
+    assert res["codes"] == 0, (step, res)
+    assert res["scales"] == 0, (step, res)
+    assert res["theta"] == 0, (step, res)
+    assert res["bf16"] == 0, (step, res)
+
+
+def test_vec4096_zipsr_ten_steps_bit_exact():
+    w = W.WORKLOADS["vec4096_zipsr"]
+    p = Pair(w.tensors, w.recipe)
+    for t in range(1, 11):
+        p.step(t, grads_for(w, t), seed=0)
+        _assert_exact(p.compare(), t)
+
+
+def test_mat_zeeden_hundred_steps_bit_exact():
+    # 1024 x 4096 slice of the 4096 x 4096 ZE-EDEN workload (same recipe, row
+    # scales and 5% zero blocks), all 100 steps compared element by element.
+    base = W.WORKLOADS["mat4096_zeeden"]
+    w = W.custom("mat1024", [(1024, 4096)], "ze_eden", grad="row_scaled", sigma=(1e-6, 1e-2),
+                 zero_block_frac=0.05)
+    assert w.recipe == base.recipe
+    p = Pair(w.tensors, w.recipe)
+    for t in range(1, 101):
+        p.step(t, grads_for(w, t))
+        if t <= 5 or t % 10 == 0:
+            _assert_exact(p.compare(), t)
+
+
+def test_mat4096_zeeden_full_size_five_steps():
+    w = W.WORKLOADS["mat4096_zeeden"]
+    p = Pair(w.tensors, w.recipe)
+    for t in range(1, 6):
+        p.step(t, grads_for(w, t))
+        _assert_exact(p.compare(), t)
+
+
+RAGGED = [(1,), (5,), (127,), (128,), (129,), (255,), (256,), (1000,), (3, 129), (257, 7), (4096 + 64,),
+          (7, 128), (128 * 13 + 17,)]
+
+
+@pytest.mark.parametrize("recipe", ["zip_sr", "ze_eden"])
+@pytest.mark.parametrize("sr", [False, True])
+def test_ragged_tensor_list(recipe, sr):
+    flags = [W.T_LM_HEAD if i % 3 == 0 else 0 for i in range(len(RAGGED))]
+    w = W.custom("rag", RAGGED, recipe, flags=flags, grad="normal", sigma=(1e-3, 1e-3))
+    offs = [128 * 5 * i for i in range(len(RAGGED))]
+    p = Pair(w.tensors, recipe, elem_offsets=offs, tensor_ids=[10 + i for i in range(len(RAGGED))])
+    for t in range(1, 8):
+        p.step(t, grads_for(w, t, tids=[10 + i for i in range(len(RAGGED))]), seed=77,
+               flags=1 if sr else 0)
+        _assert_exact(p.compare(), t)
+
+
+def test_lm_head_sr_phase_gpt_like():
+    # LM-head SR active from the start of the final phase (steps 9001..), as in
+    # the GPT-style 1.4B workload, on a reduced tensor list.
+    shapes = [(512, 256), (256,), (768, 256), (256,)]
+    flags = [W.T_LM_HEAD, 0, 0, 0]
+    w = W.custom("gptmini", shapes, "zip_sr", flags=flags, grad="tensor_scaled", sigma=(1e-5, 1e-2))
+    p = Pair(w.tensors, "zip_sr")
+    for t in range(9001, 9006):
+        p.step(t, grads_for(w, t), seed=3, flags=1)
+        _assert_exact(p.compare(), t)
+
+
+def test_degenerate_values():
+    # zero, tiny (slow-path scales), huge and mixed-magnitude gradients.
+    n = 128 * 12
+    w = W.custom("deg", [(n,)], "zip_sr")
+    rng = np.random.default_rng(5)
+    for recipe in ("zip_sr", "ze_eden", "factored"):
+        p = Pair(w.tensors, recipe)
+        for t in range(1, 5):
+            g = rng.normal(0, 1, n).astype(np.float32)
+            g[0:128] = 0.0                                  # zero block
+            g[128:256] *= 1e-38                             # subnormal moments
+            g[256:384] *= 1e-25
+            g[384:512] *= 1e25                              # huge
+            g[512:640] = np.where(rng.random(128) < 0.5, 0.0, g[512:640] * 1e-3)
+            g[640:768] *= np.float32(10.0) ** rng.uniform(-30, 10, 128).astype(np.float32)
+            gt = torch.from_numpy(g).to(torch.bfloat16)
+            p.step(t, [gt], seed=t)
+            _assert_exact(p.compare(), (recipe, t))
+
+
+def test_factored_small_list():
+    shapes = [(64, 96), (96,), (130, 128), (1, 256), (300, 40), (17,), (33, 64)]
+    w = W.custom("fac", shapes, "factored", grad="normal", sigma=(1e-3, 1e-3))
+    p = Pair(w.tensors, "factored")
+    for t in range(1, 11):
+        p.step(t, grads_for(w, t))
+        r = p.compare(exact_theta=False)
+        assert r["codes"] == 0 and r["scales"] == 0, (t, r)
+        assert r["rc"] == 0 and r["theta"] == 0 and r["bf16"] == 0, (t, r)
+
+
+def test_sharded_tensor_matches_whole():
+    # Two block-aligned shards with elem_offset produce the bits of the whole tensor.
+    n, cut = 128 * 9 + 31, 128 * 4
+    w = W.custom("shard", [(n,)], "zip_sr", flags=[W.T_LM_HEAD])
+    th = W.init_param(w.tensors[0], 0)
+    whole = Pair(w.tensors, "zip_sr", theta0=[th], tensor_ids=[4])
+    parts = W.custom("shard2", [(cut,), (n - cut,)], "zip_sr", flags=[W.T_LM_HEAD, W.T_LM_HEAD])
+    split = Pair(parts.tensors, "zip_sr", theta0=[th[:cut], th[cut:]], tensor_ids=[4, 4], elem_offsets=[0, cut])
+    for t in range(1, 5):
+        g = W.draw_grad(w, w.tensors[0], 0, t)
+        whole.step(t, [g], seed=9, flags=1)
+        split.step(t, [g[:cut], g[cut:]], seed=9, flags=1)
+        a = whole.gpu.view(0, "param").cpu()
+        b = torch.cat([split.gpu.view(0, "param").cpu(), split.gpu.view(1, "param").cpu()])
+        assert torch.equal(a, b)
+        assert torch.equal(whole.gpu.view(0, "m_codes").cpu(),
+                           torch.cat([split.gpu.view(0, "m_codes").cpu(), split.gpu.view(1, "m_codes").cpu()]))
+        assert torch.equal(whole.gpu.view(0, "v_codes").cpu(),
+                           torch.cat([split.gpu.view(0, "v_codes").cpu(), split.gpu.view(1, "v_codes").cpu()]))
+
+
+@pytest.mark.parametrize("recipe", ["zip_sr", "ze_eden", "factored"])
+def test_dequant_state_matches_oracle(recipe):
+    shapes = [(40, 64), (200,), (3, 129)]
+    w = W.custom("dq", shapes, recipe)
+    p = Pair(w.tensors, recipe)
+    for t in range(1, 4):
+        p.step(t, grads_for(w, t))
+    for i, o in enumerate(p.ora):
+        m, v = p.gpu.dequant(i)
+        torch.cuda.synchronize()
+        assert np.array_equal(m.cpu().numpy(), o.m_dequant())
+        vo = o.v_dequant(recipe)
+        if o.factored:
+            assert np.allclose(v.cpu().numpy(), vo, rtol=3e-5, atol=0)
+        else:
+            assert np.array_equal(v.cpu().numpy(), vo)
+
+
+def test_state_init_header_and_zero_state():
+    w = W.custom("hdr", [(300,), (64, 64)], "factored")
+    p = Pair(w.tensors, "factored")
+    h = p.gpu.header
+    assert h.magic == 0x57413451 and h.format == 1 and h.recipe == 2 and h.block == 128
+    assert h.n_tensors == 2 and h.numel_total == 300 + 64 * 64
+    for name in ("m_codes", "m_scale"):
+        assert int(getattr(p.gpu, name).abs().sum()) == 0
