@@ -53,6 +53,8 @@ def parse():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0, help="target oracle time of the CPU sample")
+    ap.add_argument("--tensors", type=int, default=0,
+                    help="keep only the first N tensors of the workload (small cases for profiling)")
     return ap.parse_args()
 
 
@@ -228,11 +230,20 @@ def oracle_sample(w, target_seconds: float, device_gen: str = "cpu"):
 
 
 # ---------------------------------------------------------------- arms
-def run_reference(args, rank, world):
+def get_workload(args):
+    import dataclasses
+
     from bit_quantized_adamw_q4adamw_b300 import workloads as W
+    w = W.WORKLOADS[args.workload]
+    if args.tensors > 0:
+        w = dataclasses.replace(w, name=f"{w.name}[:{args.tensors}]", tensors=w.tensors[:args.tensors])
+    return w
+
+
+def run_reference(args, rank, world):
     if rank != 0:
         return
-    w = W.WORKLOADS[args.workload]
+    w = get_workload(args)
     per_step = max(args.cpu_seconds / max(args.steps, 1), 0.5)
     vals, secs_total, desc, n = [], 0.0, "", 0
     for k in range(args.warmup + args.steps):
@@ -261,7 +272,7 @@ def run_ours(args, rank, world, local):
     from bit_quantized_adamw_q4adamw_b300 import workloads as W
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
-    w = W.WORKLOADS[args.workload]
+    w = get_workload(args)
     h = W.HYPER
     flags = 1 if w.lm_head_sr else 0
     st = build_state(w, dev)

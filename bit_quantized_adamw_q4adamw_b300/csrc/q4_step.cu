@@ -325,33 +325,33 @@ __device__ __forceinline__ void process_pair(const StepParams& P, const DevTenso
                 cv |= (uint32_t)code << (4 * i);
             }
             if (RECIPE == Q4_RECIPE_ZE_EDEN) {
-                // EDEN scale s * |y|^2 / <y, L[q]>, y = v' * (1/s), fixed summation order.
-                if (s_v >= 0x1p-126f) {
-                    float pa[2], pb[2];
+                // EDEN scale s * |y|^2 / <y, L[q]>, y = v' * (1/s), fixed summation
+                // order.  The sums run on every lane (the shuffles need the whole
+                // warp); blocks with s below the smallest normal keep s.
+                float pa[2], pb[2];
 #pragma unroll
-                    for (int h = 0; h < 2; ++h) {
-                        float sa = 0.f, sb = 0.f;
+                for (int h = 0; h < 2; ++h) {
+                    float sa = 0.f, sb = 0.f;
 #pragma unroll
-                        for (int i = 0; i < 4; ++i) {
-                            const int e = 4 * h + i;
-                            const float y = __fmul_rn(v1[e], rho);
-                            const float yh = sm.vl[q[e]];
-                            const float ta = __fmul_rn(y, y), tb = __fmul_rn(y, yh);
-                            sa = (i == 0) ? ta : __fadd_rn(sa, ta);
-                            sb = (i == 0) ? tb : __fadd_rn(sb, tb);
-                        }
-                        pa[h] = sa;
-                        pb[h] = sb;
+                    for (int i = 0; i < 4; ++i) {
+                        const int e = 4 * h + i;
+                        const float y = __fmul_rn(v1[e], rho);
+                        const float yh = sm.vl[q[e]];
+                        const float ta = __fmul_rn(y, y), tb = __fmul_rn(y, yh);
+                        sa = (i == 0) ? ta : __fadd_rn(sa, ta);
+                        sb = (i == 0) ? tb : __fadd_rn(sb, tb);
                     }
-                    float A = __fadd_rn(pa[0], pa[1]);
-                    float B = __fadd_rn(pb[0], pb[1]);
-#pragma unroll
-                    for (int o = 1; o < 16; o <<= 1) {
-                        A = __fadd_rn(A, __shfl_xor_sync(0xffffffffu, A, o));
-                        B = __fadd_rn(B, __shfl_xor_sync(0xffffffffu, B, o));
-                    }
-                    sv_store = (B == 0.f) ? 0.f : __fmul_rn(s_v, __fdiv_rn(A, B));
+                    pa[h] = sa;
+                    pb[h] = sb;
                 }
+                float A = __fadd_rn(pa[0], pa[1]);
+                float B = __fadd_rn(pb[0], pb[1]);
+#pragma unroll
+                for (int o = 1; o < 16; o <<= 1) {
+                    A = __fadd_rn(A, __shfl_xor_sync(0xffffffffu, A, o));
+                    B = __fadd_rn(B, __shfl_xor_sync(0xffffffffu, B, o));
+                }
+                if (s_v >= 0x1p-126f) sv_store = (B == 0.f) ? 0.f : __fmul_rn(s_v, __fdiv_rn(A, B));
             }
         }
     }

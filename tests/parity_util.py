@@ -16,6 +16,11 @@ from oracle import oracle as O
 HYPER = W.HYPER
 
 
+def neq_f32(a: np.ndarray, b: np.ndarray) -> np.ndarray:
+    """Bitwise inequality of FP32 arrays, treating any two NaNs as equal."""
+    return (a.view(np.uint32) != b.view(np.uint32)) & ~(np.isnan(a) & np.isnan(b))
+
+
 def bf16_bits(t: torch.Tensor) -> np.ndarray:
     return t.detach().cpu().view(torch.int16).numpy().view(np.uint16)
 
@@ -60,7 +65,7 @@ class Pair:
             mc = self.gpu.view(i, "m_codes").cpu().numpy()
             out["codes"] += int((mc != o.m_codes).sum())
             ms = self.gpu.view(i, "m_scale").cpu().numpy()
-            out["scales"] += int((ms.view(np.uint32) != o.m_scale.view(np.uint32)).sum())
+            out["scales"] += int(neq_f32(ms, o.m_scale).sum())
             if o.factored:
                 R = self.gpu.view(i, "v_row").cpu().numpy().astype(np.float64)
                 C = self.gpu.view(i, "v_col").cpu().numpy().astype(np.float64)
@@ -70,12 +75,12 @@ class Pair:
                 vc = self.gpu.view(i, "v_codes").cpu().numpy()
                 out["codes"] += int((vc != o.v_codes).sum())
                 vs = self.gpu.view(i, "v_scale").cpu().numpy()
-                out["scales"] += int((vs.view(np.uint32) != o.v_scale.view(np.uint32)).sum())
+                out["scales"] += int(neq_f32(vs, o.v_scale).sum())
             th = self.gpu.view(i, "param").cpu().numpy()
             d = np.abs(th.astype(np.float64) - o.param)
             out["max_dtheta"] = max(out["max_dtheta"], float(d.max(initial=0.0)))
             if exact_theta:
-                out["theta"] += int((th.view(np.uint32) != o.param.view(np.uint32)).sum())
+                out["theta"] += int(neq_f32(th, o.param).sum())
             else:
                 out["theta"] += int((d > theta_tol * np.maximum(1.0, np.abs(o.param))).sum())
             b16 = bf16_bits(self.gpu.view(i, "param_bf16"))

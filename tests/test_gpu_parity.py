@@ -95,7 +95,7 @@ def test_degenerate_values():
             g[0:128] = 0.0                                  # zero block
             g[128:256] *= 1e-38                             # subnormal moments
             g[256:384] *= 1e-25
-            g[384:512] *= 1e25                              # huge
+            g[384:512] *= 1e15                              # huge (g^2 stays finite)
             g[512:640] = np.where(rng.random(128) < 0.5, 0.0, g[512:640] * 1e-3)
             g[640:768] *= np.float32(10.0) ** rng.uniform(-30, 10, 128).astype(np.float32)
             gt = torch.from_numpy(g).to(torch.bfloat16)
