@@ -65,6 +65,18 @@ def dist_env():
     return rank, world, local
 
 
+def max_over_ranks(x: float) -> float:
+    """Maximum of a per-rank scalar over the process group (identity without one)."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return x
+    dev = torch.device("cuda", torch.cuda.current_device()) if dist.get_backend() == "nccl" else torch.device("cpu")
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
 def peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
@@ -305,11 +317,7 @@ def run_ours(args, rank, world, local):
         dist.barrier()
     clocks = sampler.stop() if sampler else None
     per = [evs[k].elapsed_time(evs[k + 1]) for k in range(args.steps)]
-    total_ms = evs[0].elapsed_time(evs[-1])
-    if world > 1:
-        tt = torch.tensor([total_ms], device=dev)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        total_ms = float(tt.item())
+    total_ms = max_over_ranks(evs[0].elapsed_time(evs[-1]))
     ms_per_step = total_ms / args.steps
     value = world * w.numel * args.steps / (total_ms / 1e3)
 

@@ -1,0 +1,104 @@
+"""World-size-2 gloo tests of the multi-rank path on the CPU.
+
+The step needs no collective: each rank steps its own block-aligned shards
+(elem_offset = global start), and the union of the shards must equal the
+single-rank result bit for bit.  The bench's max-over-ranks timing reduction
+is exercised with the same process group.
+"""
+import os
+import socket
+
+import numpy as np
+import pytest
+import torch
+import torch.distributed as dist
+import torch.multiprocessing as mp
+
+from bit_quantized_adamw_q4adamw_b300 import sharding
+from bit_quantized_adamw_q4adamw_b300 import workloads as W
+
+SHAPES = [(1000,), (37, 129), (4096,), (5,), (130, 64)]
+FLAGS = [W.T_LM_HEAD, 0, 0, 0, W.T_LM_HEAD]
+
+
+def _free_port() -> int:
+    s = socket.socket()
+    s.bind(("127.0.0.1", 0))
+    port = s.getsockname()[1]
+    s.close()
+    return port
+
+
+def _run_oracle(shards, recipe, steps):
+    from oracle import oracle as O
+    w = W.custom("mr", SHAPES, recipe, flags=FLAGS)
+    h = W.HYPER
+    outs = []
+    for sh in shards:
+        spec = w.tensors[sh.tensor]
+        th = W.init_param(spec, sh.tensor).numpy()[sh.start:sh.start + sh.numel]
+        t = O.OracleTensor.zeros_state(th, sh.tensor, flags=spec.flags, elem_offset=sh.elem_offset, recipe=recipe)
+        for k in range(1, steps + 1):
+            g = W.draw_grad(w, spec, sh.tensor, k)[sh.start:sh.start + sh.numel].contiguous()
+            t.step(g.view(torch.int16).numpy().view(np.uint16), h["lr"], h["beta1"], h["beta2"], h["eps"],
+                   h["weight_decay"], k, 11, recipe, O.LM_HEAD_SR_ACTIVE)
+        outs.append((sh.tensor, sh.start, t.param.copy(), t.m_codes.copy(), t.v_codes.copy(), t.v_scale.copy()))
+    return outs
+
+
+def _worker(rank, world, port, recipe, q):
+    os.environ["MASTER_ADDR"] = "127.0.0.1"
+    os.environ["MASTER_PORT"] = str(port)
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    try:
+        shards = sharding.partition([int(np.prod(s)) for s in SHAPES], world, rank)
+        outs = _run_oracle(shards, recipe, steps=3)
+        gathered = [None] * world
+        dist.all_gather_object(gathered, outs)
+        import bench
+        mx = bench.max_over_ranks(float(rank + 1) * 10.0)
+        if rank == 0:
+            q.put((gathered, mx))
+    finally:
+        dist.destroy_process_group()
+
+
+@pytest.mark.parametrize("recipe", ["zip_sr", "ze_eden"])
+def test_two_rank_shards_equal_single_rank(recipe):
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    port = _free_port()
+    procs = [ctx.Process(target=_worker, args=(r, 2, port, recipe, q)) for r in range(2)]
+    for p in procs:
+        p.start()
+    gathered, mx = q.get(timeout=300)
+    for p in procs:
+        p.join(timeout=60)
+        assert p.exitcode == 0
+    assert mx == 20.0
+    whole = _run_oracle(sharding.partition([int(np.prod(s)) for s in SHAPES], 1, 0), recipe, steps=3)
+    parts = {}
+    for outs in gathered:
+        for tensor, start, th, mc, vc, vs in outs:
+            parts.setdefault(tensor, []).append((start, th, mc, vc, vs))
+    for tensor, start, th, mc, vc, vs in whole:
+        ps = sorted(parts[tensor], key=lambda x: x[0])
+        assert ps[0][0] == 0
+        assert np.array_equal(np.concatenate([p[1] for p in ps]), th)
+        assert np.array_equal(np.concatenate([p[2] for p in ps]), mc)
+        assert np.array_equal(np.concatenate([p[3] for p in ps]), vc)
+        assert np.array_equal(np.concatenate([p[4] for p in ps]), vs)
+
+
+def test_partition_covers_every_block_once():
+    numels = [1000, 37 * 129, 4096, 5, 130 * 64, 1]
+    for world in (1, 2, 3, 4, 8):
+        seen = {}
+        for r in range(world):
+            for sh in sharding.partition(numels, world, r):
+                assert sh.start % 128 == 0 and sh.numel > 0
+                for e in range(sh.start, sh.start + sh.numel):
+                    key = (sh.tensor, e)
+                    assert key not in seen
+                    seen[key] = r
+        assert len(seen) == sum(numels)
