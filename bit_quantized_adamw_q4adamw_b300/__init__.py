@@ -20,7 +20,8 @@ from ._native import (BLOCK, Q4_LM_HEAD_SR_ACTIVE, Q4_T_FACTORED, Q4_T_LM_HEAD, 
                       Q4Tensor, lib)
 
 __all__ = ["q4adamw_version", "q4adamw_strerror", "q4adamw_state_bytes", "q4adamw_workspace_bytes",
-           "q4adamw_state_init", "q4adamw_header_check", "q4adamw_step", "q4adamw_dequant_state",
+           "q4adamw_state_init", "q4adamw_header_check", "q4adamw_step", "q4adamw_step_noalloc",
+           "q4adamw_dequant_state",
            "q4adamw_codebook", "Q4State", "Q4Tensor", "Q4Header", "Q4Error", "RECIPES", "Q4_T_LM_HEAD",
            "Q4_T_FACTORED", "Q4_LM_HEAD_SR_ACTIVE", "BLOCK"]
 
@@ -90,6 +91,16 @@ def q4adamw_step(tensors, lr, beta1, beta2, eps, weight_decay, step, seed, recip
     _check(lib().q4adamw_step(arr, n, lr, beta1, beta2, eps, weight_decay, int(step), int(seed) & (2 ** 64 - 1),
                               _recipe(recipe), int(flags), ctypes.c_void_p(workspace.data_ptr()),
                               workspace.numel() * workspace.element_size(), _stream(stream)), "q4adamw_step")
+
+
+def q4adamw_step_noalloc(tensors, lr, beta1, beta2, eps, weight_decay, step, seed, recipe, flags,
+                         stream=None) -> None:
+    """q4adamw_step using the library's fixed static device scratch instead of a
+    workspace, for callers that cannot allocate one (see include/q4adamw.h)."""
+    arr, n = _array(tensors)
+    _check(lib().q4adamw_step_noalloc(arr, n, lr, beta1, beta2, eps, weight_decay, int(step),
+                                      int(seed) & (2 ** 64 - 1), _recipe(recipe), int(flags), _stream(stream)),
+           "q4adamw_step_noalloc")
 
 
 def q4adamw_dequant_state(tensor: Q4Tensor, recipe, m_out: torch.Tensor | None = None,

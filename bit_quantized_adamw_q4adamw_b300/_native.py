@@ -26,6 +26,7 @@ Q4_T_LM_HEAD = 0x1
 Q4_T_FACTORED = 0x2
 Q4_LM_HEAD_SR_ACTIVE = 0x1
 BLOCK = 128
+NOALLOC_SCRATCH_BYTES = 4 * 1024 * 1024
 
 
 class Q4Tensor(ctypes.Structure):
@@ -59,7 +60,7 @@ _lib = None
 
 EXPORTS = ("q4adamw_version", "q4adamw_strerror", "q4adamw_last_cuda_error", "q4adamw_state_bytes",
            "q4adamw_workspace_bytes", "q4adamw_state_init", "q4adamw_header_check", "q4adamw_step",
-           "q4adamw_dequant_state", "q4adamw_codebook")
+           "q4adamw_dequant_state", "q4adamw_codebook", "q4adamw_step_noalloc")
 
 
 def lib():
@@ -84,9 +85,10 @@ def lib():
     L.q4adamw_header_check.argtypes = [ctypes.POINTER(Q4Header), I]
     L.q4adamw_step.argtypes = [TP, I, F, F, F, F, F, I64, U64, I, U32, P, I64, P]
     L.q4adamw_dequant_state.argtypes = [TP, I, P, P, P]
+    L.q4adamw_step_noalloc.argtypes = [TP, I, F, F, F, F, F, I64, U64, I, U32, P]
     L.q4adamw_codebook.argtypes = [I, P, P]
     for name in ("q4adamw_state_bytes", "q4adamw_workspace_bytes", "q4adamw_state_init", "q4adamw_header_check",
-                 "q4adamw_step", "q4adamw_dequant_state", "q4adamw_codebook"):
+                 "q4adamw_step", "q4adamw_dequant_state", "q4adamw_codebook", "q4adamw_step_noalloc"):
         getattr(L, name).restype = I
     _lib = L
     return L

@@ -164,6 +164,10 @@ DevTensor make_dev(const q4adamw_tensor_t& t, int recipe, uint32_t call_flags) {
 
 }  // namespace
 
+namespace q4 {
+int record_cuda_error(int cuda_error) { return cuda_fail((cudaError_t)cuda_error); }
+}  // namespace q4
+
 extern "C" {
 
 int q4adamw_version(void) { return Q4ADAMW_STATE_FORMAT; }

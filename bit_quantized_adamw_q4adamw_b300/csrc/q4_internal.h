@@ -86,6 +86,9 @@ struct FactoredParams {
 constexpr int kSlabRows = 64;      // rows per column-partial slab
 constexpr int kSegCols = 2048;     // columns per column tile (256 threads x 8)
 
+// Records a cudaError_t for q4adamw_last_cuda_error() and returns Q4_ECUDA.
+int record_cuda_error(int cuda_error);
+
 // Launchers (return cudaError_t as int).
 int launch_step(const StepParams& p, int grid, void* stream);
 int step_grid_size(int device, int64_t total_pairs);

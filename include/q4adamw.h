@@ -206,6 +206,31 @@ int q4adamw_step(const q4adamw_tensor_t* t, int n, float lr, float beta1, float 
 int q4adamw_dequant_state(const q4adamw_tensor_t* t, int recipe, float* m_out, float* v_out, void* stream);
 
 /*
+ * q4adamw_step without a caller workspace.  The paper has no counterpart: this
+ * exists for callers that cannot allocate device memory for the workspace --
+ * code running inside another framework's memory budget (its caching
+ * allocator already holds the device memory, so a cudaMalloc would fail or
+ * fragment it) and code on a latency-critical path where cudaMalloc's implicit
+ * device synchronisation is not acceptable.  It allocates nothing: the
+ * workspace is a statically allocated device array of
+ * Q4ADAMW_NOALLOC_SCRATCH_BYTES that every GPU loading the library keeps until
+ * the process exits.  Arguments and results are those of q4adamw_step.
+ *   - A tensor list whose workspace (q4adamw_workspace_bytes) exceeds
+ *     Q4ADAMW_NOALLOC_SCRATCH_BYTES is rejected with Q4_EWORKSPACE before any
+ *     device work.
+ *   - The first call on a device looks up the array's device address on that
+ *     device (cudaGetSymbolAddress); make that first call before any stream
+ *     capture.  A failed lookup returns Q4_ECUDA.
+ *   - All calls share the one array and it keeps the previous call's contents;
+ *     every byte a step reads from it is written earlier in the same step, so
+ *     nothing needs clearing.  Calls whose GPU work overlaps (different streams
+ *     without ordering, or different host threads) race on the array: order them.
+ */
+#define Q4ADAMW_NOALLOC_SCRATCH_BYTES (4 * 1024 * 1024)
+int q4adamw_step_noalloc(const q4adamw_tensor_t* t, int n, float lr, float beta1, float beta2, float eps,
+                         float weight_decay, int64_t step, uint64_t seed, int recipe, uint32_t flags, void* stream);
+
+/*
  * The library's own codebook tables (host-only).  which: 0 = NF4, 1 = Dyn4
  * (zero-inclusive), 2 = Dyn4-NZ (zero-excluding).  levels: 16 ascending FP32
  * levels; thresholds: the 15 FP32 RTN decision points (rounded double
