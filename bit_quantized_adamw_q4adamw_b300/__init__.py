@@ -21,7 +21,7 @@ from ._native import (BLOCK, Q4_LM_HEAD_SR_ACTIVE, Q4_T_FACTORED, Q4_T_LM_HEAD, 
 
 __all__ = ["q4adamw_version", "q4adamw_strerror", "q4adamw_state_bytes", "q4adamw_workspace_bytes",
            "q4adamw_state_init", "q4adamw_header_check", "q4adamw_step", "q4adamw_step_noalloc",
-           "q4adamw_dequant_state",
+           "q4adamw_dequant_state", "q4adamw_step_status",
            "q4adamw_codebook", "Q4State", "Q4Tensor", "Q4Header", "Q4Error", "RECIPES", "Q4_T_LM_HEAD",
            "Q4_T_FACTORED", "Q4_LM_HEAD_SR_ACTIVE", "BLOCK"]
 
@@ -101,6 +101,15 @@ def q4adamw_step_noalloc(tensors, lr, beta1, beta2, eps, weight_decay, step, see
     _check(lib().q4adamw_step_noalloc(arr, n, lr, beta1, beta2, eps, weight_decay, int(step),
                                       int(seed) & (2 ** 64 - 1), _recipe(recipe), int(flags), _stream(stream)),
            "q4adamw_step_noalloc")
+
+
+def q4adamw_step_status(workspace: torch.Tensor, stream=None) -> int:
+    """Status word of the last q4adamw_step on `workspace` (0 = completed);
+    synchronises the stream."""
+    v = ctypes.c_uint32()
+    _check(lib().q4adamw_step_status(ctypes.c_void_p(workspace.data_ptr()), ctypes.byref(v), _stream(stream)),
+           "q4adamw_step_status")
+    return v.value
 
 
 def q4adamw_dequant_state(tensor: Q4Tensor, recipe, m_out: torch.Tensor | None = None,
@@ -230,6 +239,10 @@ class Q4State:
     def step(self, step, lr, beta1, beta2, eps, weight_decay, seed=0, flags=0, stream=None) -> None:
         q4adamw_step(self.descs, lr, beta1, beta2, eps, weight_decay, step, seed, self.recipe, flags,
                      self.workspace, stream)
+
+    def status(self, stream=None) -> int:
+        """Status word of the last step (0 = completed); synchronises."""
+        return q4adamw_step_status(self.workspace, stream)
 
     def dequant(self, i: int, stream=None):
         sl = self.slots[i]

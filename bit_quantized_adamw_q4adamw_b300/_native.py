@@ -25,6 +25,7 @@ RECIPES = {"zip_sr": 0, "ze_eden": 1, "factored": 2}
 Q4_T_LM_HEAD = 0x1
 Q4_T_FACTORED = 0x2
 Q4_LM_HEAD_SR_ACTIVE = 0x1
+Q4_STATUS_STAGE_TIMEOUT = 0x1
 BLOCK = 128
 NOALLOC_SCRATCH_BYTES = 4 * 1024 * 1024
 
@@ -60,7 +61,7 @@ _lib = None
 
 EXPORTS = ("q4adamw_version", "q4adamw_strerror", "q4adamw_last_cuda_error", "q4adamw_state_bytes",
            "q4adamw_workspace_bytes", "q4adamw_state_init", "q4adamw_header_check", "q4adamw_step",
-           "q4adamw_dequant_state", "q4adamw_codebook", "q4adamw_step_noalloc")
+           "q4adamw_dequant_state", "q4adamw_codebook", "q4adamw_step_noalloc", "q4adamw_step_status")
 
 
 def lib():
@@ -87,8 +88,10 @@ def lib():
     L.q4adamw_dequant_state.argtypes = [TP, I, P, P, P]
     L.q4adamw_step_noalloc.argtypes = [TP, I, F, F, F, F, F, I64, U64, I, U32, P]
     L.q4adamw_codebook.argtypes = [I, P, P]
+    L.q4adamw_step_status.argtypes = [P, ctypes.POINTER(U32), P]
     for name in ("q4adamw_state_bytes", "q4adamw_workspace_bytes", "q4adamw_state_init", "q4adamw_header_check",
-                 "q4adamw_step", "q4adamw_dequant_state", "q4adamw_codebook", "q4adamw_step_noalloc"):
+                 "q4adamw_step", "q4adamw_dequant_state", "q4adamw_codebook", "q4adamw_step_noalloc",
+                 "q4adamw_step_status"):
         getattr(L, name).restype = I
     _lib = L
     return L

@@ -67,9 +67,10 @@ int check_tensor(const q4adamw_tensor_t& t, int recipe, bool need_grad) {
 
 int64_t round_up(int64_t x, int64_t a) { return (x + a - 1) / a * a; }
 
-// Workspace layout, all offsets 256-B aligned.
+// Workspace layout, all offsets 256-B aligned.  The uploaded part is rewritten
+// from a zeroed host image every step, which also clears the status word.
 struct Layout {
-    int64_t desc, pairs, rows, tiles, cols, fids;  // uploaded part
+    int64_t status, desc, pairs, rows, tiles, cols, fids;  // uploaded part
     int64_t upload_bytes;
     int64_t rbar, colpart;                         // device-only part
     int64_t total;
@@ -83,6 +84,7 @@ int64_t n_segs(int64_t cols) { return (cols + q4::kSegCols - 1) / q4::kSegCols; 
 Layout make_layout(const q4adamw_tensor_t* t, int n, int recipe) {
     Layout L{};
     int64_t off = 0;
+    L.status = off; off = round_up(off + 4, 256);
     L.desc = off;  off = round_up(off + (int64_t)n * (int64_t)sizeof(DevTensor), 256);
     L.pairs = off; off = round_up(off + (int64_t)(n + 1) * 8, 256);
     L.rows = off;  off = round_up(off + (int64_t)(n + 1) * 8, 256);
@@ -90,7 +92,7 @@ Layout make_layout(const q4adamw_tensor_t* t, int n, int recipe) {
     L.cols = off;  off = round_up(off + (int64_t)(n + 1) * 8, 256);
     L.fids = off;  off = round_up(off + (int64_t)(n > 0 ? n : 1) * 4, 256);
     L.upload_bytes = off;
-    L.rbar = off;  off = round_up(off + (int64_t)(n > 0 ? n : 1) * 4, 256);
+    L.rbar = off;  off = round_up(off + (int64_t)(n > 0 ? n : 1) * 8, 256);   // {mean(R), 1/mean(R)}
     L.colpart = off;
     int64_t cp = 0;
     for (int i = 0; i < n; ++i) {
@@ -157,7 +159,10 @@ DevTensor make_dev(const q4adamw_tensor_t& t, int recipe, uint32_t call_flags) {
     d.tensor_id = t.tensor_id;
     d.flags = 0;
     if ((t.flags & Q4_T_LM_HEAD) && (call_flags & Q4_LM_HEAD_SR_ACTIVE)) d.flags |= q4::DF_M_SR;
-    if (is_factored(t, recipe)) d.flags |= q4::DF_FACTORED;
+    if (is_factored(t, recipe)) {
+        d.flags |= q4::DF_FACTORED;
+        if (d.cols % 8 == 0 && aligned(t.v_col, 16)) d.flags |= q4::DF_CVEC;
+    }
     if (t.param_bf16) d.flags |= q4::DF_BF16;
     return d;
 }
@@ -302,7 +307,7 @@ int q4adamw_step(const q4adamw_tensor_t* t, int n, float lr, float beta1, float 
         cols[i + 1] = cols[i] + (f ? desc[i].cols : 0);
         tiles[i + 1] = tiles[i] + (f ? n_slabs(desc[i].rows) * n_segs(desc[i].cols) : 0);
         if (f) {
-            desc[i].rbar = reinterpret_cast<float*>(ws + L.rbar) + nf;
+            desc[i].rbar = reinterpret_cast<float*>(ws + L.rbar) + 2 * nf;
             desc[i].colpart = reinterpret_cast<float*>(ws + colpart_off);
             colpart_off += n_slabs(desc[i].rows) * desc[i].cols * 4;
             fids[nf++] = i;
@@ -334,6 +339,7 @@ int q4adamw_step(const q4adamw_tensor_t* t, int n, float lr, float beta1, float 
 
     q4::StepParams p{};
     p.tensors = d_desc;
+    p.status = reinterpret_cast<uint32_t*>(ws + L.status);
     p.pair_prefix = reinterpret_cast<const int64_t*>(ws + L.pairs);
     p.total_pairs = pairs[n];
     p.n_tensors = n;
@@ -347,6 +353,10 @@ int q4adamw_step(const q4adamw_tensor_t* t, int n, float lr, float beta1, float 
     p.decay = hs.decay;
     p.step_size = hs.step_size;
     p.step = (uint32_t)step;
+    // The fast square root / reciprocal need d = sqrt(v') c2 + eps inside
+    // [2^-126, 2^126); with v' <= FLT_MAX and c2 <= 2^12 (beta2 < 1 in FP32)
+    // that holds whenever eps lies in [2^-100, 2^60].
+    p.fast_math = (eps >= 0x1p-100f && eps <= 0x1p60f) ? 1 : 0;
     const uint32_t k0 = (uint32_t)seed, k1 = (uint32_t)(seed >> 32);
     for (int r = 0; r < 10; ++r) {
         p.round_keys[2 * r] = k0 + (uint32_t)r * 0x9E3779B9u;
@@ -358,6 +368,18 @@ int q4adamw_step(const q4adamw_tensor_t* t, int n, float lr, float beta1, float 
     if ((e = cudaGetDevice(&dev)) != cudaSuccess) return cuda_fail(e);
     const int grid = q4::step_grid_size(dev, p.total_pairs);
     if (int ce = q4::launch_step(p, grid, stream)) return cuda_fail((cudaError_t)ce);
+    return Q4_OK;
+}
+
+int q4adamw_step_status(const void* workspace, uint32_t* status, void* stream) {
+    if (!workspace || !status) return Q4_EINVAL;
+    if (!aligned(workspace, 256)) return Q4_EWORKSPACE;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    uint32_t v = 0;
+    cudaError_t e = cudaMemcpyAsync(&v, workspace, sizeof v, cudaMemcpyDeviceToHost, s);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+    if (e != cudaSuccess) return cuda_fail(e);
+    *status = v;
     return Q4_OK;
 }
 

@@ -13,7 +13,8 @@
 //                  slab's partial column sums.
 //   colfin_kernel  one thread per column: sums the slab partials in slab order,
 //                  C_j <- beta2 C_j + (1-beta2) * sum/rows.
-//   rbar_kernel    one CTA per factored tensor: mean(R) in a fixed tree order.
+//   rbar_kernel    one CTA per factored tensor: mean(R) in a fixed tree order,
+//                  stored with its correctly rounded reciprocal.
 // The step kernel then reads vhat_ij = R_i * C_j / mean(R).
 #include <cuda_runtime.h>
 
@@ -106,7 +107,7 @@ __global__ void __launch_bounds__(256) rbar_kernel(const __grid_constant__ Facto
     for (int k = blockIdx.x; k < P.n_factored; k += gridDim.x) {
         const DevTensor& d = P.tensors[__ldg(P.factored_ids + k)];
         const float mean = block_mean(d.vrow, d.rows, red);
-        if (threadIdx.x == 0) *d.rbar = mean;
+        if (threadIdx.x == 0) *reinterpret_cast<float2*>(d.rbar) = make_float2(mean, __frcp_rn(mean));
     }
 }
 

@@ -9,8 +9,9 @@
 namespace q4 {
 
 constexpr int kBlock = 128;        // elements per quantisation block
-constexpr int kThreads = 256;      // threads per CTA of the step kernel
-constexpr int kWarps = kThreads / 32;
+constexpr int kStepWarps = 16;     // warps per CTA of the step kernel
+constexpr int kStepThreads = kStepWarps * 32;
+constexpr int kStages = 4;         // staging buffers per warp (tiles in flight)
 constexpr int kVLut = 2048;        // entries of the log-bucket candidate tables
 
 // Per-tensor descriptor as the kernels read it (one 128-byte record).
@@ -30,12 +31,20 @@ struct DevTensor {
     uint64_t elem_offset;
     uint32_t tensor_id;
     uint32_t flags;        // DF_* bits
-    float* rbar;           // factored: device scalar mean(R) of this step
+    float* rbar;           // factored: {mean(R), RN(1/mean(R))} of this step
     float* colpart;        // factored: column partial sums [n_slabs][cols]
 };
 static_assert(sizeof(DevTensor) == 128, "descriptor must stay 128 bytes");
 
-enum : uint32_t { DF_M_SR = 1u, DF_FACTORED = 2u, DF_BF16 = 4u };
+enum : uint32_t {
+    DF_M_SR = 1u,        // NF4 stochastic rounding of m this step
+    DF_FACTORED = 2u,    // factored v (row/column statistics)
+    DF_BF16 = 4u,        // write the BF16 weight copy
+    DF_CVEC = 8u,        // factored with cols % 8 == 0 and 16-B aligned v_col
+};
+
+// Bits of the step's device status word (first word of the workspace).
+enum : uint32_t { ST_STAGE_TIMEOUT = 1u };
 
 // Codebooks and candidate tables (built on the host by q4_tables.cpp).
 struct Tables {
@@ -61,12 +70,14 @@ bool build_tables(int vbook, Tables* t);
 
 struct StepParams {
     const DevTensor* tensors;
+    uint32_t* status;             // device status word, zeroed by the upload
     const int64_t* pair_prefix;   // n+1 entries: first block-pair of each tensor
     int64_t total_pairs;
     int n_tensors;
     int recipe;
     float beta1, beta2, omb1, omb2, c2, eps, decay, step_size;
     uint32_t step;
+    int fast_math;                // eps and c2 keep 1/(sqrt(v) c2 + eps) in the fast domain
     uint32_t round_keys[20];      // Philox key schedule: (k0, k1) for rounds 0..9
     Tables tab;
 };

@@ -1,36 +1,62 @@
 // Fused 4-bit AdamW step kernel for sm_103a.
 //
-// One warp processes one pair of consecutive 128-element blocks of a tensor:
-// lanes 0-15 own block 2p, lanes 16-31 block 2p+1, and lane j of a half owns
-// the 8 consecutive elements 8j..8j+7 of its block.  Per lane the step loads
-// 16 B of BF16 gradient, 32 B of FP32 master weight and one 32-bit word of m
-// codes and of v codes; per block one FP32 scale of m and of v.  It writes the
-// same amounts back plus 16 B of BF16 weights.  Block reductions (absmax, the
-// EDEN sums) are half-warp shuffles; per-block tables (dequantisation levels,
-// scaled thresholds and levels, ZIP-SR preconditioner levels) are built by the
-// 16 lanes of a half in shared memory and read by table lookup.
+// Work unit: a tile = one pair of consecutive 128-element blocks of a tensor
+// (256 parameters).  One warp computes one tile: lanes 0-15 own block 2p,
+// lanes 16-31 block 2p+1, and lane j of a half owns the 8 consecutive
+// elements 8j..8j+7 of its block.
 //
-// The grid is persistent: warps stride over the global list of block pairs of
-// all tensors (tensor-chunk table = prefix sums of pairs per tensor); a warp's
-// pairs increase monotonically, so its tensor index only moves forward.
+// Data movement.  The grid is persistent (one 16-warp CTA per SM); warp w of
+// W takes tiles w, w+W, w+2W, ... of the global tile list of all tensors (the
+// tensor-chunk table is the prefix sum of tiles per tensor).  Each warp keeps
+// a ring of kStages shared-memory staging buffers: while it computes tile k,
+// tiles k+1 .. k+kStages-1 are in flight.  Lane 0 fills a buffer with
+// cp.async.bulk copies (BF16 gradient, FP32 master weight, packed m and v
+// code words; the tensor memory access unit moves whole 16-byte granules) and
+// four 4-byte cp.async copies (the block scales, which are only 4-byte
+// aligned), all completing on the buffer's mbarrier.  A tile whose length is
+// not a multiple of 8 elements (a tensor's ragged tail) is read directly from
+// global memory instead.  Results (FP32 and BF16 weights, codes, scales) are
+// written straight from registers with coalesced streaming stores.  Every
+// wait on an mbarrier is bounded by a clock limit; on expiry the warp sets
+// ST_STAGE_TIMEOUT in the step's status word, drains its own copies (again
+// with a limit) and exits.
 //
-// The arithmetic follows the per-element and per-block definitions of the
-// method (listing page "Rounding in Preconditioner Space", Abstract and
-// Tables 1-2; news page paragraphs 2-4; AReno docs "State representation")
-// operation by operation in FP32 with round-to-nearest intrinsics, so that
-// codes and scales are bit-identical to a plain sequential evaluation.
+// Arithmetic.  The method's per-element and per-block definitions (listing
+// page "Rounding in Preconditioner Space", Abstract and Tables 1-2; news page
+// paragraphs 2-4; AReno docs "State representation") are evaluated operation
+// by operation in FP32 with round-to-nearest, so that codes, scales and
+// weights are bit-identical to a plain sequential evaluation.  The square
+// root and reciprocal of r = 1/(sqrt(v') c2 + eps) and the factored quotient
+// use the correctly rounded sequences of q4_fastmath.cuh where a lane's
+// inputs are inside their verified domains, and the IEEE intrinsics
+// otherwise.  Block reductions (absmax, the EDEN sums) are half-warp
+// shuffles; per-block tables (dequantisation levels at the old scale,
+// thresholds, levels and ZIP-SR preconditioner levels at the new scale) are
+// built by the 16 lanes of a half in shared memory and read by table lookup.
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
 #include <cstdint>
 
+#include "q4_fastmath.cuh"
 #include "q4_internal.h"
 
 namespace q4 {
 namespace {
 
-constexpr float kMagic = 12582912.0f;   // 1.5 * 2^23: adding it rounds to an integer in the low mantissa bits
+constexpr float kMagic = 12582912.0f;                // 1.5 * 2^23: rounds to an integer in the low mantissa bits
 constexpr float kTwoM24 = 5.9604644775390625e-08f;   // 2^-24
+constexpr long long kWaitCycles = 2000000000ll;      // about one second at the SM clock
+
+struct __align__(16) Stage {
+    uint4 grad[32];     // 256 BF16 gradients
+    float4 param[64];   // 256 FP32 master weights
+    uint32_t mc[32];    // m code words of both blocks (64 bytes each)
+    uint32_t vc[32];    // v code words of both blocks
+    float ms[2];        // m scales of both blocks
+    float vs[2];        // v scales of both blocks
+};
+static_assert(sizeof(Stage) % 16 == 0, "stage buffers must keep 16-byte alignment");
 
 struct __align__(16) WarpTables {
     float deqm[32];   // [half][16] NF4 level * old s_m
@@ -41,36 +67,98 @@ struct __align__(16) WarpTables {
     float2 rd[32];    // [half][16] (r_k, (r_k - r_{k+1}) * 2^-24) for ZIP-SR
 };
 
-struct SmemAll {
+struct __align__(16) WarpSmem {
+    Stage st[kStages];
+    WarpTables wt;
+    DevTensor desc;                      // descriptor of the tensor being computed
+    unsigned long long bar[kStages];     // one mbarrier per staging buffer
+};
+
+struct __align__(16) SmemAll {
     float vl[16];     // unscaled v levels (EDEN reconstruction)
     uint8_t lut_nf4_t[64];
     uint8_t lut_nf4_l[64];
     uint8_t lut_v_l[kVLut];
     uint8_t lut_v_t[kVLut];
-    WarpTables w[kWarps];
+    WarpSmem w[kStepWarps];
 };
 
+// ----------------------------------------------------------------- PTX helpers
+__device__ __forceinline__ uint32_t smem_addr(const void* p) { return (uint32_t)__cvta_generic_to_shared(p); }
+
+__device__ __forceinline__ void mbar_init(unsigned long long* bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_addr(bar)), "r"(count) : "memory");
+}
+__device__ __forceinline__ void mbar_arrive_expect_tx(unsigned long long* bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_addr(bar)), "r"(bytes)
+                 : "memory");
+}
+__device__ __forceinline__ void mbar_arrive(unsigned long long* bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_addr(bar)) : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(unsigned long long* bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_addr(bar)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+// Waits for the phase with the given parity; false if it has not completed
+// within kWaitCycles.
+__device__ __forceinline__ bool mbar_wait_bounded(unsigned long long* bar, uint32_t parity) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const long long t0 = clock64();
+    while (!mbar_try_wait(bar, parity)) {
+        if (clock64() - t0 > kWaitCycles) return false;
+    }
+    return true;
+}
+__device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t bytes, unsigned long long* bar,
+                                          uint64_t policy) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1], %2, [%3], %4;" ::"r"(
+            smem_addr(dst)),
+        "l"(src), "r"(bytes), "r"(smem_addr(bar)), "l"(policy)
+        : "memory");
+}
+__device__ __forceinline__ void cp_async4(void* dst, const void* src) {
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(smem_addr(dst)), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async_arrive_noinc(unsigned long long* bar) {
+    asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(smem_addr(bar)) : "memory");
+}
+__device__ __forceinline__ uint64_t evict_first_policy() {
+    uint64_t p;
+    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+    return p;
+}
+
+// ----------------------------------------------------------------- arithmetic helpers
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
     __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
     return *reinterpret_cast<uint32_t*>(&v);
 }
 __device__ __forceinline__ uint16_t to_bf16(float x) { return __bfloat16_as_ushort(__float2bfloat16_rn(x)); }
-
 __device__ __forceinline__ float bf16lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf16hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
 
-// Philox4x32-10 (Salmon et al., SC'11) with a precomputed key schedule.
+// Philox4x32-10 (Salmon et al., SC'11) with a precomputed key schedule; each
+// round's two 32x32->64 products are single wide multiplies.
 __device__ __forceinline__ uint4 philox(uint32_t c0, uint32_t c1, uint32_t c2, uint32_t c3, const uint32_t* rk) {
 #pragma unroll
     for (int r = 0; r < 10; ++r) {
-        const uint32_t hi0 = __umulhi(0xD2511F53u, c0), lo0 = 0xD2511F53u * c0;
-        const uint32_t hi1 = __umulhi(0xCD9E8D57u, c2), lo1 = 0xCD9E8D57u * c2;
-        const uint32_t n0 = hi1 ^ c1 ^ rk[2 * r];
-        const uint32_t n2 = hi0 ^ c3 ^ rk[2 * r + 1];
+        const uint64_t p0 = (uint64_t)c0 * 0xD2511F53u;
+        const uint64_t p1 = (uint64_t)c2 * 0xCD9E8D57u;
+        const uint32_t n0 = (uint32_t)(p1 >> 32) ^ c1 ^ rk[2 * r];
+        const uint32_t n2 = (uint32_t)(p0 >> 32) ^ c3 ^ rk[2 * r + 1];
         c0 = n0;
-        c1 = lo1;
+        c1 = (uint32_t)p1;
         c2 = n2;
-        c3 = lo0;
+        c3 = (uint32_t)p0;
     }
     return make_uint4(c0, c1, c2, c3);
 }
@@ -96,51 +184,89 @@ __device__ __forceinline__ float half_max(float x) {
 // sequential search.
 __device__ __forceinline__ bool scale_in_fast_range(float s) { return s >= 0x1p-90f && s <= 0x1p90f; }
 
-// Per-element core shared by every recipe.  Returns r = 1/(sqrt(v')*c2+eps).
-__device__ __forceinline__ void adamw_core(const StepParams& P, float g, float m, float v, float& theta, float& m1,
-                                           float& v1, float& r, bool fact, float vhat) {
-    m1 = __fmaf_rn(P.beta1, m, __fmul_rn(P.omb1, g));
-    v1 = fact ? vhat : __fmaf_rn(P.beta2, v, __fmul_rn(P.omb2, __fmul_rn(g, g)));
-    r = __frcp_rn(__fadd_rn(__fmul_rn(__fsqrt_rn(v1), P.c2), P.eps));
-    theta = __fsub_rn(__fmul_rn(theta, P.decay), __fmul_rn(P.step_size, __fmul_rn(m1, r)));
+// x >= 0 (or NaN) lies in (0, 2^-100): outside the fast square root's domain.
+__device__ __forceinline__ bool tiny_positive(float x) { return (__float_as_uint(x) - 1u) < 0x0d7fffffu; }
+
+// x >= 0 lies in {0} or [2^-100, 2^100]: the quotient's safe range.
+__device__ __forceinline__ bool quot_range_ok(float x) {
+    const uint32_t b = __float_as_uint(x);
+    return b == 0u || (b - 0x0d800000u) <= (0x71800000u - 0x0d800000u);
 }
 
+// r = 1/(sqrt(v') c2 + eps), correctly rounded either way.
+template <bool FAST>
+__device__ __forceinline__ float precond(const StepParams& P, float v1) {
+    if (FAST) {
+        const float d = __fadd_rn(__fmul_rn(sqrt_rn_normal<0>(v1), P.c2), P.eps);
+        return rcp_rn_normal<1>(d);
+    }
+    return __frcp_rn(__fadd_rn(__fmul_rn(__fsqrt_rn(v1), P.c2), P.eps));
+}
+
+// The update of 8 elements: r_i and theta'_i.
+template <bool FAST>
+__device__ __forceinline__ void update8(const StepParams& P, const float m1[8], const float v1[8], float th[8],
+                                        float r[8]) {
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        r[i] = precond<FAST>(P, v1[i]);
+        th[i] = __fsub_rn(__fmul_rn(th[i], P.decay), __fmul_rn(P.step_size, __fmul_rn(m1[i], r[i])));
+    }
+}
+
+// ----------------------------------------------------------------- one tile
+// `st` is the staged tile or nullptr (ragged tail: read from global memory).
 template <int RECIPE>
-__device__ __forceinline__ void process_pair(const StepParams& P, const DevTensor& d, int64_t pair, int lane,
-                                             SmemAll& sm, const float my_nf4, const float my_nf4t,
-                                             const float my_vl, const float my_vt) {
-    WarpTables& wt = sm.w[threadIdx.x >> 5];
+__device__ __forceinline__ void compute_tile(const StepParams& P, const DevTensor& d, int64_t pair,
+                                             const Stage* st, int lane, SmemAll& sm, WarpTables& wt,
+                                             const float my_nf4, const float my_nf4t, const float my_vl,
+                                             const float my_vt) {
     const int half = lane >> 4, j = lane & 15, hb = half * 16;
-    const int64_t nblk = (d.numel + kBlock - 1) / kBlock;
+    const int64_t numel = d.numel;
+    const int64_t nblk = (numel + kBlock - 1) / kBlock;
     const int64_t blk = pair * 2 + half;
     const bool blk_ok = blk < nblk;
     const int64_t e0 = blk * kBlock + j * 8;
-    const int64_t rem = d.numel - e0;
+    const int64_t rem = numel - e0;
     const int nvalid = rem >= 8 ? 8 : (rem > 0 ? (int)rem : 0);
-    const bool fact = (RECIPE == Q4_RECIPE_FACTORED) && (d.flags & DF_FACTORED);
-    const bool m_sr = (d.flags & DF_M_SR) != 0;
+    const uint32_t flags = d.flags;
+    const bool fact = (RECIPE == Q4_RECIPE_FACTORED) && (flags & DF_FACTORED);
+    const bool m_sr = (flags & DF_M_SR) != 0;
 
     // ---- loads -------------------------------------------------------
     float g[8], th[8];
     uint32_t qmw = 0, qvw = 0;
     float sm_old = 0.f, sv_old = 0.f;
-    if (blk_ok) {
-        sm_old = __ldg(d.ms + blk);
-        qmw = __ldg(reinterpret_cast<const uint32_t*>(d.mc + blk * 64) + j);
-        if (!fact) {
-            sv_old = __ldg(d.vs + blk);
-            qvw = __ldg(reinterpret_cast<const uint32_t*>(d.vc + blk * 64) + j);
+    if (st != nullptr) {
+        if (blk_ok) {
+            sm_old = st->ms[half];
+            qmw = st->mc[hb + j];
+            if (!fact) {
+                sv_old = st->vs[half];
+                qvw = st->vc[hb + j];
+            }
         }
-    }
-    if (nvalid == 8) {
-        const uint4 gw = __ldcs(reinterpret_cast<const uint4*>(d.grad + e0));
-        const float4 t0 = __ldcs(reinterpret_cast<const float4*>(d.param + e0));
-        const float4 t1 = __ldcs(reinterpret_cast<const float4*>(d.param + e0 + 4));
-        g[0] = bf16lo(gw.x); g[1] = bf16hi(gw.x); g[2] = bf16lo(gw.y); g[3] = bf16hi(gw.y);
-        g[4] = bf16lo(gw.z); g[5] = bf16hi(gw.z); g[6] = bf16lo(gw.w); g[7] = bf16hi(gw.w);
-        th[0] = t0.x; th[1] = t0.y; th[2] = t0.z; th[3] = t0.w;
-        th[4] = t1.x; th[5] = t1.y; th[6] = t1.z; th[7] = t1.w;
+        if (nvalid == 8) {
+            const uint4 gw = st->grad[hb + j];
+            const float4 t0 = st->param[2 * (hb + j)];
+            const float4 t1 = st->param[2 * (hb + j) + 1];
+            g[0] = bf16lo(gw.x); g[1] = bf16hi(gw.x); g[2] = bf16lo(gw.y); g[3] = bf16hi(gw.y);
+            g[4] = bf16lo(gw.z); g[5] = bf16hi(gw.z); g[6] = bf16lo(gw.w); g[7] = bf16hi(gw.w);
+            th[0] = t0.x; th[1] = t0.y; th[2] = t0.z; th[3] = t0.w;
+            th[4] = t1.x; th[5] = t1.y; th[6] = t1.z; th[7] = t1.w;
+        } else {
+#pragma unroll
+            for (int i = 0; i < 8; ++i) g[i] = th[i] = 0.f;
+        }
     } else {
+        if (blk_ok) {
+            sm_old = __ldg(d.ms + blk);
+            qmw = __ldg(reinterpret_cast<const uint32_t*>(d.mc + blk * 64) + j);
+            if (!fact) {
+                sv_old = __ldg(d.vs + blk);
+                qvw = __ldg(reinterpret_cast<const uint32_t*>(d.vc + blk * 64) + j);
+            }
+        }
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
             g[i] = 0.f;
@@ -157,44 +283,96 @@ __device__ __forceinline__ void process_pair(const StepParams& P, const DevTenso
     if (!fact) wt.deqv[hb + j] = __fmul_rn(my_vl, sv_old);
     __syncwarp();
 
-    // factored second moment: vhat = R_i * C_j / mean(R)
-    float rbar = 0.f;
-    int64_t frow = 0, fcol = 0;
+    // ---- moments ------------------------------------------------------
+    float m1[8], v1[8], r[8];
+    bool lane_fast = P.fast_math != 0;
     if (fact) {
-        rbar = __ldg(d.rbar);
-        if (nvalid > 0) {
-            frow = e0 / d.cols;
-            fcol = e0 - frow * d.cols;
+        // vhat = R_i * C_j / mean(R); mean(R) and RN(1/mean(R)) come from the
+        // statistics pass.
+        const float2 rb = *reinterpret_cast<const float2*>(d.rbar);
+        const bool rb_ok = rb.x != 0.f && quot_range_ok(rb.x);
+        float R[8], C[8];
+        if (nvalid == 8 && (flags & DF_CVEC)) {
+            const uint32_t cols = (uint32_t)d.cols;
+            const uint32_t frow = (uint32_t)e0 / cols;
+            const uint32_t fcol = (uint32_t)e0 - frow * cols;
+            const float Ri = __ldg(d.vrow + frow);
+            const float4 c0 = __ldg(reinterpret_cast<const float4*>(d.vcol + fcol));
+            const float4 c1 = __ldg(reinterpret_cast<const float4*>(d.vcol + fcol + 4));
+            C[0] = c0.x; C[1] = c0.y; C[2] = c0.z; C[3] = c0.w;
+            C[4] = c1.x; C[5] = c1.y; C[6] = c1.z; C[7] = c1.w;
+#pragma unroll
+            for (int i = 0; i < 8; ++i) R[i] = Ri;
+        } else {
+            int64_t frow = 0, fcol = 0;
+            if (nvalid > 0) {
+                frow = e0 / d.cols;
+                fcol = e0 - frow * d.cols;
+            }
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                R[i] = 0.f;
+                C[i] = 0.f;
+                if (i < nvalid) {
+                    R[i] = __ldg(d.vrow + frow);
+                    C[i] = __ldg(d.vcol + fcol);
+                    if (++fcol == d.cols) { fcol = 0; ++frow; }
+                }
+            }
+        }
+        bool q_fast = rb_ok;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            const float p = __fmul_rn(R[i], C[i]);
+            const float q = div_rn_by_rcp(p, rb.x, rb.y);
+            q_fast = q_fast && quot_range_ok(p) && quot_range_ok(q);
+            v1[i] = (rb.x == 0.f) ? 0.f : q;
+        }
+        if (!q_fast) {
+#pragma unroll
+            for (int i = 0; i < 8; ++i) v1[i] = (rb.x == 0.f) ? 0.f : __fdiv_rn(__fmul_rn(R[i], C[i]), rb.x);
+        }
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            const float m = wt.deqm[hb + ((qmw >> (4 * i)) & 15u)];
+            m1[i] = __fmaf_rn(P.beta1, m, __fmul_rn(P.omb1, g[i]));
+            if (i >= nvalid) v1[i] = 0.f;
+        }
+    } else {
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            const float m = wt.deqm[hb + ((qmw >> (4 * i)) & 15u)];
+            const float v = wt.deqv[hb + ((qvw >> (4 * i)) & 15u)];
+            m1[i] = __fmaf_rn(P.beta1, m, __fmul_rn(P.omb1, g[i]));
+            v1[i] = __fmaf_rn(P.beta2, v, __fmul_rn(P.omb2, __fmul_rn(g[i], g[i])));
         }
     }
-
-    // ---- per-element AdamW --------------------------------------------
-    float m1[8], v1[8], r[8];
     float amax = 0.f, vmax = 0.f;
+    bool tiny = false;
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
-        const float m = wt.deqm[hb + ((qmw >> (4 * i)) & 15u)];
-        float v = 0.f, vhat = 0.f;
-        if (fact) {
-            if (i < nvalid) {
-                const float R = __ldg(d.vrow + frow), C = __ldg(d.vcol + fcol);
-                vhat = (rbar == 0.f) ? 0.f : __fdiv_rn(__fmul_rn(R, C), rbar);
-                if (++fcol == d.cols) { fcol = 0; ++frow; }
-            }
-        } else {
-            v = wt.deqv[hb + ((qvw >> (4 * i)) & 15u)];
-        }
-        adamw_core(P, g[i], m, v, th[i], m1[i], v1[i], r[i], fact, vhat);
+        tiny = tiny || tiny_positive(v1[i]);
+        vmax = fmaxf(vmax, v1[i]);
+    }
+    lane_fast = lane_fast && !tiny && vmax < INFINITY;
+
+    // ---- update ---------------------------------------------------------
+    if (lane_fast) update8<true>(P, m1, v1, th, r);
+    else update8<false>(P, m1, v1, th, r);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
         if (i >= nvalid) { m1[i] = 0.f; v1[i] = 0.f; }
         amax = fmaxf(amax, fabsf(m1[i]));
-        vmax = fmaxf(vmax, fabsf(v1[i]));
     }
+    vmax = 0.f;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) vmax = fmaxf(vmax, v1[i]);
 
     // ---- weights out ----------------------------------------------------
     if (nvalid == 8) {
         __stcs(reinterpret_cast<float4*>(d.param + e0), make_float4(th[0], th[1], th[2], th[3]));
         __stcs(reinterpret_cast<float4*>(d.param + e0 + 4), make_float4(th[4], th[5], th[6], th[7]));
-        if (d.flags & DF_BF16) {
+        if (flags & DF_BF16) {
             uint4 o;
             o.x = pack_bf16x2(th[0], th[1]);
             o.y = pack_bf16x2(th[2], th[3]);
@@ -207,7 +385,7 @@ __device__ __forceinline__ void process_pair(const StepParams& P, const DevTenso
         for (int i = 0; i < 8; ++i) {
             if (i < nvalid) {
                 d.param[e0 + i] = th[i];
-                if (d.flags & DF_BF16) d.bf16[e0 + i] = to_bf16(th[i]);
+                if (flags & DF_BF16) d.bf16[e0 + i] = to_bf16(th[i]);
             }
         }
     }
@@ -221,7 +399,7 @@ __device__ __forceinline__ void process_pair(const StepParams& P, const DevTenso
     if (m_sr) wt.am[hb + j] = __fmul_rn(my_nf4, s_m);
     if (RECIPE == Q4_RECIPE_ZIP_SR) {
         const float a = __fmul_rn(my_vl, s_v);
-        const float rk = __frcp_rn(__fadd_rn(__fmul_rn(__fsqrt_rn(a), P.c2), P.eps));
+        const float rk = (P.fast_math && scale_in_fast_range(s_v)) ? precond<true>(P, a) : precond<false>(P, a);
         const float rk1 = __shfl_down_sync(0xffffffffu, rk, 1);
         wt.av[hb + j] = a;
         wt.rd[hb + j] = make_float2(rk, j < 15 ? __fmul_rn(__fsub_rn(rk, rk1), kTwoM24) : 0.f);
@@ -365,12 +543,17 @@ __device__ __forceinline__ void process_pair(const StepParams& P, const DevTenso
             if (!fact) d.vs[blk] = sv_store;
         }
     }
-    __syncwarp();
 }
 
+// ----------------------------------------------------------------- the kernel
 template <int RECIPE>
-__global__ void __launch_bounds__(kThreads) step_kernel(const __grid_constant__ StepParams P) {
-    __shared__ SmemAll sm;
+__global__ void __launch_bounds__(kStepThreads, 1) step_kernel(const __grid_constant__ StepParams P) {
+    extern __shared__ __align__(128) unsigned char smem_raw[];
+    SmemAll& sm = *reinterpret_cast<SmemAll*>(smem_raw);
+    const int lane = threadIdx.x & 31;
+    const int warp = threadIdx.x >> 5;
+    WarpSmem& ws = sm.w[warp];
+
     if (threadIdx.x < 16) sm.vl[threadIdx.x] = P.tab.vl[threadIdx.x];
     for (int i = threadIdx.x; i < 64; i += blockDim.x) {
         sm.lut_nf4_t[i] = P.tab.lut_nf4_t[i];
@@ -380,51 +563,177 @@ __global__ void __launch_bounds__(kThreads) step_kernel(const __grid_constant__ 
         reinterpret_cast<uint32_t*>(sm.lut_v_l)[i] = reinterpret_cast<const uint32_t*>(P.tab.lut_v_l)[i];
         reinterpret_cast<uint32_t*>(sm.lut_v_t)[i] = reinterpret_cast<const uint32_t*>(P.tab.lut_v_t)[i];
     }
+    if (lane == 0) {
+        // count 2: the issuing lane's arrive.expect_tx and the arrive that
+        // cp.async.mbarrier.arrive.noinc triggers when the scale copies land
+        for (int s = 0; s < kStages; ++s) mbar_init(&ws.bar[s], 2);
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
     __syncthreads();
 
-    const int lane = threadIdx.x & 31;
     const int j = lane & 15;
     const float my_nf4 = P.tab.nf4[j], my_nf4t = P.tab.nf4_t[j];
     const float my_vl = P.tab.vl[j], my_vt = P.tab.vt[j];
+    const uint64_t policy = evict_first_policy();
 
-    const int64_t W = (int64_t)gridDim.x * kWarps;
-    int t = 0;
-    int loaded = -1;
-    DevTensor d;
-    for (int64_t pair = (int64_t)blockIdx.x * kWarps + (threadIdx.x >> 5); pair < P.total_pairs; pair += W) {
-        while (pair >= __ldg(P.pair_prefix + t + 1)) ++t;
-        if (t != loaded) {
-            d = P.tensors[t];
-            loaded = t;
+    const int64_t gw = (int64_t)blockIdx.x * kStepWarps + warp;
+    const int64_t W = (int64_t)gridDim.x * kStepWarps;
+    const int64_t n_it = gw < P.total_pairs ? (P.total_pairs - 1 - gw) / W + 1 : 0;
+
+    // Issue cursor: tensor of the next tile to stage and the fields the copies need.
+    int ti = 0;
+    int64_t ib = 0, ie = __ldg(P.pair_prefix + 1);
+    const uint16_t* i_grad = nullptr;
+    const float* i_param = nullptr;
+    const uint8_t* i_mc = nullptr;
+    const uint8_t* i_vc = nullptr;
+    const float* i_ms = nullptr;
+    const float* i_vs = nullptr;
+    int64_t i_numel = 0;
+    bool i_fact = false;
+    bool i_loaded = false;
+
+    auto issue = [&](int64_t it) {
+        const int64_t pair = gw + it * W;
+        bool moved = !i_loaded;
+        while (pair >= ie) {
+            ++ti;
+            ib = ie;
+            ie = __ldg(P.pair_prefix + ti + 1);
+            moved = true;
         }
-        process_pair<RECIPE>(P, d, pair - __ldg(P.pair_prefix + t), lane, sm, my_nf4, my_nf4t, my_vl, my_vt);
+        if (moved) {
+            const DevTensor* dt = P.tensors + ti;
+            i_grad = dt->grad;
+            i_param = dt->param;
+            i_mc = dt->mc;
+            i_vc = dt->vc;
+            i_ms = dt->ms;
+            i_vs = dt->vs;
+            i_numel = dt->numel;
+            i_fact = (RECIPE == Q4_RECIPE_FACTORED) && (dt->flags & DF_FACTORED);
+            i_loaded = true;
+        }
+        if (lane == 0) {
+            const int s = (int)(it % kStages);
+            Stage& st = ws.st[s];
+            unsigned long long* bar = &ws.bar[s];
+            const int64_t blk0 = (pair - ib) * 2;
+            const int64_t nblk = (i_numel + kBlock - 1) / kBlock;
+            const int nb = (nblk - blk0) >= 2 ? 2 : 1;
+            const int64_t e0 = blk0 * kBlock;
+            const int64_t left = i_numel - e0;
+            const uint32_t nel = left >= 2 * kBlock ? 2 * kBlock : (uint32_t)left;
+            if ((nel & 7u) == 0) {
+                const uint32_t cbytes = (uint32_t)nb * 64u;
+                const uint32_t bytes = nel * 2u + nel * 4u + cbytes + (i_fact ? 0u : cbytes);
+                asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+                mbar_arrive_expect_tx(bar, bytes);
+                bulk_load(st.grad, i_grad + e0, nel * 2u, bar, policy);
+                bulk_load(st.param, i_param + e0, nel * 4u, bar, policy);
+                bulk_load(st.mc, i_mc + blk0 * 64, cbytes, bar, policy);
+                if (!i_fact) bulk_load(st.vc, i_vc + blk0 * 64, cbytes, bar, policy);
+                cp_async4(&st.ms[0], i_ms + blk0);
+                if (nb == 2) cp_async4(&st.ms[1], i_ms + blk0 + 1);
+                if (!i_fact) {
+                    cp_async4(&st.vs[0], i_vs + blk0);
+                    if (nb == 2) cp_async4(&st.vs[1], i_vs + blk0 + 1);
+                }
+                cp_async_arrive_noinc(bar);
+            } else {
+                // ragged tail tile: computed from global memory; complete the phase now
+                mbar_arrive(bar);
+                mbar_arrive(bar);
+            }
+        }
+    };
+
+    const int64_t pro = n_it < kStages - 1 ? n_it : kStages - 1;
+    for (int64_t it = 0; it < pro; ++it) issue(it);
+    __syncwarp();
+
+    // Compute cursor.
+    int ci = -1;
+    int64_t cb = 0, ce = 0;
+    for (int64_t it = 0; it < n_it; ++it) {
+        if (it + kStages - 1 < n_it) issue(it + kStages - 1);
+        const int s = (int)(it % kStages);
+        const bool ok = __all_sync(0xffffffffu, mbar_wait_bounded(&ws.bar[s], (uint32_t)((it / kStages) & 1)));
+        if (!ok) {
+            if (lane == 0) atomicOr(P.status, ST_STAGE_TIMEOUT);
+            // drain the copies this warp still has in flight, then leave
+            const int64_t last = (it + kStages - 1 < n_it) ? it + kStages - 1 : n_it - 1;
+            for (int64_t k = it + 1; k <= last; ++k)
+                (void)mbar_wait_bounded(&ws.bar[k % kStages], (uint32_t)((k / kStages) & 1));
+            return;
+        }
+        const int64_t pair = gw + it * W;
+        if (pair >= ce) {
+            while (pair >= ce) {
+                ++ci;
+                cb = ce;
+                ce = __ldg(P.pair_prefix + ci + 1);
+            }
+            reinterpret_cast<uint32_t*>(&ws.desc)[lane] = __ldg(reinterpret_cast<const uint32_t*>(P.tensors + ci) + lane);
+            __syncwarp();
+        }
+        const int64_t pl = pair - cb;
+        const int64_t left = ws.desc.numel - pl * 2 * kBlock;
+        const bool staged = ((left >= 2 * kBlock ? 2 * kBlock : left) & 7) == 0;
+        compute_tile<RECIPE>(P, ws.desc, pl, staged ? &ws.st[s] : nullptr, lane, sm, ws.wt, my_nf4, my_nf4t,
+                             my_vl, my_vt);
+        __syncwarp();
     }
+}
+
+size_t step_smem_bytes() { return sizeof(SmemAll); }
+
+template <int RECIPE>
+int configure(int device) {
+    static bool done[64] = {false};
+    if (device < 0 || device >= 64) device = 0;
+    if (done[device]) return 0;
+    const cudaError_t e = cudaFuncSetAttribute(step_kernel<RECIPE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                               (int)step_smem_bytes());
+    if (e == cudaSuccess) done[device] = true;
+    return (int)e;
 }
 
 }  // namespace
 
 int step_grid_size(int device, int64_t total_pairs) {
     static int cached_sms[64] = {0};
-    static int cached_occ[64] = {0};
     if (device < 0 || device >= 64) device = 0;
     if (cached_sms[device] == 0) {
-        int sms = 0, occ = 0;
+        int sms = 0;
         cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, device);
-        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, step_kernel<Q4_RECIPE_ZIP_SR>, kThreads, 0);
         cached_sms[device] = sms > 0 ? sms : 1;
-        cached_occ[device] = occ > 0 ? occ : 1;
     }
-    const int64_t full = (int64_t)cached_sms[device] * cached_occ[device];
-    const int64_t need = (total_pairs + kWarps - 1) / kWarps;
+    const int64_t full = cached_sms[device];   // one CTA per SM (shared memory holds one)
+    const int64_t need = (total_pairs + kStepWarps - 1) / kStepWarps;
     return (int)(need < full ? (need > 0 ? need : 1) : full);
 }
 
 int launch_step(const StepParams& p, int grid, void* stream) {
     cudaStream_t s = static_cast<cudaStream_t>(stream);
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return (int)e;
+    const size_t smem = step_smem_bytes();
+    int ce = 0;
     switch (p.recipe) {
-        case Q4_RECIPE_ZIP_SR: step_kernel<Q4_RECIPE_ZIP_SR><<<grid, kThreads, 0, s>>>(p); break;
-        case Q4_RECIPE_ZE_EDEN: step_kernel<Q4_RECIPE_ZE_EDEN><<<grid, kThreads, 0, s>>>(p); break;
-        default: step_kernel<Q4_RECIPE_FACTORED><<<grid, kThreads, 0, s>>>(p); break;
+        case Q4_RECIPE_ZIP_SR:
+            if ((ce = configure<Q4_RECIPE_ZIP_SR>(dev))) return ce;
+            step_kernel<Q4_RECIPE_ZIP_SR><<<grid, kStepThreads, smem, s>>>(p);
+            break;
+        case Q4_RECIPE_ZE_EDEN:
+            if ((ce = configure<Q4_RECIPE_ZE_EDEN>(dev))) return ce;
+            step_kernel<Q4_RECIPE_ZE_EDEN><<<grid, kStepThreads, smem, s>>>(p);
+            break;
+        default:
+            if ((ce = configure<Q4_RECIPE_FACTORED>(dev))) return ce;
+            step_kernel<Q4_RECIPE_FACTORED><<<grid, kStepThreads, smem, s>>>(p);
+            break;
     }
     return (int)cudaGetLastError();
 }

@@ -198,6 +198,18 @@ int q4adamw_step(const q4adamw_tensor_t* t, int n, float lr, float beta1, float 
                  void* stream);
 
 /*
+ * Status word of the most recent q4adamw_step that used `workspace`
+ * (synchronises `stream`, then reads 4 bytes of the workspace).  0 means the
+ * step ran to completion.  Bit 0 (Q4_STATUS_STAGE_TIMEOUT) means a warp of the
+ * step kernel waited about a second for its staged input without seeing it
+ * arrive and stopped; the tensors it had not reached are not updated.  Other
+ * bits are reserved.  Returns Q4_EINVAL for NULL pointers, Q4_EWORKSPACE for a
+ * misaligned workspace, Q4_ECUDA if the copy fails.
+ */
+#define Q4_STATUS_STAGE_TIMEOUT 0x1u
+int q4adamw_step_status(const void* workspace, uint32_t* status, void* stream);
+
+/*
  * Decode the state of one tensor into FP32 device buffers of numel floats
  * (either may be NULL): m_out = NF4[qm]*s_m; v_out = V[qv]*s_v for packed v
  * (V = Dyn4 for ZIP-SR, Dyn4-NZ otherwise) or R_i*C_j/mean(R) for a factored
