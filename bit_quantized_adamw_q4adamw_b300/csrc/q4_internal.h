@@ -1,6 +1,8 @@
 // Internal definitions of the q4adamw CUDA library (not part of the ABI).
 #pragma once
 
+#include <vector_types.h>
+
 #include <cstddef>
 #include <cstdint>
 
@@ -12,7 +14,8 @@ constexpr int kBlock = 128;        // elements per quantisation block
 constexpr int kStepWarps = 16;     // warps per CTA of the step kernel
 constexpr int kStepThreads = kStepWarps * 32;
 constexpr int kStages = 4;         // staging buffers per warp (tiles in flight)
-constexpr int kVLut = 2048;        // entries of the log-bucket candidate tables
+constexpr int kVLut = 4096;        // entries of the log-bucket candidate tables
+                                   // (one per bits(x)>>19 of a non-negative float)
 
 // Per-tensor descriptor as the kernels read it (one 128-byte record).
 struct DevTensor {
@@ -56,6 +59,7 @@ struct Tables {
     uint8_t lut_nf4_l[64];   // NF4 level (cell) candidate by linear bucket
     uint8_t lut_v_l[kVLut];  // v level (cell) candidate by log bucket
     uint8_t lut_v_t[kVLut];  // v threshold candidate by log bucket
+    float2 nf4_bucket[64];   // NF4 RTN by linear bucket: {threshold of the candidate, candidate}
 };
 
 // Host-side tables: 0 = NF4, 1 = Dyn4, 2 = Dyn4-NZ.

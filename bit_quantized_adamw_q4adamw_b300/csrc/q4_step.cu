@@ -9,11 +9,11 @@
 // W takes tiles w, w+W, w+2W, ... of the global tile list of all tensors (the
 // tensor-chunk table is the prefix sum of tiles per tensor).  Each warp keeps
 // a ring of kStages shared-memory staging buffers: while it computes tile k,
-// tiles k+1 .. k+kStages-1 are in flight.  Lane 0 fills a buffer with
-// cp.async.bulk copies (BF16 gradient, FP32 master weight, packed m and v
-// code words; the tensor memory access unit moves whole 16-byte granules) and
-// four 4-byte cp.async copies (the block scales, which are only 4-byte
-// aligned), all completing on the buffer's mbarrier.  A tile whose length is
+// tiles k+1 .. k+kStages-1 are in flight.  Lanes 0-7 fill a buffer in one
+// pass: four cp.async.bulk copies (BF16 gradient, FP32 master weight, packed m
+// and v code words; the tensor memory access unit moves whole 16-byte
+// granules) and four 4-byte cp.async copies (the block scales, which are only
+// 4-byte aligned), all completing on the buffer's mbarrier.  A tile whose length is
 // not a multiple of 8 elements (a tensor's ragged tail) is read directly from
 // global memory instead.  Results (FP32 and BF16 weights, codes, scales) are
 // written straight from registers with coalesced streaming stores.  Every
@@ -33,6 +33,9 @@
 // shuffles; per-block tables (dequantisation levels at the old scale,
 // thresholds, levels and ZIP-SR preconditioner levels at the new scale) are
 // built by the 16 lanes of a half in shared memory and read by table lookup.
+// Tiles whose two blocks are complete take a branch-free path (byte-permute
+// decoding, one table entry per code decision); ragged tiles, the LM-head
+// stochastic rounding and scales outside the fast range take the general one.
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
@@ -58,29 +61,35 @@ struct __align__(16) Stage {
 };
 static_assert(sizeof(Stage) % 16 == 0, "stage buffers must keep 16-byte alignment");
 
-struct __align__(16) WarpTables {
-    float deqm[32];   // [half][16] NF4 level * old s_m
-    float deqv[32];   // [half][16] v level * old s_v
-    float tm[32];     // [half][16] NF4 threshold * new s_m
-    float am[32];     // [half][16] NF4 level * new s_m (LM-head SR)
-    float av[32];     // [half][16] v level * new s_v (ZIP-SR) or v threshold * new s_v (RTN)
-    float2 rd[32];    // [half][16] (r_k, (r_k - r_{k+1}) * 2^-24) for ZIP-SR
+// Per-warp tables.  256-byte aligned: the fast decoder forms the address of
+// deqm/deqv entries by replacing the low byte of the table's address with
+// 4*code + 64*half (+128 for v).
+struct __align__(256) WarpTables {
+    float deqm[32];        // [half][16] NF4 level * old s_m
+    float deqv[32];        // [half][16] v level * old s_v
+    float2 mt[2][64];      // fast path: [half][linear bucket] {NF4 threshold of the candidate * new s_m, candidate}
+    float4 ve[2][16][2];   // fast path: [half][cell] v search entry (32 bytes, see build_fast_tables)
+    float tm[32];          // general path: [half][16] NF4 threshold * new s_m
+    float am[32];          // [half][16] NF4 level * new s_m (LM-head SR)
+    float av[32];          // [half][16] v level * new s_v (ZIP-SR) or v threshold * new s_v (RTN)
+    float2 rd[32];         // [half][16] (r_k, (r_k - r_{k+1}) * 2^-24) for ZIP-SR
 };
 
-struct __align__(16) WarpSmem {
-    Stage st[kStages];
+struct __align__(256) WarpSmem {
     WarpTables wt;
+    Stage st[kStages];
     DevTensor desc;                      // descriptor of the tensor being computed
     unsigned long long bar[kStages];     // one mbarrier per staging buffer
 };
 
-struct __align__(16) SmemAll {
+struct __align__(256) SmemAll {
+    WarpSmem w[kStepWarps];
+    float2 nf4_bucket[64];  // NF4 RTN by linear bucket: {unscaled threshold of the candidate, candidate}
     float vl[16];     // unscaled v levels (EDEN reconstruction)
     uint8_t lut_nf4_t[64];
     uint8_t lut_nf4_l[64];
     uint8_t lut_v_l[kVLut];
     uint8_t lut_v_t[kVLut];
-    WarpSmem w[kStepWarps];
 };
 
 // ----------------------------------------------------------------- PTX helpers
@@ -130,6 +139,26 @@ __device__ __forceinline__ void cp_async4(void* dst, const void* src) {
 }
 __device__ __forceinline__ void cp_async_arrive_noinc(unsigned long long* bar) {
     asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(smem_addr(bar)) : "memory");
+}
+__device__ __forceinline__ float lds_f32(uint32_t a) {
+    float v;
+    asm volatile("ld.shared.f32 %0, [%1];" : "=f"(v) : "r"(a));
+    return v;
+}
+__device__ __forceinline__ float2 lds_f32x2(uint32_t a) {
+    float2 v;
+    asm volatile("ld.shared.v2.f32 {%0, %1}, [%2];" : "=f"(v.x), "=f"(v.y) : "r"(a));
+    return v;
+}
+__device__ __forceinline__ float4 lds_f32x4(uint32_t a) {
+    float4 v;
+    asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];" : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w) : "r"(a));
+    return v;
+}
+__device__ __forceinline__ uint32_t lds_u8(uint32_t a) {
+    uint32_t v;
+    asm volatile("ld.shared.u8 %0, [%1];" : "=r"(v) : "r"(a));
+    return v;
 }
 __device__ __forceinline__ uint64_t evict_first_policy() {
     uint64_t p;
@@ -214,187 +243,18 @@ __device__ __forceinline__ void update8(const StepParams& P, const float m1[8], 
     }
 }
 
-// ----------------------------------------------------------------- one tile
-// `st` is the staged tile or nullptr (ragged tail: read from global memory).
+// ----------------------------------------------------------------- requantisation, general path
+// Codes and scales of a tile from the updated moments m1, v1 (elements beyond
+// numel already zeroed), the new scales s_m, s_v and r (ZIP-SR).  Handles
+// every case: partial blocks, LM-head stochastic rounding, scales outside the
+// fast range (exact sequential searches).
 template <int RECIPE>
-__device__ __forceinline__ void compute_tile(const StepParams& P, const DevTensor& d, int64_t pair,
-                                             const Stage* st, int lane, SmemAll& sm, WarpTables& wt,
-                                             const float my_nf4, const float my_nf4t, const float my_vl,
-                                             const float my_vt) {
+__device__ __forceinline__ void requant_general(const StepParams& P, const DevTensor& d, const SmemAll& sm,
+                                                WarpTables& wt, int lane, int64_t blk, bool blk_ok, int64_t e0,
+                                                int nvalid, bool fact, bool m_sr, const float m1[8],
+                                                const float v1[8], const float r[8], float s_m, float s_v,
+                                                float my_nf4, float my_nf4t, float my_vl, float my_vt) {
     const int half = lane >> 4, j = lane & 15, hb = half * 16;
-    const int64_t numel = d.numel;
-    const int64_t nblk = (numel + kBlock - 1) / kBlock;
-    const int64_t blk = pair * 2 + half;
-    const bool blk_ok = blk < nblk;
-    const int64_t e0 = blk * kBlock + j * 8;
-    const int64_t rem = numel - e0;
-    const int nvalid = rem >= 8 ? 8 : (rem > 0 ? (int)rem : 0);
-    const uint32_t flags = d.flags;
-    const bool fact = (RECIPE == Q4_RECIPE_FACTORED) && (flags & DF_FACTORED);
-    const bool m_sr = (flags & DF_M_SR) != 0;
-
-    // ---- loads -------------------------------------------------------
-    float g[8], th[8];
-    uint32_t qmw = 0, qvw = 0;
-    float sm_old = 0.f, sv_old = 0.f;
-    if (st != nullptr) {
-        if (blk_ok) {
-            sm_old = st->ms[half];
-            qmw = st->mc[hb + j];
-            if (!fact) {
-                sv_old = st->vs[half];
-                qvw = st->vc[hb + j];
-            }
-        }
-        if (nvalid == 8) {
-            const uint4 gw = st->grad[hb + j];
-            const float4 t0 = st->param[2 * (hb + j)];
-            const float4 t1 = st->param[2 * (hb + j) + 1];
-            g[0] = bf16lo(gw.x); g[1] = bf16hi(gw.x); g[2] = bf16lo(gw.y); g[3] = bf16hi(gw.y);
-            g[4] = bf16lo(gw.z); g[5] = bf16hi(gw.z); g[6] = bf16lo(gw.w); g[7] = bf16hi(gw.w);
-            th[0] = t0.x; th[1] = t0.y; th[2] = t0.z; th[3] = t0.w;
-            th[4] = t1.x; th[5] = t1.y; th[6] = t1.z; th[7] = t1.w;
-        } else {
-#pragma unroll
-            for (int i = 0; i < 8; ++i) g[i] = th[i] = 0.f;
-        }
-    } else {
-        if (blk_ok) {
-            sm_old = __ldg(d.ms + blk);
-            qmw = __ldg(reinterpret_cast<const uint32_t*>(d.mc + blk * 64) + j);
-            if (!fact) {
-                sv_old = __ldg(d.vs + blk);
-                qvw = __ldg(reinterpret_cast<const uint32_t*>(d.vc + blk * 64) + j);
-            }
-        }
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-            g[i] = 0.f;
-            th[i] = 0.f;
-            if (i < nvalid) {
-                g[i] = __uint_as_float((uint32_t)d.grad[e0 + i] << 16);
-                th[i] = d.param[e0 + i];
-            }
-        }
-    }
-
-    // ---- dequantisation tables (old scales) ---------------------------
-    wt.deqm[hb + j] = __fmul_rn(my_nf4, sm_old);
-    if (!fact) wt.deqv[hb + j] = __fmul_rn(my_vl, sv_old);
-    __syncwarp();
-
-    // ---- moments ------------------------------------------------------
-    float m1[8], v1[8], r[8];
-    bool lane_fast = P.fast_math != 0;
-    if (fact) {
-        // vhat = R_i * C_j / mean(R); mean(R) and RN(1/mean(R)) come from the
-        // statistics pass.
-        const float2 rb = *reinterpret_cast<const float2*>(d.rbar);
-        const bool rb_ok = rb.x != 0.f && quot_range_ok(rb.x);
-        float R[8], C[8];
-        if (nvalid == 8 && (flags & DF_CVEC)) {
-            const uint32_t cols = (uint32_t)d.cols;
-            const uint32_t frow = (uint32_t)e0 / cols;
-            const uint32_t fcol = (uint32_t)e0 - frow * cols;
-            const float Ri = __ldg(d.vrow + frow);
-            const float4 c0 = __ldg(reinterpret_cast<const float4*>(d.vcol + fcol));
-            const float4 c1 = __ldg(reinterpret_cast<const float4*>(d.vcol + fcol + 4));
-            C[0] = c0.x; C[1] = c0.y; C[2] = c0.z; C[3] = c0.w;
-            C[4] = c1.x; C[5] = c1.y; C[6] = c1.z; C[7] = c1.w;
-#pragma unroll
-            for (int i = 0; i < 8; ++i) R[i] = Ri;
-        } else {
-            int64_t frow = 0, fcol = 0;
-            if (nvalid > 0) {
-                frow = e0 / d.cols;
-                fcol = e0 - frow * d.cols;
-            }
-#pragma unroll
-            for (int i = 0; i < 8; ++i) {
-                R[i] = 0.f;
-                C[i] = 0.f;
-                if (i < nvalid) {
-                    R[i] = __ldg(d.vrow + frow);
-                    C[i] = __ldg(d.vcol + fcol);
-                    if (++fcol == d.cols) { fcol = 0; ++frow; }
-                }
-            }
-        }
-        bool q_fast = rb_ok;
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-            const float p = __fmul_rn(R[i], C[i]);
-            const float q = div_rn_by_rcp(p, rb.x, rb.y);
-            q_fast = q_fast && quot_range_ok(p) && quot_range_ok(q);
-            v1[i] = (rb.x == 0.f) ? 0.f : q;
-        }
-        if (!q_fast) {
-#pragma unroll
-            for (int i = 0; i < 8; ++i) v1[i] = (rb.x == 0.f) ? 0.f : __fdiv_rn(__fmul_rn(R[i], C[i]), rb.x);
-        }
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-            const float m = wt.deqm[hb + ((qmw >> (4 * i)) & 15u)];
-            m1[i] = __fmaf_rn(P.beta1, m, __fmul_rn(P.omb1, g[i]));
-            if (i >= nvalid) v1[i] = 0.f;
-        }
-    } else {
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-            const float m = wt.deqm[hb + ((qmw >> (4 * i)) & 15u)];
-            const float v = wt.deqv[hb + ((qvw >> (4 * i)) & 15u)];
-            m1[i] = __fmaf_rn(P.beta1, m, __fmul_rn(P.omb1, g[i]));
-            v1[i] = __fmaf_rn(P.beta2, v, __fmul_rn(P.omb2, __fmul_rn(g[i], g[i])));
-        }
-    }
-    float amax = 0.f, vmax = 0.f;
-    bool tiny = false;
-#pragma unroll
-    for (int i = 0; i < 8; ++i) {
-        tiny = tiny || tiny_positive(v1[i]);
-        vmax = fmaxf(vmax, v1[i]);
-    }
-    lane_fast = lane_fast && !tiny && vmax < INFINITY;
-
-    // ---- update ---------------------------------------------------------
-    if (lane_fast) update8<true>(P, m1, v1, th, r);
-    else update8<false>(P, m1, v1, th, r);
-#pragma unroll
-    for (int i = 0; i < 8; ++i) {
-        if (i >= nvalid) { m1[i] = 0.f; v1[i] = 0.f; }
-        amax = fmaxf(amax, fabsf(m1[i]));
-    }
-    vmax = 0.f;
-#pragma unroll
-    for (int i = 0; i < 8; ++i) vmax = fmaxf(vmax, v1[i]);
-
-    // ---- weights out ----------------------------------------------------
-    if (nvalid == 8) {
-        __stcs(reinterpret_cast<float4*>(d.param + e0), make_float4(th[0], th[1], th[2], th[3]));
-        __stcs(reinterpret_cast<float4*>(d.param + e0 + 4), make_float4(th[4], th[5], th[6], th[7]));
-        if (flags & DF_BF16) {
-            uint4 o;
-            o.x = pack_bf16x2(th[0], th[1]);
-            o.y = pack_bf16x2(th[2], th[3]);
-            o.z = pack_bf16x2(th[4], th[5]);
-            o.w = pack_bf16x2(th[6], th[7]);
-            __stcs(reinterpret_cast<uint4*>(d.bf16 + e0), o);
-        }
-    } else {
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-            if (i < nvalid) {
-                d.param[e0 + i] = th[i];
-                if (flags & DF_BF16) d.bf16[e0 + i] = to_bf16(th[i]);
-            }
-        }
-    }
-
-    // ---- block scales -----------------------------------------------------
-    const float s_m = half_max(amax);
-    const float s_v = fact ? 0.f : half_max(vmax);
-
-    // ---- requantisation tables (new scales) ----------------------------
     wt.tm[hb + j] = __fmul_rn(my_nf4t, s_m);
     if (m_sr) wt.am[hb + j] = __fmul_rn(my_nf4, s_m);
     if (RECIPE == Q4_RECIPE_ZIP_SR) {
@@ -468,7 +328,7 @@ __device__ __forceinline__ void compute_tile(const StepParams& P, const DevTenso
                 const float x = v1[i];
                 int k;
                 if (fast) {
-                    const uint32_t bi = min(__float_as_uint(__fmul_rn(fabsf(x), rho)) >> 19, (uint32_t)(kVLut - 1));
+                    const uint32_t bi = __float_as_uint(__fmul_rn(fabsf(x), rho)) >> 19;
                     const int c = sm.lut_v_l[bi];
                     k = c + (wt.av[hb + c + 1] <= x ? 1 : 0);
                 } else {
@@ -490,7 +350,7 @@ __device__ __forceinline__ void compute_tile(const StepParams& P, const DevTenso
                 const float x = v1[i];
                 int code;
                 if (fast) {
-                    const uint32_t bi = min(__float_as_uint(__fmul_rn(fabsf(x), rho)) >> 19, (uint32_t)(kVLut - 1));
+                    const uint32_t bi = __float_as_uint(__fmul_rn(fabsf(x), rho)) >> 19;
                     const int c = sm.lut_v_t[bi];
                     code = c + (x > wt.av[hb + c] ? 1 : 0);
                 } else {
@@ -545,11 +405,404 @@ __device__ __forceinline__ void compute_tile(const StepParams& P, const DevTenso
     }
 }
 
+// ----------------------------------------------------------------- factored second moment
+// vhat = R_i * C_j / mean(R) for the lane's 8 elements; mean(R) and its
+// correctly rounded reciprocal come from the statistics pass.
+__device__ __forceinline__ void factored_vhat(const DevTensor& d, int64_t e0, int nvalid, float v1[8]) {
+    const float2 rb = *reinterpret_cast<const float2*>(d.rbar);
+    const bool rb_ok = rb.x != 0.f && quot_range_ok(rb.x);
+    float R[8], C[8];
+    if (nvalid == 8 && (d.flags & DF_CVEC)) {
+        const uint32_t cols = (uint32_t)d.cols;
+        const uint32_t frow = (uint32_t)e0 / cols;
+        const uint32_t fcol = (uint32_t)e0 - frow * cols;
+        const float Ri = __ldg(d.vrow + frow);
+        const float4 c0 = __ldg(reinterpret_cast<const float4*>(d.vcol + fcol));
+        const float4 c1 = __ldg(reinterpret_cast<const float4*>(d.vcol + fcol + 4));
+        C[0] = c0.x; C[1] = c0.y; C[2] = c0.z; C[3] = c0.w;
+        C[4] = c1.x; C[5] = c1.y; C[6] = c1.z; C[7] = c1.w;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) R[i] = Ri;
+    } else {
+        int64_t frow = 0, fcol = 0;
+        if (nvalid > 0) {
+            frow = e0 / d.cols;
+            fcol = e0 - frow * d.cols;
+        }
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            R[i] = 0.f;
+            C[i] = 0.f;
+            if (i < nvalid) {
+                R[i] = __ldg(d.vrow + frow);
+                C[i] = __ldg(d.vcol + fcol);
+                if (++fcol == d.cols) { fcol = 0; ++frow; }
+            }
+        }
+    }
+    bool q_fast = rb_ok;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        const float p = __fmul_rn(R[i], C[i]);
+        const float q = div_rn_by_rcp(p, rb.x, rb.y);
+        q_fast = q_fast && quot_range_ok(p) && quot_range_ok(q);
+        v1[i] = (rb.x == 0.f) ? 0.f : q;
+    }
+    if (!q_fast) {
+#pragma unroll
+        for (int i = 0; i < 8; ++i) v1[i] = (rb.x == 0.f) ? 0.f : __fdiv_rn(__fmul_rn(R[i], C[i]), rb.x);
+    }
+}
+
+// Update of the lane's elements from m, v (dequantised) and g: moments,
+// preconditioner, weights.  Returns whether the fast square root/reciprocal
+// were used (irrelevant to the results, which are identical either way).
+__device__ __forceinline__ void moments_and_update(const StepParams& P, const float g[8], const float m[8],
+                                                   const float v[8], bool fact, float m1[8], float v1[8],
+                                                   float th[8], float r[8]) {
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        m1[i] = __fmaf_rn(P.beta1, m[i], __fmul_rn(P.omb1, g[i]));
+        if (!fact) v1[i] = __fmaf_rn(P.beta2, v[i], __fmul_rn(P.omb2, __fmul_rn(g[i], g[i])));
+    }
+    bool tiny = false;
+    float vmax = 0.f;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        tiny = tiny || tiny_positive(v1[i]);
+        vmax = fmaxf(vmax, v1[i]);
+    }
+    if (P.fast_math && !tiny && vmax < INFINITY) update8<true>(P, m1, v1, th, r);
+    else update8<false>(P, m1, v1, th, r);
+}
+
+// ----------------------------------------------------------------- one tile, general path
+// `st` is the staged tile or nullptr (ragged tail: read from global memory).
+template <int RECIPE>
+__device__ __forceinline__ void compute_tile(const StepParams& P, const DevTensor& d, int64_t pair,
+                                             const Stage* st, int lane, SmemAll& sm, WarpTables& wt,
+                                             const float my_nf4, const float my_nf4t, const float my_vl,
+                                             const float my_vt) {
+    const int half = lane >> 4, j = lane & 15, hb = half * 16;
+    const int64_t numel = d.numel;
+    const int64_t nblk = (numel + kBlock - 1) / kBlock;
+    const int64_t blk = pair * 2 + half;
+    const bool blk_ok = blk < nblk;
+    const int64_t e0 = blk * kBlock + j * 8;
+    const int64_t rem = numel - e0;
+    const int nvalid = rem >= 8 ? 8 : (rem > 0 ? (int)rem : 0);
+    const uint32_t flags = d.flags;
+    const bool fact = (RECIPE == Q4_RECIPE_FACTORED) && (flags & DF_FACTORED);
+    const bool m_sr = (flags & DF_M_SR) != 0;
+
+    // ---- loads -------------------------------------------------------
+    float g[8], th[8];
+    uint32_t qmw = 0, qvw = 0;
+    float sm_old = 0.f, sv_old = 0.f;
+    if (st != nullptr) {
+        if (blk_ok) {
+            sm_old = st->ms[half];
+            qmw = st->mc[hb + j];
+            if (!fact) {
+                sv_old = st->vs[half];
+                qvw = st->vc[hb + j];
+            }
+        }
+        if (nvalid == 8) {
+            const uint4 gw = st->grad[hb + j];
+            const float4 t0 = st->param[2 * (hb + j)];
+            const float4 t1 = st->param[2 * (hb + j) + 1];
+            g[0] = bf16lo(gw.x); g[1] = bf16hi(gw.x); g[2] = bf16lo(gw.y); g[3] = bf16hi(gw.y);
+            g[4] = bf16lo(gw.z); g[5] = bf16hi(gw.z); g[6] = bf16lo(gw.w); g[7] = bf16hi(gw.w);
+            th[0] = t0.x; th[1] = t0.y; th[2] = t0.z; th[3] = t0.w;
+            th[4] = t1.x; th[5] = t1.y; th[6] = t1.z; th[7] = t1.w;
+        } else {
+#pragma unroll
+            for (int i = 0; i < 8; ++i) g[i] = th[i] = 0.f;
+        }
+    } else {
+        if (blk_ok) {
+            sm_old = __ldg(d.ms + blk);
+            qmw = __ldg(reinterpret_cast<const uint32_t*>(d.mc + blk * 64) + j);
+            if (!fact) {
+                sv_old = __ldg(d.vs + blk);
+                qvw = __ldg(reinterpret_cast<const uint32_t*>(d.vc + blk * 64) + j);
+            }
+        }
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            g[i] = 0.f;
+            th[i] = 0.f;
+            if (i < nvalid) {
+                g[i] = __uint_as_float((uint32_t)d.grad[e0 + i] << 16);
+                th[i] = d.param[e0 + i];
+            }
+        }
+    }
+
+    // ---- dequantisation (old scales) and update --------------------------
+    wt.deqm[hb + j] = __fmul_rn(my_nf4, sm_old);
+    if (!fact) wt.deqv[hb + j] = __fmul_rn(my_vl, sv_old);
+    __syncwarp();
+    float m[8], v[8], m1[8], v1[8], r[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        m[i] = wt.deqm[hb + ((qmw >> (4 * i)) & 15u)];
+        v[i] = fact ? 0.f : wt.deqv[hb + ((qvw >> (4 * i)) & 15u)];
+    }
+    if (fact) factored_vhat(d, e0, nvalid, v1);
+    moments_and_update(P, g, m, v, fact, m1, v1, th, r);
+    float amax = 0.f, vmax = 0.f;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        if (i >= nvalid) { m1[i] = 0.f; v1[i] = 0.f; }
+        amax = fmaxf(amax, fabsf(m1[i]));
+        vmax = fmaxf(vmax, v1[i]);
+    }
+
+    // ---- weights out ----------------------------------------------------
+    if (nvalid == 8) {
+        __stcs(reinterpret_cast<float4*>(d.param + e0), make_float4(th[0], th[1], th[2], th[3]));
+        __stcs(reinterpret_cast<float4*>(d.param + e0 + 4), make_float4(th[4], th[5], th[6], th[7]));
+        if (flags & DF_BF16) {
+            uint4 o;
+            o.x = pack_bf16x2(th[0], th[1]);
+            o.y = pack_bf16x2(th[2], th[3]);
+            o.z = pack_bf16x2(th[4], th[5]);
+            o.w = pack_bf16x2(th[6], th[7]);
+            __stcs(reinterpret_cast<uint4*>(d.bf16 + e0), o);
+        }
+    } else {
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            if (i < nvalid) {
+                d.param[e0 + i] = th[i];
+                if (flags & DF_BF16) d.bf16[e0 + i] = to_bf16(th[i]);
+            }
+        }
+    }
+
+    const float s_m = half_max(amax);
+    const float s_v = fact ? 0.f : half_max(vmax);
+    requant_general<RECIPE>(P, d, sm, wt, lane, blk, blk_ok, e0, nvalid, fact, m_sr, m1, v1, r, s_m, s_v, my_nf4,
+                            my_nf4t, my_vl, my_vt);
+}
+
+// ----------------------------------------------------------------- one tile, fast path
+// A staged tile whose two blocks are both complete (256 elements).  Decoding
+// reads the dequantisation tables through addresses built with byte permutes;
+// when neither block needs the general requantisation (LM-head stochastic
+// rounding, or a new scale outside the fast range) the codes come from
+// per-bucket entries that carry everything one comparison needs.
+template <int RECIPE>
+__device__ __forceinline__ void compute_tile_full(const StepParams& P, const DevTensor& d, int64_t pair,
+                                                  const Stage& st, int lane, SmemAll& sm, WarpTables& wt,
+                                                  const float my_nf4, const float my_nf4t, const float my_vl,
+                                                  const float my_vt, const float my_vl1) {
+    const int half = lane >> 4, j = lane & 15, hb = half * 16;
+    const int64_t blk = pair * 2 + half;
+    const int64_t e0 = blk * kBlock + j * 8;
+    const uint32_t flags = d.flags;
+    const bool fact = (RECIPE == Q4_RECIPE_FACTORED) && (flags & DF_FACTORED);
+    const bool m_sr = (flags & DF_M_SR) != 0;
+    const uint32_t tb = smem_addr(&wt);   // 256-byte aligned
+
+    // ---- loads from the stage ---------------------------------------------
+    const float sm_old = st.ms[half];
+    const uint32_t qmw = st.mc[hb + j];
+    const float sv_old = fact ? 0.f : st.vs[half];
+    const uint32_t qvw = fact ? 0u : st.vc[hb + j];
+    float g[8], th[8];
+    {
+        const uint4 gw = st.grad[hb + j];
+        const float4 t0 = st.param[2 * (hb + j)];
+        const float4 t1 = st.param[2 * (hb + j) + 1];
+        g[0] = bf16lo(gw.x); g[1] = bf16hi(gw.x); g[2] = bf16lo(gw.y); g[3] = bf16hi(gw.y);
+        g[4] = bf16lo(gw.z); g[5] = bf16hi(gw.z); g[6] = bf16lo(gw.w); g[7] = bf16hi(gw.w);
+        th[0] = t0.x; th[1] = t0.y; th[2] = t0.z; th[3] = t0.w;
+        th[4] = t1.x; th[5] = t1.y; th[6] = t1.z; th[7] = t1.w;
+    }
+
+    // ---- dequantisation: table entry address = table | (4 code + 64 half [+ 128 for v])
+    wt.deqm[hb + j] = __fmul_rn(my_nf4, sm_old);
+    if (!fact) wt.deqv[hb + j] = __fmul_rn(my_vl, sv_old);
+    __syncwarp();
+    float m[8], v[8], m1[8], v1[8], r[8];
+    {
+        const uint32_t hbytes = half ? 0x40404040u : 0u;
+        const uint32_t mlo = ((qmw << 2) & 0x3C3C3C3Cu) | hbytes;
+        const uint32_t mhi = ((qmw >> 2) & 0x3C3C3C3Cu) | hbytes;
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            m[2 * k] = lds_f32(__byte_perm(mlo, tb, 0x7650 + k));
+            m[2 * k + 1] = lds_f32(__byte_perm(mhi, tb, 0x7650 + k));
+        }
+        if (!fact) {
+            const uint32_t vlo = ((qvw << 2) & 0x3C3C3C3Cu) | hbytes | 0x80808080u;
+            const uint32_t vhi = ((qvw >> 2) & 0x3C3C3C3Cu) | hbytes | 0x80808080u;
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                v[2 * k] = lds_f32(__byte_perm(vlo, tb, 0x7650 + k));
+                v[2 * k + 1] = lds_f32(__byte_perm(vhi, tb, 0x7650 + k));
+            }
+        } else {
+#pragma unroll
+            for (int i = 0; i < 8; ++i) v[i] = 0.f;
+        }
+    }
+    if (fact) factored_vhat(d, e0, 8, v1);
+    moments_and_update(P, g, m, v, fact, m1, v1, th, r);
+
+    // ---- weights out ----------------------------------------------------
+    __stcs(reinterpret_cast<float4*>(d.param + e0), make_float4(th[0], th[1], th[2], th[3]));
+    __stcs(reinterpret_cast<float4*>(d.param + e0 + 4), make_float4(th[4], th[5], th[6], th[7]));
+    if (flags & DF_BF16) {
+        uint4 o;
+        o.x = pack_bf16x2(th[0], th[1]);
+        o.y = pack_bf16x2(th[2], th[3]);
+        o.z = pack_bf16x2(th[4], th[5]);
+        o.w = pack_bf16x2(th[6], th[7]);
+        __stcs(reinterpret_cast<uint4*>(d.bf16 + e0), o);
+    }
+
+    // ---- block scales -----------------------------------------------------
+    float amax = 0.f, vmax = 0.f;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        amax = fmaxf(amax, fabsf(m1[i]));
+        vmax = fmaxf(vmax, v1[i]);
+    }
+    const float s_m = half_max(amax);
+    const float s_v = fact ? 0.f : half_max(vmax);
+
+    const bool fast = __all_sync(0xffffffffu, !m_sr && scale_in_fast_range(s_m) &&
+                                                  (fact || scale_in_fast_range(s_v)));
+    if (!fast) {
+        requant_general<RECIPE>(P, d, sm, wt, lane, blk, true, e0, 8, fact, m_sr, m1, v1, r, s_m, s_v, my_nf4,
+                                my_nf4t, my_vl, my_vt);
+        return;
+    }
+
+    // ---- fast tables at the new scales ------------------------------------
+    // mt[half][b] = {t_c * s_m, c} for the linear bucket b (c its candidate);
+    // buckets 0..32 occur for |m'| <= s_m.
+    {
+        const float2 e1 = sm.nf4_bucket[j];
+        const float2 e2 = sm.nf4_bucket[j + 16];
+        wt.mt[half][j] = make_float2(__fmul_rn(e1.x, s_m), e1.y);
+        wt.mt[half][j + 16] = make_float2(__fmul_rn(e2.x, s_m), e2.y);
+        if (j == 0) {
+            const float2 e3 = sm.nf4_bucket[32];
+            wt.mt[half][32] = make_float2(__fmul_rn(e3.x, s_m), e3.y);
+        }
+    }
+    if (!fact) {
+        if (RECIPE == Q4_RECIPE_ZIP_SR) {
+            // ve[half][c] = {a_{c+1}, r_c, d_c, r_{c+1}}, {d_{c+1}} with a_k the level
+            // at the new scale, r_k its preconditioner, d_k = (r_k - r_{k+1}) 2^-24.
+            const float a = __fmul_rn(my_vl, s_v);
+            const float rk = P.fast_math ? precond<true>(P, a) : precond<false>(P, a);
+            const float rk1 = __shfl_down_sync(0xffffffffu, rk, 1);
+            const float dk = j < 15 ? __fmul_rn(__fsub_rn(rk, rk1), kTwoM24) : 0.f;
+            const float a1 = __shfl_down_sync(0xffffffffu, a, 1);
+            const float dk1 = __shfl_down_sync(0xffffffffu, dk, 1);
+            wt.ve[half][j][0] = make_float4(a1, rk, dk, rk1);
+            wt.ve[half][j][1] = make_float4(dk1, 0.f, 0.f, 0.f);
+        } else {
+            // ve[half][c] = {t_c * s_v, L_c, L_{c+1}} (unscaled levels for EDEN)
+            wt.ve[half][j][0] = make_float4(__fmul_rn(my_vt, s_v), my_vl, my_vl1, 0.f);
+        }
+    }
+    __syncwarp();
+
+    // ---- m codes: NF4 RTN ---------------------------------------------------
+    uint32_t cm = 0;
+    {
+        const float rho16 = __fmul_rn(16.f, rcp_rn_normal<1>(s_m));
+        const uint32_t mt_base = tb + (uint32_t)((char*)&wt.mt[half][0] - (char*)&wt);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            const float x = m1[i];
+            const uint32_t bi = __float_as_uint(__fmaf_rn(x, rho16, kMagic + 16.f)) & 63u;
+            const float2 e = lds_f32x2(mt_base + bi * 8u);
+            cm += __float_as_uint(e.y) << (4 * i);
+            cm += (x > e.x) ? (1u << (4 * i)) : 0u;
+        }
+    }
+
+    // ---- v codes ----------------------------------------------------------
+    uint32_t cv = 0;
+    float sv_store = s_v;
+    if (!fact) {
+        const float rho = rcp_rn_normal<1>(s_v);
+        const uint32_t ve_base = tb + (uint32_t)((char*)&wt.ve[half][0][0] - (char*)&wt);
+        if (RECIPE == Q4_RECIPE_ZIP_SR) {
+            const uint32_t lut = smem_addr(sm.lut_v_l);
+            uint32_t w[8];
+            draws8(d.elem_offset + (uint64_t)e0, 1u, d.tensor_id, P.step, P.round_keys, w);
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                const float x = v1[i];
+                const uint32_t c = lds_u8(lut + (__float_as_uint(__fmul_rn(x, rho)) >> 19));
+                const uint32_t ea = ve_base + c * 32u;
+                const float4 e = lds_f32x4(ea);
+                const float dk1 = lds_f32(ea + 16u);
+                const bool up_cell = e.x <= x;
+                const float rk = up_cell ? e.w : e.y;
+                const float dk = up_cell ? dk1 : e.z;
+                const bool up = __fmul_rn((float)(w[i] >> 8), dk) < __fsub_rn(rk, r[i]);
+                cv += c << (4 * i);
+                cv += up_cell ? (1u << (4 * i)) : 0u;
+                cv += up ? (1u << (4 * i)) : 0u;
+            }
+        } else {
+            const uint32_t lut = smem_addr(sm.lut_v_t);
+            float pa[2] = {0.f, 0.f}, pb[2] = {0.f, 0.f};
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                const float x = v1[i];
+                const float y = __fmul_rn(x, rho);
+                const uint32_t c = lds_u8(lut + (__float_as_uint(y) >> 19));
+                const float4 e = lds_f32x4(ve_base + c * 32u);
+                const bool up = x > e.x;
+                cv += c << (4 * i);
+                cv += up ? (1u << (4 * i)) : 0u;
+                if (RECIPE == Q4_RECIPE_ZE_EDEN) {
+                    const float yh = up ? e.z : e.y;
+                    const float ta = __fmul_rn(y, y), tb2 = __fmul_rn(y, yh);
+                    const int h = i >> 2;
+                    pa[h] = ((i & 3) == 0) ? ta : __fadd_rn(pa[h], ta);
+                    pb[h] = ((i & 3) == 0) ? tb2 : __fadd_rn(pb[h], tb2);
+                }
+            }
+            if (RECIPE == Q4_RECIPE_ZE_EDEN) {
+                float A = __fadd_rn(pa[0], pa[1]);
+                float B = __fadd_rn(pb[0], pb[1]);
+#pragma unroll
+                for (int o = 1; o < 16; o <<= 1) {
+                    A = __fadd_rn(A, __shfl_xor_sync(0xffffffffu, A, o));
+                    B = __fadd_rn(B, __shfl_xor_sync(0xffffffffu, B, o));
+                }
+                sv_store = (B == 0.f) ? 0.f : __fmul_rn(s_v, __fdiv_rn(A, B));
+            }
+        }
+    }
+
+    // ---- codes and scales out --------------------------------------------
+    reinterpret_cast<uint32_t*>(d.mc + blk * 64)[j] = cm;
+    if (!fact) reinterpret_cast<uint32_t*>(d.vc + blk * 64)[j] = cv;
+    if (j == 0) {
+        d.ms[blk] = s_m;
+        if (!fact) d.vs[blk] = sv_store;
+    }
+}
+
 // ----------------------------------------------------------------- the kernel
 template <int RECIPE>
 __global__ void __launch_bounds__(kStepThreads, 1) step_kernel(const __grid_constant__ StepParams P) {
-    extern __shared__ __align__(128) unsigned char smem_raw[];
-    SmemAll& sm = *reinterpret_cast<SmemAll*>(smem_raw);
+    extern __shared__ unsigned char smem_raw[];
+    // the tables need 256-byte alignment; the launch adds 256 bytes of slack
+    SmemAll& sm = *reinterpret_cast<SmemAll*>(smem_raw + ((256u - (smem_addr(smem_raw) & 255u)) & 255u));
     const int lane = threadIdx.x & 31;
     const int warp = threadIdx.x >> 5;
     WarpSmem& ws = sm.w[warp];
@@ -558,15 +811,17 @@ __global__ void __launch_bounds__(kStepThreads, 1) step_kernel(const __grid_cons
     for (int i = threadIdx.x; i < 64; i += blockDim.x) {
         sm.lut_nf4_t[i] = P.tab.lut_nf4_t[i];
         sm.lut_nf4_l[i] = P.tab.lut_nf4_l[i];
+        sm.nf4_bucket[i] = P.tab.nf4_bucket[i];
     }
     for (int i = threadIdx.x; i < kVLut / 4; i += blockDim.x) {
         reinterpret_cast<uint32_t*>(sm.lut_v_l)[i] = reinterpret_cast<const uint32_t*>(P.tab.lut_v_l)[i];
         reinterpret_cast<uint32_t*>(sm.lut_v_t)[i] = reinterpret_cast<const uint32_t*>(P.tab.lut_v_t)[i];
     }
     if (lane == 0) {
-        // count 2: the issuing lane's arrive.expect_tx and the arrive that
-        // cp.async.mbarrier.arrive.noinc triggers when the scale copies land
-        for (int s = 0; s < kStages; ++s) mbar_init(&ws.bar[s], 2);
+        // count 5: the arrive.expect_tx of lane 0 and the arrives that
+        // cp.async.mbarrier.arrive.noinc of lanes 4..7 trigger once their
+        // scale copies have landed
+        for (int s = 0; s < kStages; ++s) mbar_init(&ws.bar[s], 5);
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
     __syncthreads();
@@ -574,77 +829,64 @@ __global__ void __launch_bounds__(kStepThreads, 1) step_kernel(const __grid_cons
     const int j = lane & 15;
     const float my_nf4 = P.tab.nf4[j], my_nf4t = P.tab.nf4_t[j];
     const float my_vl = P.tab.vl[j], my_vt = P.tab.vt[j];
+    const float my_vl1 = P.tab.vl[j < 15 ? j + 1 : 15];
     const uint64_t policy = evict_first_policy();
 
     const int64_t gw = (int64_t)blockIdx.x * kStepWarps + warp;
     const int64_t W = (int64_t)gridDim.x * kStepWarps;
     const int64_t n_it = gw < P.total_pairs ? (P.total_pairs - 1 - gw) / W + 1 : 0;
 
-    // Issue cursor: tensor of the next tile to stage and the fields the copies need.
+    // Issue cursor: tensor of the next tile to stage.
     int ti = 0;
     int64_t ib = 0, ie = __ldg(P.pair_prefix + 1);
-    const uint16_t* i_grad = nullptr;
-    const float* i_param = nullptr;
-    const uint8_t* i_mc = nullptr;
-    const uint8_t* i_vc = nullptr;
-    const float* i_ms = nullptr;
-    const float* i_vs = nullptr;
-    int64_t i_numel = 0;
-    bool i_fact = false;
-    bool i_loaded = false;
+    const DevTensor* idesc = P.tensors;
 
+    // Lanes 0..7 each issue one copy of a tile: 0 gradient, 1 master weight,
+    // 2 m codes, 3 v codes (bulk copies); 4, 5 m scales and 6, 7 v scales of
+    // the tile's two blocks (4-byte copies).  Lane 0 first announces the
+    // bulk byte count; lanes 4..7 always arrive, with or without a copy.
     auto issue = [&](int64_t it) {
         const int64_t pair = gw + it * W;
-        bool moved = !i_loaded;
         while (pair >= ie) {
             ++ti;
             ib = ie;
             ie = __ldg(P.pair_prefix + ti + 1);
-            moved = true;
         }
-        if (moved) {
-            const DevTensor* dt = P.tensors + ti;
-            i_grad = dt->grad;
-            i_param = dt->param;
-            i_mc = dt->mc;
-            i_vc = dt->vc;
-            i_ms = dt->ms;
-            i_vs = dt->vs;
-            i_numel = dt->numel;
-            i_fact = (RECIPE == Q4_RECIPE_FACTORED) && (dt->flags & DF_FACTORED);
-            i_loaded = true;
-        }
-        if (lane == 0) {
-            const int s = (int)(it % kStages);
-            Stage& st = ws.st[s];
-            unsigned long long* bar = &ws.bar[s];
+        idesc = P.tensors + ti;
+        const int s = (int)(it % kStages);
+        Stage& st = ws.st[s];
+        unsigned long long* bar = &ws.bar[s];
+        if (lane < 8) {
+            const int64_t numel = idesc->numel;
+            const bool fact = (RECIPE == Q4_RECIPE_FACTORED) && (idesc->flags & DF_FACTORED);
             const int64_t blk0 = (pair - ib) * 2;
-            const int64_t nblk = (i_numel + kBlock - 1) / kBlock;
+            const int64_t nblk = (numel + kBlock - 1) / kBlock;
             const int nb = (nblk - blk0) >= 2 ? 2 : 1;
             const int64_t e0 = blk0 * kBlock;
-            const int64_t left = i_numel - e0;
+            const int64_t left = numel - e0;
             const uint32_t nel = left >= 2 * kBlock ? 2 * kBlock : (uint32_t)left;
-            if ((nel & 7u) == 0) {
-                const uint32_t cbytes = (uint32_t)nb * 64u;
-                const uint32_t bytes = nel * 2u + nel * 4u + cbytes + (i_fact ? 0u : cbytes);
-                asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-                mbar_arrive_expect_tx(bar, bytes);
-                bulk_load(st.grad, i_grad + e0, nel * 2u, bar, policy);
-                bulk_load(st.param, i_param + e0, nel * 4u, bar, policy);
-                bulk_load(st.mc, i_mc + blk0 * 64, cbytes, bar, policy);
-                if (!i_fact) bulk_load(st.vc, i_vc + blk0 * 64, cbytes, bar, policy);
-                cp_async4(&st.ms[0], i_ms + blk0);
-                if (nb == 2) cp_async4(&st.ms[1], i_ms + blk0 + 1);
-                if (!i_fact) {
-                    cp_async4(&st.vs[0], i_vs + blk0);
-                    if (nb == 2) cp_async4(&st.vs[1], i_vs + blk0 + 1);
-                }
-                cp_async_arrive_noinc(bar);
-            } else {
-                // ragged tail tile: computed from global memory; complete the phase now
-                mbar_arrive(bar);
-                mbar_arrive(bar);
+            const bool staged = (nel & 7u) == 0;
+            const uint32_t cbytes = (uint32_t)nb * 64u;
+            if (lane == 0) {
+                if (staged) mbar_arrive_expect_tx(bar, nel * 6u + cbytes + (fact ? 0u : cbytes));
+                else mbar_arrive(bar);   // ragged tail tile: computed from global memory
             }
+            __syncwarp(0xffu);
+            if (staged) {
+                // the warp's earlier reads of this buffer precede the copies into it
+                if (lane < 4) asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+                if (lane == 0) bulk_load(st.grad, idesc->grad + e0, nel * 2u, bar, policy);
+                else if (lane == 1) bulk_load(st.param, idesc->param + e0, nel * 4u, bar, policy);
+                else if (lane == 2) bulk_load(st.mc, idesc->mc + blk0 * 64, cbytes, bar, policy);
+                else if (lane == 3) { if (!fact) bulk_load(st.vc, idesc->vc + blk0 * 64, cbytes, bar, policy); }
+                else {
+                    const int k = lane - 4;              // 0, 1: m scales; 2, 3: v scales
+                    const int b = k & 1;
+                    if (b < nb && (k < 2 || !fact))
+                        cp_async4(k < 2 ? &st.ms[b] : &st.vs[b], (k < 2 ? idesc->ms : idesc->vs) + blk0 + b);
+                }
+            }
+            if (lane >= 4) cp_async_arrive_noinc(bar);
         }
     };
 
@@ -679,14 +921,18 @@ __global__ void __launch_bounds__(kStepThreads, 1) step_kernel(const __grid_cons
         }
         const int64_t pl = pair - cb;
         const int64_t left = ws.desc.numel - pl * 2 * kBlock;
-        const bool staged = ((left >= 2 * kBlock ? 2 * kBlock : left) & 7) == 0;
-        compute_tile<RECIPE>(P, ws.desc, pl, staged ? &ws.st[s] : nullptr, lane, sm, ws.wt, my_nf4, my_nf4t,
-                             my_vl, my_vt);
+        if (left >= 2 * kBlock) {
+            compute_tile_full<RECIPE>(P, ws.desc, pl, ws.st[s], lane, sm, ws.wt, my_nf4, my_nf4t, my_vl, my_vt,
+                                      my_vl1);
+        } else {
+            compute_tile<RECIPE>(P, ws.desc, pl, (left & 7) == 0 ? &ws.st[s] : nullptr, lane, sm, ws.wt, my_nf4,
+                                 my_nf4t, my_vl, my_vt);
+        }
         __syncwarp();
     }
 }
 
-size_t step_smem_bytes() { return sizeof(SmemAll); }
+size_t step_smem_bytes() { return sizeof(SmemAll) + 256; }
 
 template <int RECIPE>
 int configure(int device) {

@@ -129,7 +129,9 @@ float bits_to_float(uint32_t u) {
     return f;
 }
 
-// Log bucket i = bits(x/s) >> 19 (1/16 octave), clamped to kVLut - 1.
+// Log bucket i = bits(x/s) >> 19 (1/16 octave) of a non-negative x/s; the
+// table covers every such bit pattern (buckets above 2 hold only inputs that
+// cannot occur for finite x <= s, and NaN).
 bool build_log(const float* pts, int np, bool levels, uint8_t* lut) {
     for (int i = 0; i < kVLut; ++i) {
         double lo = bits_to_float((uint32_t)i << 19);
@@ -186,6 +188,11 @@ bool build_tables(int vbook, Tables* t) {
     if (!build_linear(nf4.levels, 16, true, t->lut_nf4_l)) return false;
     if (!build_log(v.levels, 16, true, t->lut_v_l)) return false;
     if (!build_log(v.thresholds, 15, false, t->lut_v_t)) return false;
+    for (int i = 0; i < 64; ++i) {
+        const int c = t->lut_nf4_t[i];
+        t->nf4_bucket[i].x = nf4.thresholds[c];
+        std::memcpy(&t->nf4_bucket[i].y, &c, 4);   // the candidate code, as raw bits
+    }
     return true;
 }
 
