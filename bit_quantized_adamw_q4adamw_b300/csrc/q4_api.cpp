@@ -357,6 +357,14 @@ int q4adamw_step(const q4adamw_tensor_t* t, int n, float lr, float beta1, float 
     // [2^-126, 2^126); with v' <= FLT_MAX and c2 <= 2^12 (beta2 < 1 in FP32)
     // that holds whenever eps lies in [2^-100, 2^60].
     p.fast_math = (eps >= 0x1p-100f && eps <= 0x1p60f) ? 1 : 0;
+    p.x2_beta1 = make_float2(p.beta1, p.beta1);
+    p.x2_beta2 = make_float2(p.beta2, p.beta2);
+    p.x2_omb1 = make_float2(p.omb1, p.omb1);
+    p.x2_omb2 = make_float2(p.omb2, p.omb2);
+    p.x2_c2 = make_float2(p.c2, p.c2);
+    p.x2_eps = make_float2(p.eps, p.eps);
+    p.x2_decay = make_float2(p.decay, p.decay);
+    p.x2_neg_step = make_float2(-p.step_size, -p.step_size);   // negation is exact
     const uint32_t k0 = (uint32_t)seed, k1 = (uint32_t)(seed >> 32);
     for (int r = 0; r < 10; ++r) {
         p.round_keys[2 * r] = k0 + (uint32_t)r * 0x9E3779B9u;

@@ -68,7 +68,7 @@ struct __align__(256) WarpTables {
     float deqm[32];        // [half][16] NF4 level * old s_m
     float deqv[32];        // [half][16] v level * old s_v
     float2 mt[2][64];      // fast path: [half][linear bucket] {NF4 threshold of the candidate * new s_m, candidate}
-    float4 ve[2][16][2];   // fast path: [half][cell] v search entry (32 bytes, see build_fast_tables)
+    float4 ve[2][16];      // fast path: [half][cell] v search entry (see compute_tile_full)
     float tm[32];          // general path: [half][16] NF4 threshold * new s_m
     float am[32];          // [half][16] NF4 level * new s_m (LM-head SR)
     float av[32];          // [half][16] v level * new s_v (ZIP-SR) or v threshold * new s_v (RTN)
@@ -202,10 +202,15 @@ __device__ __forceinline__ void draws8(uint64_t idx, uint32_t purpose, uint32_t 
     w[4] = b.x; w[5] = b.y; w[6] = b.z; w[7] = b.w;
 }
 
-__device__ __forceinline__ float half_max(float x) {
-#pragma unroll
-    for (int o = 1; o < 16; o <<= 1) x = fmaxf(x, __shfl_xor_sync(0xffffffffu, x, o));
-    return x;
+// Maximum over the 16 lanes of this lane's half of a lane value x >= +0 that
+// is not NaN (a max of fmaxf's started at +0).  For such floats the order of
+// the bit patterns is the order of the values, so two integer warp reductions
+// give the exact result.
+__device__ __forceinline__ float half_max(float x, int half) {
+    const uint32_t b = __float_as_uint(x);
+    const uint32_t m0 = __reduce_max_sync(0xffffffffu, half ? 0u : b);
+    const uint32_t m1 = __reduce_max_sync(0xffffffffu, half ? b : 0u);
+    return __uint_as_float(half ? m1 : m0);
 }
 
 // Fast candidate paths need a scale whose reciprocal and scaled tables are
@@ -241,6 +246,59 @@ __device__ __forceinline__ void update8(const StepParams& P, const float m1[8], 
         r[i] = precond<FAST>(P, v1[i]);
         th[i] = __fsub_rn(__fmul_rn(th[i], P.decay), __fmul_rn(P.step_size, __fmul_rn(m1[i], r[i])));
     }
+}
+
+// ----------------------------------------------------------------- paired arithmetic
+__device__ __forceinline__ float2 neg2(float2 a) { return make_float2(-a.x, -a.y); }
+
+// Moments and update of the lane's 8 elements as 4 pairs (2k, 2k+1), with the
+// paired FP32 instructions; each component rounds as the scalar sequence:
+// m' = fma(b1, m, omb1 g), v' = fma(b2, v, omb2 (g g)),
+// r = 1/(sqrt(v') c2 + eps), theta' = theta decay + (-step) (m' r), where
+// theta decay - step (m' r) = theta decay + (-step) (m' r) exactly.
+// Lanes with a v' outside the fast square root's domain take the scalar IEEE
+// sequence.
+__device__ __forceinline__ void update_pairs(const StepParams& P, const float2 g[4], const float2 m[4],
+                                             const float2 v[4], bool fact, float2 m1[4], float2 v1[4],
+                                             float2 th[4], float2 r[4]) {
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+        m1[k] = fma2_rn(P.x2_beta1, m[k], mul2_rn(P.x2_omb1, g[k]));
+        if (!fact) v1[k] = fma2_rn(P.x2_beta2, v[k], mul2_rn(P.x2_omb2, mul2_rn(g[k], g[k])));
+    }
+    bool tiny = false;
+    float vmax = 0.f;
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+        tiny = tiny || tiny_positive(v1[k].x) || tiny_positive(v1[k].y);
+        vmax = fmaxf(vmax, fmaxf(v1[k].x, v1[k].y));
+    }
+    if (P.fast_math && !tiny && vmax < INFINITY) {
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            // products paired, sums scalar (a paired product must not feed a paired add)
+            const float2 sc = mul2_rn(sqrt2_rn_normal(v1[k]), P.x2_c2);
+            r[k] = rcp2_rn_normal(make_float2(__fadd_rn(sc.x, P.eps), __fadd_rn(sc.y, P.eps)));
+            const float2 t1 = mul2_rn(th[k], P.x2_decay);
+            const float2 t2 = mul2_rn(P.x2_neg_step, mul2_rn(m1[k], r[k]));
+            th[k] = make_float2(__fadd_rn(t1.x, t2.x), __fadd_rn(t1.y, t2.y));
+        }
+    } else {
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            r[k].x = precond<false>(P, v1[k].x);
+            r[k].y = precond<false>(P, v1[k].y);
+            th[k].x = __fsub_rn(__fmul_rn(th[k].x, P.decay), __fmul_rn(P.step_size, __fmul_rn(m1[k].x, r[k].x)));
+            th[k].y = __fsub_rn(__fmul_rn(th[k].y, P.decay), __fmul_rn(P.step_size, __fmul_rn(m1[k].y, r[k].y)));
+        }
+    }
+}
+
+// Packs eight 4-bit codes (element i in bits 4i..4i+3) with a shallow tree.
+__device__ __forceinline__ uint32_t pack8(const uint32_t c[8]) {
+    const uint32_t b0 = c[0] + (c[1] << 4), b1 = c[2] + (c[3] << 4);
+    const uint32_t b2 = c[4] + (c[5] << 4), b3 = c[6] + (c[7] << 4);
+    return __byte_perm(__byte_perm(b0, b1, 0x0040), __byte_perm(b2, b3, 0x0040), 0x5410);
 }
 
 // ----------------------------------------------------------------- requantisation, general path
@@ -582,8 +640,8 @@ __device__ __forceinline__ void compute_tile(const StepParams& P, const DevTenso
         }
     }
 
-    const float s_m = half_max(amax);
-    const float s_v = fact ? 0.f : half_max(vmax);
+    const float s_m = half_max(amax, half);
+    const float s_v = fact ? 0.f : half_max(vmax, half);
     requant_general<RECIPE>(P, d, sm, wt, lane, blk, blk_ok, e0, nvalid, fact, m_sr, m1, v1, r, s_m, s_v, my_nf4,
                             my_nf4t, my_vl, my_vt);
 }
@@ -612,73 +670,85 @@ __device__ __forceinline__ void compute_tile_full(const StepParams& P, const Dev
     const uint32_t qmw = st.mc[hb + j];
     const float sv_old = fact ? 0.f : st.vs[half];
     const uint32_t qvw = fact ? 0u : st.vc[hb + j];
-    float g[8], th[8];
+    float2 g[4], th[4];
     {
         const uint4 gw = st.grad[hb + j];
         const float4 t0 = st.param[2 * (hb + j)];
         const float4 t1 = st.param[2 * (hb + j) + 1];
-        g[0] = bf16lo(gw.x); g[1] = bf16hi(gw.x); g[2] = bf16lo(gw.y); g[3] = bf16hi(gw.y);
-        g[4] = bf16lo(gw.z); g[5] = bf16hi(gw.z); g[6] = bf16lo(gw.w); g[7] = bf16hi(gw.w);
-        th[0] = t0.x; th[1] = t0.y; th[2] = t0.z; th[3] = t0.w;
-        th[4] = t1.x; th[5] = t1.y; th[6] = t1.z; th[7] = t1.w;
+        g[0] = make_float2(bf16lo(gw.x), bf16hi(gw.x));
+        g[1] = make_float2(bf16lo(gw.y), bf16hi(gw.y));
+        g[2] = make_float2(bf16lo(gw.z), bf16hi(gw.z));
+        g[3] = make_float2(bf16lo(gw.w), bf16hi(gw.w));
+        th[0] = make_float2(t0.x, t0.y);
+        th[1] = make_float2(t0.z, t0.w);
+        th[2] = make_float2(t1.x, t1.y);
+        th[3] = make_float2(t1.z, t1.w);
     }
 
     // ---- dequantisation: table entry address = table | (4 code + 64 half [+ 128 for v])
     wt.deqm[hb + j] = __fmul_rn(my_nf4, sm_old);
     if (!fact) wt.deqv[hb + j] = __fmul_rn(my_vl, sv_old);
     __syncwarp();
-    float m[8], v[8], m1[8], v1[8], r[8];
+    float2 m[4], v[4], m1[4], v1[4], r[4];
     {
         const uint32_t hbytes = half ? 0x40404040u : 0u;
         const uint32_t mlo = ((qmw << 2) & 0x3C3C3C3Cu) | hbytes;
         const uint32_t mhi = ((qmw >> 2) & 0x3C3C3C3Cu) | hbytes;
 #pragma unroll
-        for (int k = 0; k < 4; ++k) {
-            m[2 * k] = lds_f32(__byte_perm(mlo, tb, 0x7650 + k));
-            m[2 * k + 1] = lds_f32(__byte_perm(mhi, tb, 0x7650 + k));
-        }
+        for (int k = 0; k < 4; ++k)
+            m[k] = make_float2(lds_f32(__byte_perm(mlo, tb, 0x7650 + k)), lds_f32(__byte_perm(mhi, tb, 0x7650 + k)));
         if (!fact) {
             const uint32_t vlo = ((qvw << 2) & 0x3C3C3C3Cu) | hbytes | 0x80808080u;
             const uint32_t vhi = ((qvw >> 2) & 0x3C3C3C3Cu) | hbytes | 0x80808080u;
 #pragma unroll
-            for (int k = 0; k < 4; ++k) {
-                v[2 * k] = lds_f32(__byte_perm(vlo, tb, 0x7650 + k));
-                v[2 * k + 1] = lds_f32(__byte_perm(vhi, tb, 0x7650 + k));
-            }
+            for (int k = 0; k < 4; ++k)
+                v[k] = make_float2(lds_f32(__byte_perm(vlo, tb, 0x7650 + k)),
+                                   lds_f32(__byte_perm(vhi, tb, 0x7650 + k)));
         } else {
+            float vf[8];
+            factored_vhat(d, e0, 8, vf);
 #pragma unroll
-            for (int i = 0; i < 8; ++i) v[i] = 0.f;
+            for (int k = 0; k < 4; ++k) {
+                v[k] = make_float2(0.f, 0.f);
+                v1[k] = make_float2(vf[2 * k], vf[2 * k + 1]);
+            }
         }
     }
-    if (fact) factored_vhat(d, e0, 8, v1);
-    moments_and_update(P, g, m, v, fact, m1, v1, th, r);
+    update_pairs(P, g, m, v, fact, m1, v1, th, r);
 
     // ---- weights out ----------------------------------------------------
-    __stcs(reinterpret_cast<float4*>(d.param + e0), make_float4(th[0], th[1], th[2], th[3]));
-    __stcs(reinterpret_cast<float4*>(d.param + e0 + 4), make_float4(th[4], th[5], th[6], th[7]));
+    __stcs(reinterpret_cast<float4*>(d.param + e0), make_float4(th[0].x, th[0].y, th[1].x, th[1].y));
+    __stcs(reinterpret_cast<float4*>(d.param + e0 + 4), make_float4(th[2].x, th[2].y, th[3].x, th[3].y));
     if (flags & DF_BF16) {
         uint4 o;
-        o.x = pack_bf16x2(th[0], th[1]);
-        o.y = pack_bf16x2(th[2], th[3]);
-        o.z = pack_bf16x2(th[4], th[5]);
-        o.w = pack_bf16x2(th[6], th[7]);
+        o.x = pack_bf16x2(th[0].x, th[0].y);
+        o.y = pack_bf16x2(th[1].x, th[1].y);
+        o.z = pack_bf16x2(th[2].x, th[2].y);
+        o.w = pack_bf16x2(th[3].x, th[3].y);
         __stcs(reinterpret_cast<uint4*>(d.bf16 + e0), o);
     }
 
     // ---- block scales -----------------------------------------------------
     float amax = 0.f, vmax = 0.f;
 #pragma unroll
-    for (int i = 0; i < 8; ++i) {
-        amax = fmaxf(amax, fabsf(m1[i]));
-        vmax = fmaxf(vmax, v1[i]);
+    for (int k = 0; k < 4; ++k) {
+        amax = fmaxf(amax, fmaxf(fabsf(m1[k].x), fabsf(m1[k].y)));
+        vmax = fmaxf(vmax, fmaxf(v1[k].x, v1[k].y));
     }
-    const float s_m = half_max(amax);
-    const float s_v = fact ? 0.f : half_max(vmax);
+    const float s_m = half_max(amax, half);
+    const float s_v = fact ? 0.f : half_max(vmax, half);
 
     const bool fast = __all_sync(0xffffffffu, !m_sr && scale_in_fast_range(s_m) &&
                                                   (fact || scale_in_fast_range(s_v)));
     if (!fast) {
-        requant_general<RECIPE>(P, d, sm, wt, lane, blk, true, e0, 8, fact, m_sr, m1, v1, r, s_m, s_v, my_nf4,
+        float m1s[8], v1s[8], rs[8];
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            m1s[2 * k] = m1[k].x; m1s[2 * k + 1] = m1[k].y;
+            v1s[2 * k] = v1[k].x; v1s[2 * k + 1] = v1[k].y;
+            rs[2 * k] = r[k].x; rs[2 * k + 1] = r[k].y;
+        }
+        requant_general<RECIPE>(P, d, sm, wt, lane, blk, true, e0, 8, fact, m_sr, m1s, v1s, rs, s_m, s_v, my_nf4,
                                 my_nf4t, my_vl, my_vt);
         return;
     }
@@ -698,36 +768,37 @@ __device__ __forceinline__ void compute_tile_full(const StepParams& P, const Dev
     }
     if (!fact) {
         if (RECIPE == Q4_RECIPE_ZIP_SR) {
-            // ve[half][c] = {a_{c+1}, r_c, d_c, r_{c+1}}, {d_{c+1}} with a_k the level
-            // at the new scale, r_k its preconditioner, d_k = (r_k - r_{k+1}) 2^-24.
+            // ve[half][c] = {a_{c+1}, r_c, d_c, r_{c+1}} with a_k the level at the new
+            // scale, r_k its preconditioner, d_k = (r_k - r_{k+1}) 2^-24; d_{c+1} is
+            // read from the next entry.
             const float a = __fmul_rn(my_vl, s_v);
             const float rk = P.fast_math ? precond<true>(P, a) : precond<false>(P, a);
             const float rk1 = __shfl_down_sync(0xffffffffu, rk, 1);
             const float dk = j < 15 ? __fmul_rn(__fsub_rn(rk, rk1), kTwoM24) : 0.f;
             const float a1 = __shfl_down_sync(0xffffffffu, a, 1);
-            const float dk1 = __shfl_down_sync(0xffffffffu, dk, 1);
-            wt.ve[half][j][0] = make_float4(a1, rk, dk, rk1);
-            wt.ve[half][j][1] = make_float4(dk1, 0.f, 0.f, 0.f);
+            wt.ve[half][j] = make_float4(a1, rk, dk, rk1);
         } else {
             // ve[half][c] = {t_c * s_v, L_c, L_{c+1}} (unscaled levels for EDEN)
-            wt.ve[half][j][0] = make_float4(__fmul_rn(my_vt, s_v), my_vl, my_vl1, 0.f);
+            wt.ve[half][j] = make_float4(__fmul_rn(my_vt, s_v), my_vl, my_vl1, 0.f);
         }
     }
     __syncwarp();
 
     // ---- m codes: NF4 RTN ---------------------------------------------------
-    uint32_t cm = 0;
+    uint32_t cm;
     {
         const float rho16 = __fmul_rn(16.f, rcp_rn_normal<1>(s_m));
         const uint32_t mt_base = tb + (uint32_t)((char*)&wt.mt[half][0] - (char*)&wt);
+        uint32_t c[8];
 #pragma unroll
-        for (int i = 0; i < 8; ++i) {
-            const float x = m1[i];
-            const uint32_t bi = __float_as_uint(__fmaf_rn(x, rho16, kMagic + 16.f)) & 63u;
-            const float2 e = lds_f32x2(mt_base + bi * 8u);
-            cm += __float_as_uint(e.y) << (4 * i);
-            cm += (x > e.x) ? (1u << (4 * i)) : 0u;
+        for (int k = 0; k < 4; ++k) {
+            const float2 z = fma2_rn(m1[k], make_float2(rho16, rho16), make_float2(kMagic + 16.f, kMagic + 16.f));
+            const float2 e0v = lds_f32x2(mt_base + (__float_as_uint(z.x) & 63u) * 8u);
+            const float2 e1v = lds_f32x2(mt_base + (__float_as_uint(z.y) & 63u) * 8u);
+            c[2 * k] = __float_as_uint(e0v.y) + (m1[k].x > e0v.x ? 1u : 0u);
+            c[2 * k + 1] = __float_as_uint(e1v.y) + (m1[k].y > e1v.x ? 1u : 0u);
         }
+        cm = pack8(c);
     }
 
     // ---- v codes ----------------------------------------------------------
@@ -735,47 +806,59 @@ __device__ __forceinline__ void compute_tile_full(const StepParams& P, const Dev
     float sv_store = s_v;
     if (!fact) {
         const float rho = rcp_rn_normal<1>(s_v);
-        const uint32_t ve_base = tb + (uint32_t)((char*)&wt.ve[half][0][0] - (char*)&wt);
+        const uint32_t ve_base = tb + (uint32_t)((char*)&wt.ve[half][0] - (char*)&wt);
+        uint32_t c[8];
         if (RECIPE == Q4_RECIPE_ZIP_SR) {
             const uint32_t lut = smem_addr(sm.lut_v_l);
             uint32_t w[8];
             draws8(d.elem_offset + (uint64_t)e0, 1u, d.tensor_id, P.step, P.round_keys, w);
 #pragma unroll
-            for (int i = 0; i < 8; ++i) {
-                const float x = v1[i];
-                const uint32_t c = lds_u8(lut + (__float_as_uint(__fmul_rn(x, rho)) >> 19));
-                const uint32_t ea = ve_base + c * 32u;
-                const float4 e = lds_f32x4(ea);
-                const float dk1 = lds_f32(ea + 16u);
-                const bool up_cell = e.x <= x;
-                const float rk = up_cell ? e.w : e.y;
-                const float dk = up_cell ? dk1 : e.z;
-                const bool up = __fmul_rn((float)(w[i] >> 8), dk) < __fsub_rn(rk, r[i]);
-                cv += c << (4 * i);
-                cv += up_cell ? (1u << (4 * i)) : 0u;
-                cv += up ? (1u << (4 * i)) : 0u;
+            for (int k = 0; k < 4; ++k) {
+                const float2 y = mul2_rn(v1[k], make_float2(rho, rho));
+                const uint32_t c0 = lds_u8(lut + (__float_as_uint(y.x) >> 19));
+                const uint32_t c1 = lds_u8(lut + (__float_as_uint(y.y) >> 19));
+                const float4 e0v = lds_f32x4(ve_base + c0 * 16u);
+                const float4 e1v = lds_f32x4(ve_base + c1 * 16u);
+                const float d0 = lds_f32(ve_base + c0 * 16u + 24u);   // d_{c+1}: field z of entry c+1
+                const float d1 = lds_f32(ve_base + c1 * 16u + 24u);
+                const bool up0 = e0v.x <= v1[k].x, up1 = e1v.x <= v1[k].y;
+                const float2 rk = make_float2(up0 ? e0v.w : e0v.y, up1 ? e1v.w : e1v.y);
+                const float2 dk = make_float2(up0 ? d0 : e0v.z, up1 ? d1 : e1v.z);
+                // u (r_k - r_{k+1}) with u = (w >> 8) 2^-24, as (w >> 8) ((r_k - r_{k+1}) 2^-24)
+                const float2 t = mul2_rn(make_float2((float)(w[2 * k] >> 8), (float)(w[2 * k + 1] >> 8)), dk);
+                const float2 gap = add2_rn(rk, neg2(r[k]));
+                c[2 * k] = c0 + (up0 ? 1u : 0u) + (t.x < gap.x ? 1u : 0u);
+                c[2 * k + 1] = c1 + (up1 ? 1u : 0u) + (t.y < gap.y ? 1u : 0u);
             }
         } else {
             const uint32_t lut = smem_addr(sm.lut_v_t);
-            float pa[2] = {0.f, 0.f}, pb[2] = {0.f, 0.f};
+            float ta[8], tb2[8];
 #pragma unroll
-            for (int i = 0; i < 8; ++i) {
-                const float x = v1[i];
-                const float y = __fmul_rn(x, rho);
-                const uint32_t c = lds_u8(lut + (__float_as_uint(y) >> 19));
-                const float4 e = lds_f32x4(ve_base + c * 32u);
-                const bool up = x > e.x;
-                cv += c << (4 * i);
-                cv += up ? (1u << (4 * i)) : 0u;
+            for (int k = 0; k < 4; ++k) {
+                const float2 y = mul2_rn(v1[k], make_float2(rho, rho));
+                const uint32_t c0 = lds_u8(lut + (__float_as_uint(y.x) >> 19));
+                const uint32_t c1 = lds_u8(lut + (__float_as_uint(y.y) >> 19));
+                const float4 e0v = lds_f32x4(ve_base + c0 * 16u);
+                const float4 e1v = lds_f32x4(ve_base + c1 * 16u);
+                const bool up0 = v1[k].x > e0v.x, up1 = v1[k].y > e1v.x;
+                c[2 * k] = c0 + (up0 ? 1u : 0u);
+                c[2 * k + 1] = c1 + (up1 ? 1u : 0u);
                 if (RECIPE == Q4_RECIPE_ZE_EDEN) {
-                    const float yh = up ? e.z : e.y;
-                    const float ta = __fmul_rn(y, y), tb2 = __fmul_rn(y, yh);
-                    const int h = i >> 2;
-                    pa[h] = ((i & 3) == 0) ? ta : __fadd_rn(pa[h], ta);
-                    pb[h] = ((i & 3) == 0) ? tb2 : __fadd_rn(pb[h], tb2);
+                    const float2 yh = make_float2(up0 ? e0v.z : e0v.y, up1 ? e1v.z : e1v.y);
+                    const float2 a2 = mul2_rn(y, y), b2 = mul2_rn(y, yh);
+                    ta[2 * k] = a2.x; ta[2 * k + 1] = a2.y;
+                    tb2[2 * k] = b2.x; tb2[2 * k + 1] = b2.y;
                 }
             }
             if (RECIPE == Q4_RECIPE_ZE_EDEN) {
+                // groups of 4 consecutive elements left to right, then the two groups
+                // (scalar sums: the terms are paired products)
+                float pa[2], pb[2];
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {
+                    pa[h] = __fadd_rn(__fadd_rn(__fadd_rn(ta[4 * h], ta[4 * h + 1]), ta[4 * h + 2]), ta[4 * h + 3]);
+                    pb[h] = __fadd_rn(__fadd_rn(__fadd_rn(tb2[4 * h], tb2[4 * h + 1]), tb2[4 * h + 2]), tb2[4 * h + 3]);
+                }
                 float A = __fadd_rn(pa[0], pa[1]);
                 float B = __fadd_rn(pb[0], pb[1]);
 #pragma unroll
@@ -786,6 +869,7 @@ __device__ __forceinline__ void compute_tile_full(const StepParams& P, const Dev
                 sv_store = (B == 0.f) ? 0.f : __fmul_rn(s_v, __fdiv_rn(A, B));
             }
         }
+        cv = pack8(c);
     }
 
     // ---- codes and scales out --------------------------------------------

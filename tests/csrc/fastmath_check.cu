@@ -1,5 +1,6 @@
 // Exhaustive GPU check of the step kernel's correctly rounded square root and
-// reciprocal against CUDA's IEEE intrinsics (__fsqrt_rn, __frcp_rn), and a
+// reciprocal (scalar and paired forms) against CUDA's IEEE intrinsics
+// (__fsqrt_rn, __frcp_rn), and a
 // randomised check of the reciprocal-based quotient against __fdiv_rn.
 // Test infrastructure: built and loaded by tests/test_gpu_fastmath.py.
 #include <cuda_runtime.h>
@@ -26,6 +27,27 @@ __global__ void sqrt_kernel(uint64_t lo, uint64_t hi, unsigned long long* count,
         const float x = __uint_as_float((unsigned)i);
         if (!q4::sqrt_fast_domain(x)) continue;
         if (!same(q4::sqrt_rn_normal<V>(x), __fsqrt_rn(x))) record(count, first, (unsigned)i);
+    }
+}
+
+// Paired versions: component 0 takes input i, component 1 input i ^ 1 (every
+// input appears in both lanes of some pair).
+__global__ void sqrt2_kernel(uint64_t lo, uint64_t hi, unsigned long long* count, unsigned* first) {
+    const uint64_t stride = (uint64_t)gridDim.x * blockDim.x;
+    for (uint64_t i = lo + (uint64_t)blockIdx.x * blockDim.x + threadIdx.x; i < hi; i += stride) {
+        const float x0 = __uint_as_float((unsigned)i), x1 = __uint_as_float((unsigned)i ^ 1u);
+        if (!q4::sqrt_fast_domain(x0) || !q4::sqrt_fast_domain(x1)) continue;
+        const float2 s = q4::sqrt2_rn_normal(make_float2(x0, x1));
+        if (!same(s.x, __fsqrt_rn(x0)) || !same(s.y, __fsqrt_rn(x1))) record(count, first, (unsigned)i);
+    }
+}
+
+__global__ void rcp2_kernel(uint64_t lo, uint64_t hi, unsigned long long* count, unsigned* first) {
+    const uint64_t stride = (uint64_t)gridDim.x * blockDim.x;
+    for (uint64_t i = lo + (uint64_t)blockIdx.x * blockDim.x + threadIdx.x; i < hi; i += stride) {
+        const float d0 = __uint_as_float((unsigned)i), d1 = __uint_as_float((unsigned)i ^ 1u);
+        const float2 y = q4::rcp2_rn_normal(make_float2(d0, d1));
+        if (!same(y.x, __frcp_rn(d0)) || !same(y.y, __frcp_rn(d1))) record(count, first, (unsigned)i);
     }
 }
 
@@ -65,6 +87,34 @@ __global__ void div_kernel(uint64_t n, uint64_t seed, unsigned long long* count,
     }
 }
 
+// The paired-arithmetic patterns the step kernel relies on, each against the
+// scalar operations: paired mul, add and fma alone; a single-use paired product
+// finished by a scalar add; a single-use paired product as the addend of a
+// paired fma.  (A single-use paired product feeding a paired add may be fused
+// by the compiler; the kernel never uses that pattern.)
+__global__ void pair_ops_kernel(uint64_t n, uint64_t seed, unsigned long long* count, unsigned* first) {
+    const uint64_t stride = (uint64_t)gridDim.x * blockDim.x;
+    for (uint64_t i = (uint64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += stride) {
+        const uint32_t u0 = mix(seed * 0x100000000ull + 3 * i), u1 = mix(seed * 0x100000000ull + 3 * i + 1);
+        const uint32_t u2 = mix(seed * 0x100000000ull + 3 * i + 2);
+        const float a = __uint_as_float(((90u + (u0 >> 26)) << 23) | (u0 & 0x7fffffu));
+        const float b = __uint_as_float(((90u + (u1 >> 26)) << 23) | (u1 & 0x7fffffu));
+        const float c = __uint_as_float(((110u + (u2 >> 27)) << 23) | (u2 & 0x7fffffu) | ((u2 & 0x4000000u) << 5));
+        const float2 m = q4::mul2_rn(make_float2(a, b), make_float2(b, c));
+        const float2 s = q4::add2_rn(make_float2(a, b), make_float2(c, -c));
+        const float2 f = q4::fma2_rn(make_float2(a, b), make_float2(c, a), make_float2(b, c));
+        const float2 pm = q4::mul2_rn(make_float2(a, b), make_float2(b, a));
+        const float2 p = make_float2(__fadd_rn(pm.x, c), __fadd_rn(pm.y, -c));
+        const float2 fm = q4::fma2_rn(make_float2(c, b), make_float2(b, c), q4::mul2_rn(make_float2(a, c), make_float2(c, a)));
+        const bool bad = !same(m.x, __fmul_rn(a, b)) || !same(m.y, __fmul_rn(b, c)) ||
+                         !same(s.x, __fadd_rn(a, c)) || !same(s.y, __fadd_rn(b, -c)) ||
+                         !same(f.x, __fmaf_rn(a, c, b)) || !same(f.y, __fmaf_rn(b, a, c)) ||
+                         !same(p.x, __fadd_rn(__fmul_rn(a, b), c)) || !same(p.y, __fadd_rn(__fmul_rn(b, a), -c)) ||
+                         !same(fm.x, __fmaf_rn(c, b, __fmul_rn(a, c))) || !same(fm.y, __fmaf_rn(b, c, __fmul_rn(c, a)));
+        if (bad) record(count, first, (unsigned)(i & 0xffffffffu));
+    }
+}
+
 }  // namespace
 
 extern "C" int fm_check(int which, int variant, uint64_t lo, uint64_t hi, unsigned long long* count,
@@ -77,6 +127,9 @@ extern "C" int fm_check(int which, int variant, uint64_t lo, uint64_t hi, unsign
         case 11: rcp_kernel<1><<<grid, block, 0, s>>>(lo, hi, count, first); break;
         case 12: rcp_kernel<2><<<grid, block, 0, s>>>(lo, hi, count, first); break;
         case 20: div_kernel<<<grid, block, 0, s>>>(hi, lo, count, first); break;
+        case 30: sqrt2_kernel<<<grid, block, 0, s>>>(lo, hi, count, first); break;
+        case 31: rcp2_kernel<<<grid, block, 0, s>>>(lo, hi, count, first); break;
+        case 40: pair_ops_kernel<<<grid, block, 0, s>>>(hi, lo, count, first); break;
         default: return -1;
     }
     return (int)cudaGetLastError();

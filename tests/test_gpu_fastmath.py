@@ -1,5 +1,6 @@
 """Exhaustive GPU check of the step kernel's correctly rounded square root and
-reciprocal, and a randomised check of its reciprocal-based quotient.
+reciprocal (scalar and paired FP32x2 forms), and a randomised check of its
+reciprocal-based quotient.
 
 The step kernel evaluates sqrt(v') and 1/d with a hardware approximation plus
 FMA corrections (q4_fastmath.cuh).  Bit-identity with the oracle requires that
@@ -63,6 +64,21 @@ def test_sqrt_exhaustive_zero_and_positive_normals():
 def test_rcp_exhaustive_normal_range():
     n, first = run_check(1, RCP_VARIANT, 0x00800000, 0x7E800000)
     assert n == 0, f"{n} mismatches, first input bits {first:#010x}"
+
+
+def test_paired_sqrt_exhaustive():
+    n, first = run_check(3, 0, 0, 0x7F800000)
+    assert n == 0, f"{n} mismatches, first input bits {first:#010x}"
+
+
+def test_paired_rcp_exhaustive():
+    n, first = run_check(3, 1, 0x00800000, 0x7E800000)
+    assert n == 0, f"{n} mismatches, first input bits {first:#010x}"
+
+
+def test_paired_patterns_round_like_scalar_ops():
+    n, first = run_check(4, 0, 7, 1 << 28)
+    assert n == 0, f"{n} mismatches, first sample {first}"
 
 
 def test_quotient_random_and_adversarial_pairs():
