@@ -39,6 +39,7 @@
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
+#include <cstddef>
 #include <cstdint>
 
 #include "q4_fastmath.cuh"
@@ -98,13 +99,6 @@ __device__ __forceinline__ uint32_t smem_addr(const void* p) { return (uint32_t)
 __device__ __forceinline__ void mbar_init(unsigned long long* bar, uint32_t count) {
     asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_addr(bar)), "r"(count) : "memory");
 }
-__device__ __forceinline__ void mbar_arrive_expect_tx(unsigned long long* bar, uint32_t bytes) {
-    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_addr(bar)), "r"(bytes)
-                 : "memory");
-}
-__device__ __forceinline__ void mbar_arrive(unsigned long long* bar) {
-    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_addr(bar)) : "memory");
-}
 __device__ __forceinline__ bool mbar_try_wait(unsigned long long* bar, uint32_t parity) {
     uint32_t ok;
     asm volatile(
@@ -126,19 +120,43 @@ __device__ __forceinline__ bool mbar_wait_bounded(unsigned long long* bar, uint3
     }
     return true;
 }
-__device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t bytes, unsigned long long* bar,
-                                          uint64_t policy) {
+// Predicated forms (no branch): the operation runs on lanes whose flag is set.
+__device__ __forceinline__ void mbar_arrive_expect_tx_if(uint32_t flag, uint32_t bar, uint32_t bytes) {
     asm volatile(
-        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1], %2, [%3], %4;" ::"r"(
-            smem_addr(dst)),
-        "l"(src), "r"(bytes), "r"(smem_addr(bar)), "l"(policy)
+        "{\n\t.reg .pred p;\n\tsetp.ne.u32 p, %0, 0;\n\t"
+        "@p mbarrier.arrive.expect_tx.shared::cta.b64 _, [%1], %2;\n\t}" ::"r"(flag),
+        "r"(bar), "r"(bytes)
         : "memory");
 }
-__device__ __forceinline__ void cp_async4(void* dst, const void* src) {
-    asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(smem_addr(dst)), "l"(src) : "memory");
+__device__ __forceinline__ void mbar_arrive_if(uint32_t flag, uint32_t bar) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tsetp.ne.u32 p, %0, 0;\n\t"
+        "@p mbarrier.arrive.shared::cta.b64 _, [%1];\n\t}" ::"r"(flag),
+        "r"(bar)
+        : "memory");
 }
-__device__ __forceinline__ void cp_async_arrive_noinc(unsigned long long* bar) {
-    asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(smem_addr(bar)) : "memory");
+__device__ __forceinline__ void bulk_load_if(uint32_t flag, uint32_t dst, const void* src, uint32_t bytes,
+                                             uint32_t bar, uint64_t policy) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tsetp.ne.u32 p, %0, 0;\n\t"
+        "@p cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint [%1], [%2], %3, [%4], "
+        "%5;\n\t}" ::"r"(flag),
+        "r"(dst), "l"(src), "r"(bytes), "r"(bar), "l"(policy)
+        : "memory");
+}
+__device__ __forceinline__ void cp_async4_if(uint32_t flag, uint32_t dst, const void* src) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tsetp.ne.u32 p, %0, 0;\n\t"
+        "@p cp.async.ca.shared.global [%1], [%2], 4;\n\t}" ::"r"(flag),
+        "r"(dst), "l"(src)
+        : "memory");
+}
+__device__ __forceinline__ void cp_async_arrive_noinc_if(uint32_t flag, uint32_t bar) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tsetp.ne.u32 p, %0, 0;\n\t"
+        "@p cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%1];\n\t}" ::"r"(flag),
+        "r"(bar)
+        : "memory");
 }
 __device__ __forceinline__ float lds_f32(uint32_t a) {
     float v;
@@ -920,58 +938,74 @@ __global__ void __launch_bounds__(kStepThreads, 1) step_kernel(const __grid_cons
     const int64_t W = (int64_t)gridDim.x * kStepWarps;
     const int64_t n_it = gw < P.total_pairs ? (P.total_pairs - 1 - gw) / W + 1 : 0;
 
-    // Issue cursor: tensor of the next tile to stage.
-    int ti = 0;
-    int64_t ib = 0, ie = __ldg(P.pair_prefix + 1);
-    const DevTensor* idesc = P.tensors;
+    // Issue cursor: tensor of the next tile to stage.  Lanes 0..7 each own one
+    // copy of every tile: 0 gradient, 1 master weight, 2 m codes, 3 v codes
+    // (bulk copies); 4, 5 the m scales and 6, 7 the v scales of the tile's two
+    // blocks (4-byte copies).  Each lane keeps its own source base pointer, so
+    // a tile's copies are computed and issued without loads or branches.
+    const uint32_t cp_field = lane == 0 ? (uint32_t)offsetof(DevTensor, grad)
+                              : lane == 1 ? (uint32_t)offsetof(DevTensor, param)
+                              : lane == 2 ? (uint32_t)offsetof(DevTensor, mc)
+                              : lane == 3 ? (uint32_t)offsetof(DevTensor, vc)
+                              : lane < 6  ? (uint32_t)offsetof(DevTensor, ms)
+                                          : (uint32_t)offsetof(DevTensor, vs);
+    const uint32_t cp_dst = lane == 0 ? (uint32_t)offsetof(Stage, grad)
+                            : lane == 1 ? (uint32_t)offsetof(Stage, param)
+                            : lane == 2 ? (uint32_t)offsetof(Stage, mc)
+                            : lane == 3 ? (uint32_t)offsetof(Stage, vc)
+                            : lane < 6  ? (uint32_t)offsetof(Stage, ms) + 4u * (lane & 1)
+                                        : (uint32_t)offsetof(Stage, vs) + 4u * (lane & 1);
+    const uint32_t cp_unit = lane == 0 ? 2u : lane == 1 ? 4u : lane < 4 ? 64u : 4u;
+    const uint32_t is_bulk = lane < 4 ? 1u : 0u;
+    const uint32_t is_scale = (lane >= 4 && lane < 8) ? 1u : 0u;
+    const uint32_t stage0 = smem_addr(&ws.st[0]);
+    const uint32_t bar0 = smem_addr(&ws.bar[0]);
 
-    // Lanes 0..7 each issue one copy of a tile: 0 gradient, 1 master weight,
-    // 2 m codes, 3 v codes (bulk copies); 4, 5 m scales and 6, 7 v scales of
-    // the tile's two blocks (4-byte copies).  Lane 0 first announces the
-    // bulk byte count; lanes 4..7 always arrive, with or without a copy.
+    int ti = -1;
+    int64_t ib = 0, ie = 0, i_numel = 0, i_nblk = 0;
+    bool i_fact = false;
+    const char* i_base = nullptr;
+
     auto issue = [&](int64_t it) {
         const int64_t pair = gw + it * W;
-        while (pair >= ie) {
-            ++ti;
-            ib = ie;
-            ie = __ldg(P.pair_prefix + ti + 1);
+        if (pair >= ie) {
+            do {
+                ++ti;
+                ib = ie;
+                ie = __ldg(P.pair_prefix + ti + 1);
+            } while (pair >= ie);
+            const DevTensor* dt = P.tensors + ti;
+            i_numel = dt->numel;
+            i_nblk = (i_numel + kBlock - 1) / kBlock;
+            i_fact = (RECIPE == Q4_RECIPE_FACTORED) && (dt->flags & DF_FACTORED);
+            i_base = *reinterpret_cast<const char* const*>(reinterpret_cast<const char*>(dt) + cp_field);
         }
-        idesc = P.tensors + ti;
         const int s = (int)(it % kStages);
-        Stage& st = ws.st[s];
-        unsigned long long* bar = &ws.bar[s];
-        if (lane < 8) {
-            const int64_t numel = idesc->numel;
-            const bool fact = (RECIPE == Q4_RECIPE_FACTORED) && (idesc->flags & DF_FACTORED);
-            const int64_t blk0 = (pair - ib) * 2;
-            const int64_t nblk = (numel + kBlock - 1) / kBlock;
-            const int nb = (nblk - blk0) >= 2 ? 2 : 1;
-            const int64_t e0 = blk0 * kBlock;
-            const int64_t left = numel - e0;
-            const uint32_t nel = left >= 2 * kBlock ? 2 * kBlock : (uint32_t)left;
-            const bool staged = (nel & 7u) == 0;
-            const uint32_t cbytes = (uint32_t)nb * 64u;
-            if (lane == 0) {
-                if (staged) mbar_arrive_expect_tx(bar, nel * 6u + cbytes + (fact ? 0u : cbytes));
-                else mbar_arrive(bar);   // ragged tail tile: computed from global memory
-            }
-            __syncwarp(0xffu);
-            if (staged) {
-                // the warp's earlier reads of this buffer precede the copies into it
-                if (lane < 4) asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-                if (lane == 0) bulk_load(st.grad, idesc->grad + e0, nel * 2u, bar, policy);
-                else if (lane == 1) bulk_load(st.param, idesc->param + e0, nel * 4u, bar, policy);
-                else if (lane == 2) bulk_load(st.mc, idesc->mc + blk0 * 64, cbytes, bar, policy);
-                else if (lane == 3) { if (!fact) bulk_load(st.vc, idesc->vc + blk0 * 64, cbytes, bar, policy); }
-                else {
-                    const int k = lane - 4;              // 0, 1: m scales; 2, 3: v scales
-                    const int b = k & 1;
-                    if (b < nb && (k < 2 || !fact))
-                        cp_async4(k < 2 ? &st.ms[b] : &st.vs[b], (k < 2 ? idesc->ms : idesc->vs) + blk0 + b);
-                }
-            }
-            if (lane >= 4) cp_async_arrive_noinc(bar);
-        }
+        const uint32_t bar = bar0 + 8u * (uint32_t)s;
+        const int64_t blk0 = (pair - ib) * 2;
+        const int64_t e0 = blk0 * kBlock;
+        const int64_t left = i_numel - e0;
+        const uint32_t nel = left >= 2 * kBlock ? 2u * kBlock : (uint32_t)left;
+        const uint32_t nb = (i_nblk - blk0) >= 2 ? 2u : 1u;
+        const uint32_t staged = (nel & 7u) == 0 ? 1u : 0u;
+        const uint32_t b = lane & 1;
+        const int64_t idx = lane < 2 ? e0 : (lane < 4 ? blk0 : blk0 + b);
+        const uint32_t bytes = lane < 2   ? nel * cp_unit
+                               : lane < 4 ? ((lane == 3 && i_fact) ? 0u : nb * 64u)
+                                          : ((b < nb && (lane < 6 || !i_fact)) ? 4u : 0u);
+        const char* src = i_base + idx * (int64_t)cp_unit;
+        const uint32_t dst = stage0 + (uint32_t)s * (uint32_t)sizeof(Stage) + cp_dst;
+        const uint32_t total = nel * 6u + nb * 64u * (i_fact ? 1u : 2u);
+        // lane 0 announces the bulk bytes (or completes its arrival for a ragged
+        // tile, which is then read from global memory) before any copy starts
+        mbar_arrive_expect_tx_if(lane == 0 && staged, bar, total);
+        mbar_arrive_if(lane == 0 && !staged, bar);
+        __syncwarp();
+        // the warp's earlier reads of this buffer precede the copies into it
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        bulk_load_if(staged & is_bulk & (bytes != 0u), dst, src, bytes, bar, policy);
+        cp_async4_if(staged & is_scale & (bytes != 0u), dst, src);
+        cp_async_arrive_noinc_if(is_scale, bar);
     };
 
     const int64_t pro = n_it < kStages - 1 ? n_it : kStages - 1;

@@ -21,6 +21,16 @@ def neq_f32(a: np.ndarray, b: np.ndarray) -> np.ndarray:
     return (a.view(np.uint32) != b.view(np.uint32)) & ~(np.isnan(a) & np.isnan(b))
 
 
+def bf16_close(a: np.ndarray, b: np.ndarray, theta_tol: float = 1e-6) -> np.ndarray:
+    """BF16 copies of weights that agree within theta_tol * max(1, |theta|):
+    equal up to one BF16 unit in the last place, or (near zero, where the two
+    may round to opposite signs) within the weight tolerance itself."""
+    fa = (a.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+    fb = (b.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+    d = np.abs(fa - fb)
+    return (d <= 2.0 ** -7 * np.maximum(np.abs(fa), np.abs(fb))) | (d <= 2 * theta_tol * np.maximum(1.0, np.abs(fb)))
+
+
 def bf16_bits(t: torch.Tensor) -> np.ndarray:
     return t.detach().cpu().view(torch.int16).numpy().view(np.uint16)
 
@@ -87,8 +97,7 @@ class Pair:
             if exact_theta:
                 out["bf16"] += int((b16 != o.param_bf16).sum())
             else:
-                diff = np.abs(b16.astype(np.int32) - o.param_bf16.astype(np.int32))
-                out["bf16"] += int((diff > 1).sum())
+                out["bf16"] += int((~bf16_close(b16, o.param_bf16, theta_tol)).sum())
             assert nb == ms.size
         return out
 

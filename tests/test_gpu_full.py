@@ -1,0 +1,178 @@
+"""Parity of the CUDA step with the oracle at the full workload sizes.
+
+Each workload is built exactly as bench.py builds it (one Q4State over the
+whole tensor list, inputs drawn on the device by the seeded generators of
+workloads.py, state zeroed) and stepped with the same single multi-tensor
+launch bench.py times.  The oracle cannot run 8 billion parameters in a test,
+so it checks samples it can compute on its own:
+
+  * packed (ZIP-SR, ZE-EDEN, factored 1-D) tensors: blocks are independent,
+    so for every tensor the first, the last and two seeded random blocks are
+    stepped by the oracle as one-block tensors (elem_offset = the block's
+    start, so the random draws are the same) from the same initial weights
+    and gradients, and compared bit for bit after every step;
+  * factored rank >= 2 tensors: their statistics span the whole tensor, so a
+    subset of whole tensors (the embedding and every tensor of the first and
+    last layer) is stepped by the oracle and compared with the factored
+    tolerances of the small-list test.
+
+Nothing the CUDA library writes is ever fed to the oracle: both sides start
+from the generator's initial weights and read the generator's gradients.
+"""
+import gc
+
+import numpy as np
+import pytest
+import torch
+
+import bit_quantized_adamw_q4adamw_b300 as q4
+from bit_quantized_adamw_q4adamw_b300 import workloads as W
+from oracle import oracle as O
+from parity_util import HYPER, bf16_bits, bf16_close, neq_f32
+
+pytestmark = pytest.mark.gpu
+
+BLOCK = 128
+
+
+def _build(w, dev):
+    st = q4.Q4State(w.tensors, w.recipe, device=dev)
+    for i, s in enumerate(w.tensors):
+        st.view(i, "param").copy_(W.init_param(s, i, device=dev))
+    st.init()
+    return st
+
+
+def _draw(w, st, t, dev):
+    for i, s in enumerate(w.tensors):
+        W.draw_grad(w, s, i, t, device=dev, out=st.view(i, "grad"))
+
+
+def _sample_blocks(numel, rng):
+    nb = (numel + BLOCK - 1) // BLOCK
+    return sorted({0, nb - 1, *rng.integers(0, nb, size=2).tolist()})
+
+
+def _free(st):
+    del st
+    gc.collect()
+    torch.cuda.empty_cache()
+
+
+def _run_packed(w, steps, flags, tensor_filter=None):
+    """Step the whole workload on the GPU; check sampled blocks of the tensors
+    tensor_filter accepts (all packed ones by default) against the oracle."""
+    dev = torch.device("cuda", 0)
+    st = _build(w, dev)
+    rng = np.random.default_rng(1234)
+    samples = []          # (tensor index, block, OracleTensor)
+    for i, s in enumerate(w.tensors):
+        factored = w.recipe == "factored" and bool(s.flags & W.T_FACTORED)
+        if factored or (tensor_filter is not None and not tensor_filter(i, s)):
+            continue
+        th = st.view(i, "param")
+        for b in _sample_blocks(s.numel, rng):
+            lo, hi = b * BLOCK, min(b * BLOCK + BLOCK, s.numel)
+            samples.append((i, b, O.OracleTensor.zeros_state(th[lo:hi].cpu().numpy(), i, rows=1, flags=s.flags,
+                                                              elem_offset=lo, recipe=w.recipe)))
+    h = HYPER
+    checked = 0
+    for t in range(w.first_step, w.first_step + steps):
+        _draw(w, st, t, dev)
+        grads = {}
+        for i, b, _ in samples:
+            if i not in grads:
+                grads[i] = st.view(i, "grad")
+        host_g = {}
+        for i, b, o in samples:
+            lo = b * BLOCK
+            hi = lo + o.param.size
+            host_g[(i, b)] = bf16_bits(grads[i][lo:hi])
+        st.step(t, h["lr"], h["beta1"], h["beta2"], h["eps"], h["weight_decay"], seed=0, flags=flags)
+        torch.cuda.synchronize()
+        assert st.status() == 0
+        for i, b, o in samples:
+            o.step(host_g[(i, b)], h["lr"], h["beta1"], h["beta2"], h["eps"], h["weight_decay"], t, 0, w.recipe,
+                   flags)
+            lo, n = b * BLOCK, o.param.size
+            th = st.view(i, "param")[lo:lo + n].cpu().numpy()
+            assert not neq_f32(th, o.param).any(), (w.name, i, b, t, "param")
+            assert np.array_equal(bf16_bits(st.view(i, "param_bf16")[lo:lo + n]), o.param_bf16), (w.name, i, b, t)
+            mc = st.view(i, "m_codes")[b * 64:(b + 1) * 64].cpu().numpy()
+            assert np.array_equal(mc, o.m_codes), (w.name, i, b, t, "m_codes")
+            ms = st.view(i, "m_scale")[b:b + 1].cpu().numpy()
+            assert not neq_f32(ms, o.m_scale).any(), (w.name, i, b, t, "m_scale")
+            vc = st.view(i, "v_codes")[b * 64:(b + 1) * 64].cpu().numpy()
+            assert np.array_equal(vc, o.v_codes), (w.name, i, b, t, "v_codes")
+            vs = st.view(i, "v_scale")[b:b + 1].cpu().numpy()
+            assert not neq_f32(vs, o.v_scale).any(), (w.name, i, b, t, "v_scale")
+            checked += 1
+    _free(st)
+    return checked
+
+
+def test_gpt1p4b_zipsr_lm_head_sr_sampled_blocks():
+    w = W.WORKLOADS["gpt1p4b_zipsr"]
+    n = _run_packed(w, 2, q4.Q4_LM_HEAD_SR_ACTIVE)
+    assert n >= 2 * 4 * 100
+
+
+@pytest.mark.parametrize("name", ["llama8b_zipsr", "llama8b_zeeden"])
+def test_llama8b_sampled_blocks(name):
+    w = W.WORKLOADS[name]
+    n = _run_packed(w, 2, 0)
+    assert n >= 2 * 4 * 100
+
+
+def test_qwen0p6b_factored_whole_tensors_and_sampled_blocks():
+    w = W.WORKLOADS["qwen0p6b_factored"]
+    dev = torch.device("cuda", 0)
+    st = _build(w, dev)
+    per_layer = 11
+    last0 = 1 + 27 * per_layer
+    whole = [0, *range(1, 1 + per_layer), *range(last0, last0 + per_layer), len(w.tensors) - 1]
+    ora = {}
+    for i in whole:
+        s = w.tensors[i]
+        ora[i] = O.OracleTensor.zeros_state(st.view(i, "param").cpu().numpy(), i, rows=s.rows, flags=s.flags,
+                                            recipe="factored")
+    rng = np.random.default_rng(99)
+    blocks = []
+    for i, s in enumerate(w.tensors):
+        if i in ora or (s.flags & W.T_FACTORED):
+            continue
+        th = st.view(i, "param")
+        for b in _sample_blocks(s.numel, rng):
+            lo, hi = b * BLOCK, min(b * BLOCK + BLOCK, s.numel)
+            blocks.append((i, b, O.OracleTensor.zeros_state(th[lo:hi].cpu().numpy(), i, rows=1, flags=s.flags,
+                                                             elem_offset=lo, recipe="factored")))
+    h = HYPER
+    for t in (1, 2):
+        _draw(w, st, t, dev)
+        host_g = {i: bf16_bits(st.view(i, "grad")) for i in ora}
+        host_b = {(i, b): bf16_bits(st.view(i, "grad")[b * BLOCK:b * BLOCK + o.param.size]) for i, b, o in blocks}
+        st.step(t, h["lr"], h["beta1"], h["beta2"], h["eps"], h["weight_decay"], seed=0)
+        torch.cuda.synchronize()
+        assert st.status() == 0
+        for i, o in ora.items():
+            o.step(host_g[i], h["lr"], h["beta1"], h["beta2"], h["eps"], h["weight_decay"], t, 0, "factored")
+            assert np.array_equal(st.view(i, "m_codes").cpu().numpy(), o.m_codes), (i, t)
+            assert not neq_f32(st.view(i, "m_scale").cpu().numpy(), o.m_scale).any(), (i, t)
+            th = st.view(i, "param").cpu().numpy()
+            d = np.abs(th.astype(np.float64) - o.param)
+            assert (d <= 1e-6 * np.maximum(1.0, np.abs(o.param))).all(), (i, t, float(d.max()))
+            assert bf16_close(bf16_bits(st.view(i, "param_bf16")), o.param_bf16).all(), (i, t)
+            if o.factored:
+                R = st.view(i, "v_row").cpu().numpy().astype(np.float64)
+                C = st.view(i, "v_col").cpu().numpy().astype(np.float64)
+                assert (np.abs(R - o.v_row) <= 1e-5 * np.abs(o.v_row)).all(), (i, t)
+                assert (np.abs(C - o.v_col) <= 1e-5 * np.abs(o.v_col)).all(), (i, t)
+            else:
+                assert np.array_equal(st.view(i, "v_codes").cpu().numpy(), o.v_codes), (i, t)
+                assert not neq_f32(st.view(i, "v_scale").cpu().numpy(), o.v_scale).any(), (i, t)
+        for i, b, o in blocks:
+            o.step(host_b[(i, b)], h["lr"], h["beta1"], h["beta2"], h["eps"], h["weight_decay"], t, 0, "factored")
+            lo, n = b * BLOCK, o.param.size
+            assert not neq_f32(st.view(i, "param")[lo:lo + n].cpu().numpy(), o.param).any(), (i, b, t)
+            assert np.array_equal(st.view(i, "v_codes")[b * 64:(b + 1) * 64].cpu().numpy(), o.v_codes), (i, b, t)
+    _free(st)
