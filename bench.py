@@ -55,6 +55,8 @@ def parse():
     ap.add_argument("--cpu-seconds", type=float, default=12.0, help="target oracle time of the CPU sample")
     ap.add_argument("--tensors", type=int, default=0,
                     help="keep only the first N tensors of the workload (small cases for profiling)")
+    ap.add_argument("--tensor-slice", default="",
+                    help="keep tensors a:b of the workload (e.g. 1:10 = the first decoder layer of the 8B set)")
     return ap.parse_args()
 
 
@@ -143,9 +145,14 @@ class ClockSampler:
 
 
 def kernel_source_hash() -> str:
-    p = os.path.join(ROOT, "bit_quantized_adamw_q4adamw_b300", "csrc", "q4_step.cu")
-    with open(p, "rb") as f:
-        return hashlib.sha256(f.read()).hexdigest()[:16]
+    """Hash of every source of the CUDA library (a traffic record is valid
+    only for the kernel it was measured on)."""
+    h = hashlib.sha256()
+    d = os.path.join(ROOT, "bit_quantized_adamw_q4adamw_b300", "csrc")
+    for name in sorted(os.listdir(d)):
+        with open(os.path.join(d, name), "rb") as f:
+            h.update(name.encode() + b"\0" + f.read())
+    return h.hexdigest()[:16]
 
 
 def traffic_record(workload: str):
@@ -249,6 +256,9 @@ def get_workload(args):
     w = W.WORKLOADS[args.workload]
     if args.tensors > 0:
         w = dataclasses.replace(w, name=f"{w.name}[:{args.tensors}]", tensors=w.tensors[:args.tensors])
+    if args.tensor_slice:
+        a, b = (int(x) for x in args.tensor_slice.split(":"))
+        w = dataclasses.replace(w, name=f"{w.name}[{a}:{b}]", tensors=w.tensors[a:b])
     return w
 
 

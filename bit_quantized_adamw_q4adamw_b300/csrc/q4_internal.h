@@ -14,6 +14,7 @@ constexpr int kBlock = 128;        // elements per quantisation block
 constexpr int kStepWarps = 16;     // warps per CTA of the step kernel
 constexpr int kStepThreads = kStepWarps * 32;
 constexpr int kStages = 4;         // staging buffers per warp (tiles in flight)
+static_assert((kStages & (kStages - 1)) == 0 && kStages >= 2, "the staging ring is indexed with a mask");
 constexpr int kVLut = 4096;        // entries of the log-bucket candidate tables
                                    // (one per bits(x)>>19 of a non-negative float)
 

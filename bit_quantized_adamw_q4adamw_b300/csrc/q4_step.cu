@@ -5,9 +5,11 @@
 // lanes 16-31 block 2p+1, and lane j of a half owns the 8 consecutive
 // elements 8j..8j+7 of its block.
 //
-// Data movement.  The grid is persistent (one 16-warp CTA per SM); warp w of
-// W takes tiles w, w+W, w+2W, ... of the global tile list of all tensors (the
-// tensor-chunk table is the prefix sum of tiles per tensor).  Each warp keeps
+// Data movement.  The grid is persistent (one 16-warp CTA per SM).  The global
+// list of tiles of all tensors (the tensor-chunk table is the prefix sum of
+// tiles per tensor) is cut into chunks of kChunk consecutive tiles, dealt
+// round-robin to the warps of the grid; within a chunk and a tensor each copy
+// source advances by a constant per tile.  Each warp keeps
 // a ring of kStages shared-memory staging buffers: while it computes tile k,
 // tiles k+1 .. k+kStages-1 are in flight.  Lanes 0-7 fill a buffer in one
 // pass: four cp.async.bulk copies (BF16 gradient, FP32 master weight, packed m
@@ -51,6 +53,7 @@ namespace {
 constexpr float kMagic = 12582912.0f;                // 1.5 * 2^23: rounds to an integer in the low mantissa bits
 constexpr float kTwoM24 = 5.9604644775390625e-08f;   // 2^-24
 constexpr long long kWaitCycles = 2000000000ll;      // about one second at the SM clock
+constexpr int kChunk = 16;                           // consecutive tiles a warp takes at a time
 
 struct __align__(16) Stage {
     uint4 grad[32];     // 256 BF16 gradients
@@ -934,15 +937,36 @@ __global__ void __launch_bounds__(kStepThreads, 1) step_kernel(const __grid_cons
     const float my_vl1 = P.tab.vl[j < 15 ? j + 1 : 15];
     const uint64_t policy = evict_first_policy();
 
+    // Work split: the global tile list is cut into chunks of kChunk consecutive
+    // tiles, dealt round-robin to the W warps of the grid (warp w takes chunks
+    // w, w+W, ...).  Inside a chunk a warp's tiles are consecutive, so within a
+    // tensor every copy source advances by a constant; dealing chunks
+    // round-robin spreads tensors of unequal cost over all warps.
     const int64_t gw = (int64_t)blockIdx.x * kStepWarps + warp;
     const int64_t W = (int64_t)gridDim.x * kStepWarps;
-    const int64_t n_it = gw < P.total_pairs ? (P.total_pairs - 1 - gw) / W + 1 : 0;
+    const int64_t total = P.total_pairs;
+    const int64_t n_chunks = (total + kChunk - 1) / kChunk;
+    if (gw >= n_chunks) return;
+    const int64_t my_chunks = (n_chunks - 1 - gw) / W + 1;
+    const bool owns_last = (n_chunks - 1) % W == gw;
+    const int n_it = (int)(my_chunks * kChunk - (owns_last ? n_chunks * kChunk - total : 0));
+    const int64_t t_begin = gw * kChunk;
+    const int64_t chunk_jump = (W - 1) * kChunk;   // tiles skipped between two of this warp's chunks
 
-    // Issue cursor: tensor of the next tile to stage.  Lanes 0..7 each own one
-    // copy of every tile: 0 gradient, 1 master weight, 2 m codes, 3 v codes
-    // (bulk copies); 4, 5 the m scales and 6, 7 the v scales of the tile's two
-    // blocks (4-byte copies).  Each lane keeps its own source base pointer, so
-    // a tile's copies are computed and issued without loads or branches.
+    // Tensor holding t_begin: the last t with prefix[t] <= t_begin.
+    int t0 = 0;
+    {
+        int lo = 0, hi = P.n_tensors - 1;
+        while (lo < hi) {
+            const int mid = (lo + hi + 1) >> 1;
+            if (__ldg(P.pair_prefix + mid) <= t_begin) lo = mid; else hi = mid - 1;
+        }
+        t0 = lo;
+    }
+
+    // Issue cursor.  Lanes 0..7 each own one copy of every tile: 0 gradient,
+    // 1 master weight, 2 m codes, 3 v codes (bulk copies); 4, 5 the m scales and
+    // 6, 7 the v scales of the tile's two blocks (4-byte copies).
     const uint32_t cp_field = lane == 0 ? (uint32_t)offsetof(DevTensor, grad)
                               : lane == 1 ? (uint32_t)offsetof(DevTensor, param)
                               : lane == 2 ? (uint32_t)offsetof(DevTensor, mc)
@@ -955,47 +979,69 @@ __global__ void __launch_bounds__(kStepThreads, 1) step_kernel(const __grid_cons
                             : lane == 3 ? (uint32_t)offsetof(Stage, vc)
                             : lane < 6  ? (uint32_t)offsetof(Stage, ms) + 4u * (lane & 1)
                                         : (uint32_t)offsetof(Stage, vs) + 4u * (lane & 1);
-    const uint32_t cp_unit = lane == 0 ? 2u : lane == 1 ? 4u : lane < 4 ? 64u : 4u;
+    // bytes of this lane's copy for a complete tile, and the source advance per tile
+    const uint32_t cp_full = lane == 0 ? 512u : lane == 1 ? 1024u : lane < 4 ? 128u : lane < 8 ? 4u : 0u;
+    const int64_t cp_step = lane == 0 ? 512 : lane == 1 ? 1024 : lane < 4 ? 128 : 8;
+    const uint32_t cp_first = (lane >= 4 && (lane & 1)) ? 4u : 0u;    // second block's scale
     const uint32_t is_bulk = lane < 4 ? 1u : 0u;
     const uint32_t is_scale = (lane >= 4 && lane < 8) ? 1u : 0u;
     const uint32_t stage0 = smem_addr(&ws.st[0]);
     const uint32_t bar0 = smem_addr(&ws.bar[0]);
 
-    int ti = -1;
-    int64_t ib = 0, ie = 0, i_numel = 0, i_nblk = 0;
+    int i_t = t0;
+    int64_t i_tile = t_begin;                                // global tile index
+    int i_k = 0;                                             // tile index within the chunk
+    int64_t i_p = t_begin - __ldg(P.pair_prefix + t0);      // tile index within the tensor
+    int64_t i_n = __ldg(P.pair_prefix + t0 + 1) - __ldg(P.pair_prefix + t0);
+    int64_t i_numel = 0;
+    uint32_t i_bytes = 0, i_total = 0;
     bool i_fact = false;
-    const char* i_base = nullptr;
+    const char* i_src = nullptr;
+    auto load_issue_tensor = [&]() {
+        const DevTensor* dt = P.tensors + i_t;
+        i_numel = dt->numel;
+        i_fact = (RECIPE == Q4_RECIPE_FACTORED) && (dt->flags & DF_FACTORED);
+        const char* base = *reinterpret_cast<const char* const*>(reinterpret_cast<const char*>(dt) + cp_field);
+        i_src = base + cp_first + i_p * cp_step;
+        i_bytes = (i_fact && (lane == 3 || lane >= 6)) ? 0u : cp_full;
+        i_total = 1536u + 128u + (i_fact ? 0u : 128u);
+    };
+    load_issue_tensor();
 
-    auto issue = [&](int64_t it) {
-        const int64_t pair = gw + it * W;
-        if (pair >= ie) {
+    auto issue = [&](int it) {
+        if (i_k == kChunk) {
+            // next chunk of this warp: seek forward to the tensor holding it
+            i_k = 0;
+            i_tile += chunk_jump;
+            while (i_tile >= __ldg(P.pair_prefix + i_t + 1)) ++i_t;
+            const int64_t pb = __ldg(P.pair_prefix + i_t);
+            i_p = i_tile - pb;
+            i_n = __ldg(P.pair_prefix + i_t + 1) - pb;
+            load_issue_tensor();
+        } else if (i_p == i_n) {
             do {
-                ++ti;
-                ib = ie;
-                ie = __ldg(P.pair_prefix + ti + 1);
-            } while (pair >= ie);
-            const DevTensor* dt = P.tensors + ti;
-            i_numel = dt->numel;
-            i_nblk = (i_numel + kBlock - 1) / kBlock;
-            i_fact = (RECIPE == Q4_RECIPE_FACTORED) && (dt->flags & DF_FACTORED);
-            i_base = *reinterpret_cast<const char* const*>(reinterpret_cast<const char*>(dt) + cp_field);
+                ++i_t;
+                i_n = __ldg(P.pair_prefix + i_t + 1) - __ldg(P.pair_prefix + i_t);
+            } while (i_n == 0);
+            i_p = 0;
+            load_issue_tensor();
         }
-        const int s = (int)(it % kStages);
+        const int s = it & (kStages - 1);
         const uint32_t bar = bar0 + 8u * (uint32_t)s;
-        const int64_t blk0 = (pair - ib) * 2;
-        const int64_t e0 = blk0 * kBlock;
-        const int64_t left = i_numel - e0;
-        const uint32_t nel = left >= 2 * kBlock ? 2u * kBlock : (uint32_t)left;
-        const uint32_t nb = (i_nblk - blk0) >= 2 ? 2u : 1u;
-        const uint32_t staged = (nel & 7u) == 0 ? 1u : 0u;
-        const uint32_t b = lane & 1;
-        const int64_t idx = lane < 2 ? e0 : (lane < 4 ? blk0 : blk0 + b);
-        const uint32_t bytes = lane < 2   ? nel * cp_unit
-                               : lane < 4 ? ((lane == 3 && i_fact) ? 0u : nb * 64u)
-                                          : ((b < nb && (lane < 6 || !i_fact)) ? 4u : 0u);
-        const char* src = i_base + idx * (int64_t)cp_unit;
         const uint32_t dst = stage0 + (uint32_t)s * (uint32_t)sizeof(Stage) + cp_dst;
-        const uint32_t total = nel * 6u + nb * 64u * (i_fact ? 1u : 2u);
+        uint32_t bytes = i_bytes, total = i_total, staged = 1u;
+        if (i_p == i_n - 1) {
+            // a tensor's last tile may hold one block and a partial block
+            const int64_t left = i_numel - i_p * 2 * kBlock;
+            const uint32_t nel = left >= 2 * kBlock ? 2u * kBlock : (uint32_t)left;
+            const uint32_t nb = nel > (uint32_t)kBlock ? 2u : 1u;
+            staged = (nel & 7u) == 0 ? 1u : 0u;
+            const uint32_t b = lane & 1;
+            bytes = lane < 2   ? nel * (lane == 0 ? 2u : 4u)
+                    : lane < 4 ? ((lane == 3 && i_fact) ? 0u : nb * 64u)
+                               : ((b < nb && (lane < 6 || !i_fact)) ? 4u : 0u);
+            total = nel * 6u + nb * 64u * (i_fact ? 1u : 2u);
+        }
         // lane 0 announces the bulk bytes (or completes its arrival for a ragged
         // tile, which is then read from global memory) before any copy starts
         mbar_arrive_expect_tx_if(lane == 0 && staged, bar, total);
@@ -1003,49 +1049,68 @@ __global__ void __launch_bounds__(kStepThreads, 1) step_kernel(const __grid_cons
         __syncwarp();
         // the warp's earlier reads of this buffer precede the copies into it
         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-        bulk_load_if(staged & is_bulk & (bytes != 0u), dst, src, bytes, bar, policy);
-        cp_async4_if(staged & is_scale & (bytes != 0u), dst, src);
+        bulk_load_if(staged & is_bulk & (bytes != 0u), dst, i_src, bytes, bar, policy);
+        cp_async4_if(staged & is_scale & (bytes != 0u), dst, i_src);
         cp_async_arrive_noinc_if(is_scale, bar);
+        i_src += cp_step;
+        ++i_p;
+        ++i_tile;
+        ++i_k;
     };
 
-    const int64_t pro = n_it < kStages - 1 ? n_it : kStages - 1;
-    for (int64_t it = 0; it < pro; ++it) issue(it);
+    const int pro = n_it < kStages - 1 ? n_it : kStages - 1;
+    for (int it = 0; it < pro; ++it) issue(it);
     __syncwarp();
 
     // Compute cursor.
-    int ci = -1;
-    int64_t cb = 0, ce = 0;
-    for (int64_t it = 0; it < n_it; ++it) {
+    int c_t = t0;
+    int64_t c_tile = t_begin;
+    int c_k = 0;
+    int64_t c_p = t_begin - __ldg(P.pair_prefix + t0);
+    int64_t c_n = __ldg(P.pair_prefix + t0 + 1) - __ldg(P.pair_prefix + t0);
+    reinterpret_cast<uint32_t*>(&ws.desc)[lane] = __ldg(reinterpret_cast<const uint32_t*>(P.tensors + c_t) + lane);
+    __syncwarp();
+    for (int it = 0; it < n_it; ++it) {
         if (it + kStages - 1 < n_it) issue(it + kStages - 1);
-        const int s = (int)(it % kStages);
+        const int s = it & (kStages - 1);
         const bool ok = __all_sync(0xffffffffu, mbar_wait_bounded(&ws.bar[s], (uint32_t)((it / kStages) & 1)));
         if (!ok) {
             if (lane == 0) atomicOr(P.status, ST_STAGE_TIMEOUT);
             // drain the copies this warp still has in flight, then leave
-            const int64_t last = (it + kStages - 1 < n_it) ? it + kStages - 1 : n_it - 1;
-            for (int64_t k = it + 1; k <= last; ++k)
-                (void)mbar_wait_bounded(&ws.bar[k % kStages], (uint32_t)((k / kStages) & 1));
+            const int last = (it + kStages - 1 < n_it) ? it + kStages - 1 : n_it - 1;
+            for (int k = it + 1; k <= last; ++k)
+                (void)mbar_wait_bounded(&ws.bar[k & (kStages - 1)], (uint32_t)((k / kStages) & 1));
             return;
         }
-        const int64_t pair = gw + it * W;
-        if (pair >= ce) {
-            while (pair >= ce) {
-                ++ci;
-                cb = ce;
-                ce = __ldg(P.pair_prefix + ci + 1);
+        if (c_k == kChunk || c_p == c_n) {
+            if (c_k == kChunk) {
+                c_k = 0;
+                c_tile += chunk_jump;
+                while (c_tile >= __ldg(P.pair_prefix + c_t + 1)) ++c_t;
+            } else {
+                do {
+                    ++c_t;
+                } while (__ldg(P.pair_prefix + c_t + 1) == __ldg(P.pair_prefix + c_t));
             }
-            reinterpret_cast<uint32_t*>(&ws.desc)[lane] = __ldg(reinterpret_cast<const uint32_t*>(P.tensors + ci) + lane);
+            const int64_t pb = __ldg(P.pair_prefix + c_t);
+            c_p = c_tile - pb;
+            c_n = __ldg(P.pair_prefix + c_t + 1) - pb;
+            reinterpret_cast<uint32_t*>(&ws.desc)[lane] =
+                __ldg(reinterpret_cast<const uint32_t*>(P.tensors + c_t) + lane);
             __syncwarp();
         }
-        const int64_t pl = pair - cb;
-        const int64_t left = ws.desc.numel - pl * 2 * kBlock;
-        if (left >= 2 * kBlock) {
-            compute_tile_full<RECIPE>(P, ws.desc, pl, ws.st[s], lane, sm, ws.wt, my_nf4, my_nf4t, my_vl, my_vt,
+        const bool full = c_p < c_n - 1 || ws.desc.numel - c_p * 2 * kBlock >= 2 * kBlock;
+        if (full) {
+            compute_tile_full<RECIPE>(P, ws.desc, c_p, ws.st[s], lane, sm, ws.wt, my_nf4, my_nf4t, my_vl, my_vt,
                                       my_vl1);
         } else {
-            compute_tile<RECIPE>(P, ws.desc, pl, (left & 7) == 0 ? &ws.st[s] : nullptr, lane, sm, ws.wt, my_nf4,
+            const int64_t left = ws.desc.numel - c_p * 2 * kBlock;
+            compute_tile<RECIPE>(P, ws.desc, c_p, (left & 7) == 0 ? &ws.st[s] : nullptr, lane, sm, ws.wt, my_nf4,
                                  my_nf4t, my_vl, my_vt);
         }
+        ++c_p;
+        ++c_tile;
+        ++c_k;
         __syncwarp();
     }
 }
