@@ -72,7 +72,8 @@ struct __align__(256) WarpTables {
     float deqm[32];        // [half][16] NF4 level * old s_m
     float deqv[32];        // [half][16] v level * old s_v
     float2 mt[2][64];      // fast path: [half][linear bucket] {NF4 threshold of the candidate * new s_m, candidate}
-    float4 ve[2][16];      // fast path: [half][cell] v search entry (see compute_tile_full)
+    float4 ve[2][16];      // fast path, per half: ZIP-SR a_{c+1} by cell (floats 0..15) and (r_k, d_k)
+                           // by cell (float2 8..23); RTN {t_c s_v, L_c, L_{c+1}} by cell
     float tm[32];          // general path: [half][16] NF4 threshold * new s_m
     float am[32];          // [half][16] NF4 level * new s_m (LM-head SR)
     float av[32];          // [half][16] v level * new s_v (ZIP-SR) or v threshold * new s_v (RTN)
@@ -279,20 +280,26 @@ __device__ __forceinline__ float2 neg2(float2 a) { return make_float2(-a.x, -a.y
 // theta decay - step (m' r) = theta decay + (-step) (m' r) exactly.
 // Lanes with a v' outside the fast square root's domain take the scalar IEEE
 // sequence.
-__device__ __forceinline__ void update_pairs(const StepParams& P, const float2 g[4], const float2 m[4],
-                                             const float2 v[4], bool fact, float2 m1[4], float2 v1[4],
-                                             float2 th[4], float2 r[4]) {
+__device__ __forceinline__ float update_pairs(const StepParams& P, const float2 g[4], const float2 m[4],
+                                              const float2 v[4], bool fact, float2 m1[4], float2 v1[4],
+                                              float2 th[4], float2 r[4]) {
 #pragma unroll
     for (int k = 0; k < 4; ++k) {
         m1[k] = fma2_rn(P.x2_beta1, m[k], mul2_rn(P.x2_omb1, g[k]));
         if (!fact) v1[k] = fma2_rn(P.x2_beta2, v[k], mul2_rn(P.x2_omb2, mul2_rn(g[k], g[k])));
     }
-    bool tiny = false;
-    float vmax = 0.f;
+    // lane max of v' (the block scale input) and min (the fast square root's
+    // domain: every v' is +0 or in [2^-100, +inf))
+    float vmax = 0.f, vmin = INFINITY;
 #pragma unroll
     for (int k = 0; k < 4; ++k) {
-        tiny = tiny || tiny_positive(v1[k].x) || tiny_positive(v1[k].y);
         vmax = fmaxf(vmax, fmaxf(v1[k].x, v1[k].y));
+        vmin = fminf(vmin, fminf(v1[k].x, v1[k].y));
+    }
+    bool tiny = false;
+    if (!(vmin >= 0x1p-100f)) {
+#pragma unroll
+        for (int k = 0; k < 4; ++k) tiny = tiny || tiny_positive(v1[k].x) || tiny_positive(v1[k].y);
     }
     if (P.fast_math && !tiny && vmax < INFINITY) {
 #pragma unroll
@@ -313,6 +320,7 @@ __device__ __forceinline__ void update_pairs(const StepParams& P, const float2 g
             th[k].y = __fsub_rn(__fmul_rn(th[k].y, P.decay), __fmul_rn(P.step_size, __fmul_rn(m1[k].y, r[k].y)));
         }
     }
+    return vmax;
 }
 
 // Packs eight 4-bit codes (element i in bits 4i..4i+3) with a shallow tree.
@@ -735,7 +743,7 @@ __device__ __forceinline__ void compute_tile_full(const StepParams& P, const Dev
             }
         }
     }
-    update_pairs(P, g, m, v, fact, m1, v1, th, r);
+    const float vmax_lane = update_pairs(P, g, m, v, fact, m1, v1, th, r);
 
     // ---- weights out ----------------------------------------------------
     __stcs(reinterpret_cast<float4*>(d.param + e0), make_float4(th[0].x, th[0].y, th[1].x, th[1].y));
@@ -750,14 +758,11 @@ __device__ __forceinline__ void compute_tile_full(const StepParams& P, const Dev
     }
 
     // ---- block scales -----------------------------------------------------
-    float amax = 0.f, vmax = 0.f;
+    float amax = 0.f;
 #pragma unroll
-    for (int k = 0; k < 4; ++k) {
-        amax = fmaxf(amax, fmaxf(fabsf(m1[k].x), fabsf(m1[k].y)));
-        vmax = fmaxf(vmax, fmaxf(v1[k].x, v1[k].y));
-    }
+    for (int k = 0; k < 4; ++k) amax = fmaxf(amax, fmaxf(fabsf(m1[k].x), fabsf(m1[k].y)));
     const float s_m = half_max(amax, half);
-    const float s_v = fact ? 0.f : half_max(vmax, half);
+    const float s_v = fact ? 0.f : half_max(vmax_lane, half);
 
     const bool fast = __all_sync(0xffffffffu, !m_sr && scale_in_fast_range(s_m) &&
                                                   (fact || scale_in_fast_range(s_v)));
@@ -789,15 +794,15 @@ __device__ __forceinline__ void compute_tile_full(const StepParams& P, const Dev
     }
     if (!fact) {
         if (RECIPE == Q4_RECIPE_ZIP_SR) {
-            // ve[half][c] = {a_{c+1}, r_c, d_c, r_{c+1}} with a_k the level at the new
-            // scale, r_k its preconditioner, d_k = (r_k - r_{k+1}) 2^-24; d_{c+1} is
-            // read from the next entry.
+            // a_k = level k at the new scale, r_k its preconditioner, d_k =
+            // (r_k - r_{k+1}) 2^-24: the cell search reads a_{c+1}, then (r_k, d_k).
             const float a = __fmul_rn(my_vl, s_v);
             const float rk = P.fast_math ? precond<true>(P, a) : precond<false>(P, a);
             const float rk1 = __shfl_down_sync(0xffffffffu, rk, 1);
             const float dk = j < 15 ? __fmul_rn(__fsub_rn(rk, rk1), kTwoM24) : 0.f;
             const float a1 = __shfl_down_sync(0xffffffffu, a, 1);
-            wt.ve[half][j] = make_float4(a1, rk, dk, rk1);
+            reinterpret_cast<float*>(&wt.ve[half][0])[j] = a1;                  // a_{c+1} by cell
+            reinterpret_cast<float2*>(&wt.ve[half][4])[j] = make_float2(rk, dk);  // (r_k, d_k) by cell
         } else {
             // ve[half][c] = {t_c * s_v, L_c, L_{c+1}} (unscaled levels for EDEN)
             wt.ve[half][j] = make_float4(__fmul_rn(my_vt, s_v), my_vl, my_vl1, 0.f);
@@ -838,18 +843,18 @@ __device__ __forceinline__ void compute_tile_full(const StepParams& P, const Dev
                 const float2 y = mul2_rn(v1[k], make_float2(rho, rho));
                 const uint32_t c0 = lds_u8(lut + (__float_as_uint(y.x) >> 19));
                 const uint32_t c1 = lds_u8(lut + (__float_as_uint(y.y) >> 19));
-                const float4 e0v = lds_f32x4(ve_base + c0 * 16u);
-                const float4 e1v = lds_f32x4(ve_base + c1 * 16u);
-                const float d0 = lds_f32(ve_base + c0 * 16u + 24u);   // d_{c+1}: field z of entry c+1
-                const float d1 = lds_f32(ve_base + c1 * 16u + 24u);
-                const bool up0 = e0v.x <= v1[k].x, up1 = e1v.x <= v1[k].y;
-                const float2 rk = make_float2(up0 ? e0v.w : e0v.y, up1 ? e1v.w : e1v.y);
-                const float2 dk = make_float2(up0 ? d0 : e0v.z, up1 ? d1 : e1v.z);
+                const bool up0 = lds_f32(ve_base + c0 * 4u) <= v1[k].x;
+                const bool up1 = lds_f32(ve_base + c1 * 4u) <= v1[k].y;
+                const uint32_t k0 = c0 + (up0 ? 1u : 0u), k1 = c1 + (up1 ? 1u : 0u);
+                const float2 e0v = lds_f32x2(ve_base + 64u + k0 * 8u);
+                const float2 e1v = lds_f32x2(ve_base + 64u + k1 * 8u);
+                const float2 rk = make_float2(e0v.x, e1v.x);
+                const float2 dk = make_float2(e0v.y, e1v.y);
                 // u (r_k - r_{k+1}) with u = (w >> 8) 2^-24, as (w >> 8) ((r_k - r_{k+1}) 2^-24)
                 const float2 t = mul2_rn(make_float2((float)(w[2 * k] >> 8), (float)(w[2 * k + 1] >> 8)), dk);
                 const float2 gap = add2_rn(rk, neg2(r[k]));
-                c[2 * k] = c0 + (up0 ? 1u : 0u) + (t.x < gap.x ? 1u : 0u);
-                c[2 * k + 1] = c1 + (up1 ? 1u : 0u) + (t.y < gap.y ? 1u : 0u);
+                c[2 * k] = k0 + (t.x < gap.x ? 1u : 0u);
+                c[2 * k + 1] = k1 + (t.y < gap.y ? 1u : 0u);
             }
         } else {
             const uint32_t lut = smem_addr(sm.lut_v_t);
