@@ -98,7 +98,7 @@ Layout make_layout(const q4adamw_tensor_t* t, int n, int recipe) {
     for (int i = 0; i < n; ++i) {
         if (is_factored(t[i], recipe) && t[i].numel > 0) {
             L.n_factored++;
-            cp += n_slabs(t[i].rows) * (t[i].numel / t[i].rows);
+            cp += n_slabs(t[i].rows) * (t[i].numel / t[i].rows) + t[i].rows * n_segs(t[i].numel / t[i].rows);
         }
     }
     L.colpart_floats = cp;
@@ -309,7 +309,7 @@ int q4adamw_step(const q4adamw_tensor_t* t, int n, float lr, float beta1, float 
         if (f) {
             desc[i].rbar = reinterpret_cast<float*>(ws + L.rbar) + 2 * nf;
             desc[i].colpart = reinterpret_cast<float*>(ws + colpart_off);
-            colpart_off += n_slabs(desc[i].rows) * desc[i].cols * 4;
+            colpart_off += (n_slabs(desc[i].rows) * desc[i].cols + desc[i].rows * n_segs(desc[i].cols)) * 4;
             fids[nf++] = i;
         }
     }

@@ -3,18 +3,21 @@
 // column means of g^2 over the [shape[0], -1] view, kept as exponential
 // averages; 1-D tensors keep packed 4-bit v).
 //
-// Three passes, all multi-tensor and deterministic (fixed summation order, no
-// atomics):
-//   row_kernel     one warp per row: FP32 sum of g^2 along the row (each lane a
-//                  strided partial, then a warp tree), R_i <- beta2 R_i +
-//                  (1-beta2) * sum/cols.
-//   colpart_kernel one CTA per (tensor, 64-row slab, 2048-column segment): each
-//                  thread sums g^2 of 8 columns down the slab and writes the
-//                  slab's partial column sums.
-//   colfin_kernel  one thread per column: sums the slab partials in slab order,
-//                  C_j <- beta2 C_j + (1-beta2) * sum/rows.
-//   rbar_kernel    one CTA per factored tensor: mean(R) in a fixed tree order,
-//                  stored with its correctly rounded reciprocal.
+// Three launches, all multi-tensor and deterministic (fixed summation order,
+// no atomics):
+//   stats_kernel    one CTA (8 warps) per tile of 256 rows x 256 columns of a
+//                   tensor: g is read once, 16 bytes (8 BF16) per lane and row.
+//                   Each lane sums the 8 squares of its row chunk; a warp's 32
+//                   row chunks are reduced across lanes by a transpose tree
+//                   (lane l ends with row l's sum over the 256 columns), giving
+//                   row partials per 256-column segment.  Column sums over the
+//                   warp's 32 rows are combined over the 8 warps in warp order,
+//                   giving column partials per 256-row slab.
+//   finalize_kernel one thread per factored row or column: sums its partials in
+//                   segment (slab) order, mean = sum / cols (rows), and the
+//                   average R_i <- beta2 R_i + (1-beta2) mean (C_j likewise).
+//   rbar_kernel     one CTA per factored tensor: mean(R) in a fixed tree order,
+//                   stored with its correctly rounded reciprocal.
 // The step kernel then reads vhat_ij = R_i * C_j / mean(R).
 #include <cuda_runtime.h>
 
@@ -35,70 +38,112 @@ __device__ __forceinline__ int find_tensor(const int64_t* prefix, int n, int64_t
     return lo;
 }
 
-__device__ __forceinline__ float sq_bf16(uint16_t h) {
-    const float g = __uint_as_float((uint32_t)h << 16);
-    return __fmul_rn(g, g);
-}
-
 namespace {
 
-__global__ void __launch_bounds__(256) row_kernel(const __grid_constant__ FactoredParams P) {
-    const int lane = threadIdx.x & 31;
-    const int64_t gw = (int64_t)blockIdx.x * 8 + (threadIdx.x >> 5);
-    const int64_t W = (int64_t)gridDim.x * 8;
-    for (int64_t row = gw; row < P.total_rows; row += W) {
-        const int t = find_tensor(P.row_prefix, P.n_tensors, row);
-        const DevTensor& d = P.tensors[t];
-        const int64_t i = row - __ldg(P.row_prefix + t);
-        const uint16_t* g = d.grad + i * d.cols;
-        float acc = 0.f;
-        for (int64_t c = lane; c < d.cols; c += 32) acc = __fadd_rn(acc, sq_bf16(g[c]));
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) acc = __fadd_rn(acc, __shfl_xor_sync(0xffffffffu, acc, o));
-        if (lane == 0) {
-            const float mean = __fdiv_rn(acc, (float)d.cols);
-            d.vrow[i] = __fmaf_rn(P.beta2, d.vrow[i], __fmul_rn(P.omb2, mean));
-        }
-    }
-}
+constexpr int kStatsWarps = kSlabRows / 32;   // 8 warps, 32 rows each
 
-__global__ void __launch_bounds__(256) colpart_kernel(const __grid_constant__ FactoredParams P) {
+__device__ __forceinline__ float bf16f(uint32_t h) { return __uint_as_float(h << 16); }
+
+__global__ void __launch_bounds__(kStatsWarps * 32) stats_kernel(const __grid_constant__ FactoredParams P) {
+    __shared__ float colsum[kStatsWarps][kSegCols];
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     for (int64_t tile = blockIdx.x; tile < P.total_tiles; tile += gridDim.x) {
         const int t = find_tensor(P.tile_prefix, P.n_tensors, tile);
         const DevTensor& d = P.tensors[t];
         const int64_t local = tile - __ldg(P.tile_prefix + t);
-        const int64_t nseg = (d.cols + kSegCols - 1) / kSegCols;
+        const int64_t rows = d.rows, cols = d.cols;
+        const int64_t nseg = (cols + kSegCols - 1) / kSegCols;
         const int64_t slab = local / nseg, seg = local - slab * nseg;
-        const int64_t c0 = seg * kSegCols + (int64_t)threadIdx.x * 8;
-        const int64_t r0 = slab * kSlabRows;
-        const int64_t r1 = (r0 + kSlabRows < d.rows) ? r0 + kSlabRows : d.rows;
-        if (c0 >= d.cols) continue;
-        const int nc = (d.cols - c0 >= 8) ? 8 : (int)(d.cols - c0);
-        float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-        for (int64_t r = r0; r < r1; ++r) {
-            const uint16_t* g = d.grad + r * d.cols + c0;
+        const int64_t r0 = slab * kSlabRows + warp * 32;
+        const int64_t c0 = seg * kSegCols + lane * 8;
+        const int nc = c0 >= cols ? 0 : (cols - c0 >= 8 ? 8 : (int)(cols - c0));
+        const bool vec = nc == 8 && (cols & 7) == 0;
+        float col[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+        float rowp[32];
 #pragma unroll
-            for (int k = 0; k < 8; ++k)
-                if (k < nc) acc[k] = __fadd_rn(acc[k], sq_bf16(g[k]));
+        for (int i = 0; i < 32; ++i) {
+            const int64_t r = r0 + i;
+            float sq[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+            if (r < rows && nc > 0) {
+                const uint16_t* g = d.grad + r * cols + c0;
+                if (vec) {
+                    const uint4 w = __ldcs(reinterpret_cast<const uint4*>(g));
+                    const uint32_t h[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+                    for (int k = 0; k < 4; ++k) {
+                        const float lo = bf16f(h[k] & 0xffffu), hi = bf16f(h[k] >> 16);
+                        sq[2 * k] = __fmul_rn(lo, lo);
+                        sq[2 * k + 1] = __fmul_rn(hi, hi);
+                    }
+                } else {
+#pragma unroll
+                    for (int k = 0; k < 8; ++k) {
+                        if (k < nc) {
+                            const float x = bf16f(g[k]);
+                            sq[k] = __fmul_rn(x, x);
+                        }
+                    }
+                }
+            }
+#pragma unroll
+            for (int k = 0; k < 8; ++k) col[k] = __fadd_rn(col[k], sq[k]);
+            rowp[i] = __fadd_rn(__fadd_rn(__fadd_rn(sq[0], sq[1]), __fadd_rn(sq[2], sq[3])),
+                                __fadd_rn(__fadd_rn(sq[4], sq[5]), __fadd_rn(sq[6], sq[7])));
         }
-        float* out = d.colpart + slab * d.cols + c0;
+        // transpose reduction: afterwards rowp[0] of lane l is the sum over the
+        // 32 lanes of row l (a fixed tree)
 #pragma unroll
-        for (int k = 0; k < 8; ++k)
-            if (k < nc) out[k] = acc[k];
+        for (int o = 16; o >= 1; o >>= 1) {
+            const bool upper = (lane & o) != 0;
+#pragma unroll
+            for (int i = 0; i < o; ++i) {
+                const float send = upper ? rowp[i] : rowp[i + o];
+                const float keep = upper ? rowp[i + o] : rowp[i];
+                rowp[i] = __fadd_rn(keep, __shfl_xor_sync(0xffffffffu, send, o));
+            }
+        }
+        const int64_t nslab = (rows + kSlabRows - 1) / kSlabRows;
+        if (r0 + lane < rows) d.colpart[nslab * cols + (r0 + lane) * nseg + seg] = rowp[0];
+#pragma unroll
+        for (int k = 0; k < 8; ++k) colsum[warp][lane * 8 + k] = col[k];
+        __syncthreads();
+        {
+            const int c = threadIdx.x;                 // column within the segment
+            float s = colsum[0][c];
+#pragma unroll
+            for (int w = 1; w < kStatsWarps; ++w) s = __fadd_rn(s, colsum[w][c]);
+            const int64_t col_g = seg * kSegCols + c;
+            if (col_g < cols) d.colpart[slab * cols + col_g] = s;
+        }
+        __syncthreads();
     }
 }
 
-__global__ void __launch_bounds__(256) colfin_kernel(const __grid_constant__ FactoredParams P) {
-    for (int64_t col = (int64_t)blockIdx.x * 256 + threadIdx.x; col < P.total_cols;
-         col += (int64_t)gridDim.x * 256) {
-        const int t = find_tensor(P.col_prefix, P.n_tensors, col);
-        const DevTensor& d = P.tensors[t];
-        const int64_t j = col - __ldg(P.col_prefix + t);
-        const int64_t nslab = (d.rows + kSlabRows - 1) / kSlabRows;
-        float acc = 0.f;
-        for (int64_t s = 0; s < nslab; ++s) acc = __fadd_rn(acc, __ldg(d.colpart + s * d.cols + j));
-        const float mean = __fdiv_rn(acc, (float)d.rows);
-        d.vcol[j] = __fmaf_rn(P.beta2, d.vcol[j], __fmul_rn(P.omb2, mean));
+__global__ void __launch_bounds__(256) finalize_kernel(const __grid_constant__ FactoredParams P) {
+    const int64_t total = P.total_rows + P.total_cols;
+    for (int64_t idx = (int64_t)blockIdx.x * 256 + threadIdx.x; idx < total; idx += (int64_t)gridDim.x * 256) {
+        if (idx < P.total_rows) {
+            const int t = find_tensor(P.row_prefix, P.n_tensors, idx);
+            const DevTensor& d = P.tensors[t];
+            const int64_t i = idx - __ldg(P.row_prefix + t);
+            const int64_t nseg = (d.cols + kSegCols - 1) / kSegCols;
+            const int64_t nslab = (d.rows + kSlabRows - 1) / kSlabRows;
+            const float* p = d.colpart + nslab * d.cols + i * nseg;
+            float acc = __ldg(p);
+            for (int64_t q = 1; q < nseg; ++q) acc = __fadd_rn(acc, __ldg(p + q));
+            const float mean = __fdiv_rn(acc, (float)d.cols);
+            d.vrow[i] = __fmaf_rn(P.beta2, d.vrow[i], __fmul_rn(P.omb2, mean));
+        } else {
+            const int64_t cidx = idx - P.total_rows;
+            const int t = find_tensor(P.col_prefix, P.n_tensors, cidx);
+            const DevTensor& d = P.tensors[t];
+            const int64_t j = cidx - __ldg(P.col_prefix + t);
+            const int64_t nslab = (d.rows + kSlabRows - 1) / kSlabRows;
+            float acc = __ldg(d.colpart + j);
+            for (int64_t s = 1; s < nslab; ++s) acc = __fadd_rn(acc, __ldg(d.colpart + s * d.cols + j));
+            const float mean = __fdiv_rn(acc, (float)d.rows);
+            d.vcol[j] = __fmaf_rn(P.beta2, d.vcol[j], __fmul_rn(P.omb2, mean));
+        }
     }
 }
 
@@ -111,10 +156,10 @@ __global__ void __launch_bounds__(256) rbar_kernel(const __grid_constant__ Facto
     }
 }
 
-int grid_for(int64_t work, int per_cta) {
+int grid_for(int64_t work, int per_cta, int64_t cap) {
     int64_t g = (work + per_cta - 1) / per_cta;
     if (g < 1) g = 1;
-    if (g > 148 * 16) g = 148 * 16;
+    if (g > cap) g = cap;
     return (int)g;
 }
 
@@ -123,9 +168,8 @@ int grid_for(int64_t work, int per_cta) {
 int launch_factored(const FactoredParams& p, void* stream) {
     if (p.n_factored == 0) return 0;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    row_kernel<<<grid_for(p.total_rows, 8), 256, 0, s>>>(p);
-    colpart_kernel<<<grid_for(p.total_tiles, 1), 256, 0, s>>>(p);
-    colfin_kernel<<<grid_for(p.total_cols, 256), 256, 0, s>>>(p);
+    stats_kernel<<<grid_for(p.total_tiles, 1, 148 * 8), kStatsWarps * 32, 0, s>>>(p);
+    finalize_kernel<<<grid_for(p.total_rows + p.total_cols, 256, 148 * 16), 256, 0, s>>>(p);
     rbar_kernel<<<p.n_factored < 1024 ? p.n_factored : 1024, 256, 0, s>>>(p);
     return (int)cudaGetLastError();
 }

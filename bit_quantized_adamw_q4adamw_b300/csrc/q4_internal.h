@@ -36,7 +36,8 @@ struct DevTensor {
     uint32_t tensor_id;
     uint32_t flags;        // DF_* bits
     float* rbar;           // factored: {mean(R), RN(1/mean(R))} of this step
-    float* colpart;        // factored: column partial sums [n_slabs][cols]
+    float* colpart;        // factored: column partial sums [n_slabs][cols], then
+                           // row partial sums [rows][n_segs]
 };
 static_assert(sizeof(DevTensor) == 128, "descriptor must stay 128 bytes");
 
@@ -101,8 +102,8 @@ struct FactoredParams {
     float beta2, omb2;
 };
 
-constexpr int kSlabRows = 64;      // rows per column-partial slab
-constexpr int kSegCols = 2048;     // columns per column tile (256 threads x 8)
+constexpr int kSlabRows = 256;     // rows per column-partial slab (8 warps x 32 rows)
+constexpr int kSegCols = 256;      // columns per row-partial segment (32 lanes x 8)
 
 // Records a cudaError_t for q4adamw_last_cuda_error() and returns Q4_ECUDA.
 int record_cuda_error(int cuda_error);
