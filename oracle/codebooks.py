@@ -24,6 +24,14 @@ Readings (the pages are silent on the level values):
     and decodes to 10^-e * (0.1 + 0.9 * (j + 1) / 2^f), j < 2^f; the
     all-zero code is 0.  Dyn4-NZ maps the all-zero code to the next
     exponent rung, 10^-4, so no level is zero.
+  * SDyn4 (TorchAO baseline's first moment, listing page Table 2) is the
+    signed 4-bit dynamic-exponent map as the dynamic quantisation of
+    Dettmers et al. defines it for 4 bits with 3 exponent rungs: on rung
+    i = 0, 1, 2 the interval [0.1, 1] is cut into 2^i equal parts whose
+    midpoints, scaled by 10^(i-2), are the magnitudes (7 in all); both
+    signs of each, plus 0 and +1, give 16 levels.
+  * Lin4-NZ (TorchAO baseline's second moment, Table 2) is the linear
+    zero-excluding map k/16, k = 1..16.
   * Codes index the levels sorted ascending.  RTN thresholds are the FP32
     rounding of the double midpoint of adjacent FP32 levels.
 """
@@ -52,6 +60,22 @@ def dyn4_levels(zero_excluding: bool = False) -> np.ndarray:
     return np.array(sorted(vals), dtype=np.float64).astype(np.float32)
 
 
+def sdyn4_levels() -> np.ndarray:
+    mags = []
+    for i in range(3):
+        parts = 2 ** i
+        for j in range(parts):
+            lo = 0.1 + 0.9 * j / parts
+            hi = 0.1 + 0.9 * (j + 1) / parts
+            mags.append(10.0 ** (i - 2) * (lo + hi) / 2.0)
+    vals = sorted([m for m in mags] + [-m for m in mags] + [0.0, 1.0])
+    return np.array(vals, dtype=np.float64).astype(np.float32)
+
+
+def lin4nz_levels() -> np.ndarray:
+    return np.array([k / 16.0 for k in range(1, 17)], dtype=np.float64).astype(np.float32)
+
+
 def midpoints(levels: np.ndarray) -> np.ndarray:
     lv = levels.astype(np.float64)
     return ((lv[:-1] + lv[1:]) / 2.0).astype(np.float32)
@@ -61,8 +85,12 @@ def all_codebooks() -> dict:
     nf4 = nf4_levels()
     d4 = dyn4_levels(False)
     d4nz = dyn4_levels(True)
+    sd4 = sdyn4_levels()
+    l4 = lin4nz_levels()
     return {
         "nf4": nf4, "nf4_t": midpoints(nf4),
         "dyn4": d4, "dyn4_t": midpoints(d4),
         "dyn4nz": d4nz, "dyn4nz_t": midpoints(d4nz),
+        "sdyn4": sd4, "sdyn4_t": midpoints(sd4),
+        "lin4nz": l4, "lin4nz_t": midpoints(l4),
     }

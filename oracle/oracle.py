@@ -48,10 +48,12 @@ BUILD_DIR = os.path.join(HERE, "_build")
 LIB_PATH = os.path.join(BUILD_DIR, "liboracle.so")
 
 BLOCK = 128
-RECIPES = {"zip_sr": 0, "ze_eden": 1, "factored": 2}
+RECIPES = {"zip_sr": 0, "ze_eden": 1, "factored": 2, "torchao": 3}
 T_LM_HEAD = 1
 T_FACTORED = 2
 LM_HEAD_SR_ACTIVE = 1
+M_SR_ALL = 2          # State-SR for the first moment of every tensor (ablation)
+V_UPDATE_RTN = 4      # Update-RTN instead of Update-SR under ZIP-SR (ablation)
 PURPOSE_M_SR = 0
 PURPOSE_V_SR = 1
 RULES = {"state_rtn": 0, "state_sr": 1, "update_rtn": 2, "update_sr": 3}
@@ -88,6 +90,8 @@ class _Codebooks(ctypes.Structure):
         ("nf4", ctypes.c_float * 16), ("nf4_t", ctypes.c_float * 15),
         ("dyn4", ctypes.c_float * 16), ("dyn4_t", ctypes.c_float * 15),
         ("dyn4nz", ctypes.c_float * 16), ("dyn4nz_t", ctypes.c_float * 15),
+        ("sdyn4", ctypes.c_float * 16), ("sdyn4_t", ctypes.c_float * 15),
+        ("lin4nz", ctypes.c_float * 16), ("lin4nz_t", ctypes.c_float * 15),
     ]
 
 
@@ -130,7 +134,7 @@ def codebooks() -> dict:
 def _cb_struct() -> _Codebooks:
     c = codebooks()
     s = _Codebooks()
-    for name in ("nf4", "nf4_t", "dyn4", "dyn4_t", "dyn4nz", "dyn4nz_t"):
+    for name in ("nf4", "nf4_t", "dyn4", "dyn4_t", "dyn4nz", "dyn4nz_t", "sdyn4", "sdyn4_t", "lin4nz", "lin4nz_t"):
         getattr(s, name)[:] = [float(x) for x in c[name]]
     return s
 
@@ -276,8 +280,9 @@ class OracleTensor:
         if rc != 0:
             raise ValueError(f"oracle_step_tensor failed: {rc}")
 
-    def m_dequant(self) -> np.ndarray:
-        return dequant(codebooks()["nf4"], self.m_codes, self.m_scale, self.param.size)
+    def m_dequant(self, recipe: str = "zip_sr") -> np.ndarray:
+        L = codebooks()["sdyn4" if recipe == "torchao" else "nf4"]
+        return dequant(L, self.m_codes, self.m_scale, self.param.size)
 
     def v_dequant(self, recipe: str) -> np.ndarray:
         if self.factored:
@@ -286,5 +291,5 @@ class OracleTensor:
             if rbar == 0:
                 return np.zeros(self.param.size, np.float32)
             return ((self.v_row[:, None] * self.v_col[None, :]) / rbar).astype(np.float32).reshape(-1)
-        L = codebooks()["dyn4" if recipe == "zip_sr" else "dyn4nz"]
+        L = codebooks()["dyn4" if recipe == "zip_sr" else "lin4nz" if recipe == "torchao" else "dyn4nz"]
         return dequant(L, self.v_codes, self.v_scale, self.param.size)

@@ -34,9 +34,13 @@
 
 #define OB 128 /* block size: AReno docs "4-bit AdamW", State representation */
 
-enum { OR_ZIP_SR = 0, OR_ZE_EDEN = 1, OR_FACTORED = 2 };
+enum { OR_ZIP_SR = 0, OR_ZE_EDEN = 1, OR_FACTORED = 2, OR_TORCHAO = 3 };
 enum { OT_LM_HEAD = 1u, OT_FACTORED = 2u };
-enum { OS_LM_HEAD_SR_ACTIVE = 1u };
+/* Per-call flags: the LM-head SR phase (Table 2 note) and two rounding
+ * variants of the listing page's ablations: State-SR for the first moment of
+ * every tensor, and Update-RTN in place of Update-SR under ZIP-SR (Table 1
+ * rules). */
+enum { OS_LM_HEAD_SR_ACTIVE = 1u, OS_M_SR_ALL = 2u, OS_V_UPDATE_RTN = 4u };
 enum { OP_M_SR = 0u, OP_V_SR = 1u };
 
 /* ------------------------------------------------------------------ */
@@ -363,6 +367,8 @@ typedef struct {
     float nf4[16], nf4_t[15];
     float dyn4[16], dyn4_t[15];
     float dyn4nz[16], dyn4nz_t[15];
+    float sdyn4[16], sdyn4_t[15];
+    float lin4nz[16], lin4nz_t[15];
 } oracle_codebooks;
 
 int oracle_step_tensor(const oracle_codebooks* cb, const oracle_tensor* T, float lr, float beta1, float beta2,
@@ -370,7 +376,11 @@ int oracle_step_tensor(const oracle_codebooks* cb, const oracle_tensor* T, float
     if (step < 1 || T->numel < 0) return -1;
     scal_t s = make_scalars(lr, beta1, beta2, eps, wd, step);
     const int factored = (recipe == OR_FACTORED) && (T->flags & OT_FACTORED);
-    const int m_sr = (T->flags & OT_LM_HEAD) && (call_flags & OS_LM_HEAD_SR_ACTIVE);
+    /* Listing page Table 2: the LM-head first moment switches to SR in the
+     * final phase under ZIP-SR and ZE-EDEN; the TorchAO baseline keeps RTN. */
+    const int m_sr = ((T->flags & OT_LM_HEAD) && (call_flags & OS_LM_HEAD_SR_ACTIVE) && recipe != OR_TORCHAO) ||
+                     (call_flags & OS_M_SR_ALL);
+    const int v_update_rtn = (recipe == OR_ZIP_SR) && (call_flags & OS_V_UPDATE_RTN);
     int64_t cols = 0;
     float rbar = 0.0f;
     if (factored) {
@@ -378,8 +388,12 @@ int oracle_step_tensor(const oracle_codebooks* cb, const oracle_tensor* T, float
         cols = T->numel / T->rows;
         factored_update(&s, T->grad, T->rows, cols, T->v_row, T->v_col, &rbar);
     }
-    const float* Lv = (recipe == OR_ZIP_SR) ? cb->dyn4 : cb->dyn4nz;
-    const float* tv = (recipe == OR_ZIP_SR) ? cb->dyn4_t : cb->dyn4nz_t;
+    /* Listing page Table 2: ZIP-SR v in Dyn4, ZE-EDEN v in Dyn4-NZ, TorchAO
+     * v in Lin4-NZ and m in SDyn4; AReno docs: factored 1-D v excludes zero. */
+    const float* Lv = (recipe == OR_ZIP_SR) ? cb->dyn4 : (recipe == OR_TORCHAO) ? cb->lin4nz : cb->dyn4nz;
+    const float* tv = (recipe == OR_ZIP_SR) ? cb->dyn4_t : (recipe == OR_TORCHAO) ? cb->lin4nz_t : cb->dyn4nz_t;
+    const float* Lm = (recipe == OR_TORCHAO) ? cb->sdyn4 : cb->nf4;
+    const float* tm = (recipe == OR_TORCHAO) ? cb->sdyn4_t : cb->nf4_t;
 
     int64_t nblocks = (T->numel + OB - 1) / OB;
     for (int64_t b = 0; b < nblocks; ++b) {
@@ -392,7 +406,7 @@ int oracle_step_tensor(const oracle_codebooks* cb, const oracle_tensor* T, float
         for (int i = 0; i < n; ++i) {
             int64_t e = e0 + i;
             float g = bf16_to_f32(T->grad[e]);
-            float m = cb->nf4[code_at(T->m_codes, e)] * sm_old;
+            float m = Lm[code_at(T->m_codes, e)] * sm_old;
             float mm = fmaf(s.beta1, m, s.omb1 * g);
             float vv;
             if (factored) {
@@ -417,7 +431,7 @@ int oracle_step_tensor(const oracle_codebooks* cb, const oracle_tensor* T, float
         memset(qv, 0, sizeof qv);
         float sm = block_absmax(m1, n);
         float am[16], Tm[15];
-        scale_tables(cb->nf4, cb->nf4_t, sm, am, Tm);
+        scale_tables(Lm, tm, sm, am, Tm);
         for (int i = 0; i < n; ++i) {
             if (m_sr) {
                 uint32_t w = oracle_draw(seed, (uint32_t)step, T->tensor_id, T->elem_offset + (uint64_t)(e0 + i), OP_M_SR);
@@ -433,7 +447,9 @@ int oracle_step_tensor(const oracle_codebooks* cb, const oracle_tensor* T, float
         float sv = block_absmax(v1, n);
         float av[16], Tv[15];
         scale_tables(Lv, tv, sv, av, Tv);
-        if (recipe == OR_ZIP_SR) {
+        if (recipe == OR_ZIP_SR && v_update_rtn) {
+            for (int i = 0; i < n; ++i) qv[i] = (uint8_t)rule_update_rtn(av, v1[i], r[i], &s);
+        } else if (recipe == OR_ZIP_SR) {
             for (int i = 0; i < n; ++i) {
                 uint32_t w = oracle_draw(seed, (uint32_t)step, T->tensor_id, T->elem_offset + (uint64_t)(e0 + i), OP_V_SR);
                 qv[i] = (uint8_t)rule_update_sr(av, v1[i], r[i], oracle_uniform(w), &s);

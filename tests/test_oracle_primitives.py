@@ -130,9 +130,33 @@ def test_dyn4_exact_rationals(nz):
         assert lv[0] == 0.0
 
 
+def test_sdyn4_exact_rationals():
+    # signed dynamic-exponent map: rung i = 0..2 splits [1/10, 1] into 2^i equal
+    # parts; their midpoints times 10^(i-2), with both signs, plus 0 and +1
+    lv = O.codebooks()["sdyn4"]
+    mags = []
+    for i in range(3):
+        for j in range(2 ** i):
+            mid = Fraction(1, 10) + Fraction(9 * (2 * j + 1), 20 * 2 ** i)
+            mags.append(mid * Fraction(10) ** (i - 2))
+    exact = sorted(mags + [-m for m in mags] + [Fraction(0), Fraction(1)])
+    assert len(exact) == 16
+    for x, q in zip(lv, exact):
+        assert x == _nearest_f32(q), (x, q)
+    assert np.all(np.diff(lv) > 0) and lv[-1] == 1.0 and 0.0 in lv
+    # symmetric except the top level
+    assert sorted((-lv[lv != 1.0]).tolist()) == sorted(lv[lv != 1.0].tolist())
+
+
+def test_lin4nz_exact_rationals():
+    lv = O.codebooks()["lin4nz"]
+    assert [Fraction(float(x)) for x in lv] == [Fraction(k, 16) for k in range(1, 17)]
+    assert lv.min() > 0
+
+
 def test_thresholds_are_rounded_midpoints():
     cb = O.codebooks()
-    for name in ("nf4", "dyn4", "dyn4nz"):
+    for name in ("nf4", "dyn4", "dyn4nz", "sdyn4", "lin4nz"):
         L, t = cb[name], cb[name + "_t"]
         assert t.size == 15
         for k in range(15):

@@ -121,14 +121,14 @@ def test_update_sr_is_unbiased_in_r_and_state_sr_in_v():
     assert np.all(np.abs(mv - x) <= 4.5 * sv + 1e-6 * x)
 
 
-@pytest.mark.parametrize("name", ["nf4", "dyn4", "dyn4nz"])
+@pytest.mark.parametrize("name", ["nf4", "dyn4", "dyn4nz", "sdyn4", "lin4nz"])
 def test_rtn_is_brute_force_nearest_level(name):
     rng = np.random.default_rng(1)
     L, t = O.codebooks()[name], O.codebooks()[name + "_t"]
     for trial in range(200):
         n = int(rng.integers(1, 129))
         x = rng.normal(0, 1, n).astype(np.float32) * np.float32(10.0 ** rng.uniform(-20, 20))
-        if name != "nf4":
+        if name not in ("nf4", "sdyn4"):
             x = np.abs(x)
         c, s = O.quant_block(L, t, x, "state_rtn")
         assert s == np.abs(x).max()
@@ -142,7 +142,7 @@ def test_rtn_is_brute_force_nearest_level(name):
 
 def test_rtn_identity_on_levels():
     # quant o dequant is the identity on codebook levels (power-of-two scale: exact products)
-    for name in ("nf4", "dyn4", "dyn4nz"):
+    for name in ("nf4", "dyn4", "dyn4nz", "sdyn4", "lin4nz"):
         L, t = O.codebooks()[name], O.codebooks()[name + "_t"]
         for s in (1.0, 2.0 ** -20, 2.0 ** 30):
             x = (L * np.float32(s)).astype(np.float32)
@@ -153,7 +153,7 @@ def test_rtn_identity_on_levels():
             for rule in ("state_sr", "update_sr"):
                 w = O.draws(1, 1, 0, 0, 16, 1)
                 c2, _ = O.quant_block(L, t, x, rule, words=w, c2=1.0, eps=1e-8)
-                if name != "nf4" or rule == "state_sr":
+                if name not in ("nf4", "sdyn4") or rule == "state_sr":
                     assert np.array_equal(c2, np.arange(16)), (name, rule)
 
 

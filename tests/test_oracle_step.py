@@ -75,7 +75,7 @@ def _one_tensor_steps(recipe, numel, steps, grads_fn, rows=1, flags=0, call_flag
     return theta0, t
 
 
-@pytest.mark.parametrize("recipe", ["zip_sr", "ze_eden"])
+@pytest.mark.parametrize("recipe", ["zip_sr", "ze_eden", "torchao"])
 def test_first_step_update_is_textbook_adamw(recipe):
     # From the zero state the first update uses exact moments, so theta after
     # step 1 equals torch.optim.AdamW's first step.
@@ -228,3 +228,102 @@ def test_partial_block_padding_codes_are_zero():
     codes_m = np.stack([t.m_codes & 15, t.m_codes >> 4], 1).reshape(-1)
     codes_v = np.stack([t.v_codes & 15, t.v_codes >> 4], 1).reshape(-1)
     assert np.all(codes_m[n:] == 0) and np.all(codes_v[n:] == 0)
+
+
+def _codes(packed, n):
+    return np.array([(packed[e >> 1] >> (4 * (e & 1))) & 15 for e in range(n)])
+
+
+def test_torchao_first_step_state_is_nearest_sdyn4_and_lin4nz_level():
+    # TorchAO baseline (listing page Table 2): m in SDyn4 and v in Lin4-NZ, both
+    # State-RTN at scale max|x| per block; after step 1 the moments are
+    # (1-b1) g and (1-b2) g^2 (float64 restatement).
+    rng = np.random.default_rng(18)
+    n = 700
+    g = _bf16(rng.normal(0, 1e-3, n))
+    gf = _from_bf16(g).astype(np.float64)
+    _, t = _one_tensor_steps("torchao", n, 1, lambda k: g)
+    h = O.host_scalars(H["lr"], H["beta1"], H["beta2"], H["wd"], 1)
+    m1 = np.float32(h["omb1"]) * gf
+    v1 = np.float32(h["omb2"]) * gf * gf
+    cb = O.codebooks()
+    qm, qv = _codes(t.m_codes, n), _codes(t.v_codes, n)
+    for b in range(O.nblocks(n)):
+        sl = slice(128 * b, min(128 * b + 128, n))
+        sm, sv = np.abs(m1[sl]).max(), v1[sl].max()
+        assert abs(t.m_scale[b] - sm) <= 1e-6 * sm and abs(t.v_scale[b] - sv) <= 1e-6 * sv
+        dm = np.abs(m1[sl][:, None] - cb["sdyn4"][None, :].astype(np.float64) * sm)
+        assert np.all(dm[np.arange(dm.shape[0]), qm[sl]] <= dm.min(1) + 1e-6 * sm)
+        dv = np.abs(v1[sl][:, None] - cb["lin4nz"][None, :].astype(np.float64) * sv)
+        assert np.all(dv[np.arange(dv.shape[0]), qv[sl]] <= dv.min(1) + 1e-6 * sv)
+
+
+def test_torchao_lm_head_stays_rtn_in_the_final_phase():
+    # Table 2: the TorchAO baseline uses SDyn4-RTN for the LM head too.
+    rng = np.random.default_rng(19)
+    n = 512
+    th = rng.normal(0, 0.02, n).astype(np.float32)
+    a = O.OracleTensor.zeros_state(th, 3, flags=O.T_LM_HEAD, recipe="torchao")
+    b = O.OracleTensor.zeros_state(th, 3, flags=0, recipe="torchao")
+    for step in range(1, 4):
+        g = _bf16(rng.normal(0, 1e-3, n))
+        a.step(g, H["lr"], H["beta1"], H["beta2"], H["eps"], H["wd"], step, 5, "torchao", O.LM_HEAD_SR_ACTIVE)
+        b.step(g, H["lr"], H["beta1"], H["beta2"], H["eps"], H["wd"], step, 5, "torchao", 0)
+    assert np.array_equal(a.m_codes, b.m_codes) and np.array_equal(a.param, b.param)
+
+
+def test_m_sr_all_is_unbiased_over_seeds():
+    # Ablation flag M_SR_ALL: every tensor's m takes State-SR.  Over seeds the
+    # dequantised first moment averages to m' = (1-b1) g (step 1, float64),
+    # and every code is one of the two levels around m'.
+    rng = np.random.default_rng(20)
+    n = 128
+    g = _bf16(rng.normal(0, 1e-3, n))
+    m1 = np.float32(O.host_scalars(H["lr"], H["beta1"], H["beta2"], H["wd"], 1)["omb1"]) * \
+        _from_bf16(g).astype(np.float64)
+    th = rng.normal(0, 0.02, n).astype(np.float32)
+    acc = np.zeros(n)
+    seeds = 600
+    L = O.codebooks()["nf4"].astype(np.float64)
+    for seed in range(seeds):
+        t = O.OracleTensor.zeros_state(th, 0, recipe="zip_sr")
+        t.step(g, H["lr"], H["beta1"], H["beta2"], H["eps"], H["wd"], 1, seed, "zip_sr", O.M_SR_ALL)
+        q = _codes(t.m_codes, n)
+        s = float(t.m_scale[0])
+        cell = np.searchsorted(L * s, m1, side="right") - 1
+        assert np.all((q == cell) | (q == np.minimum(cell + 1, 15)))
+        acc += L[q] * s
+    mean = acc / seeds
+    gap = np.diff(L)[np.clip(np.searchsorted(L * s, m1, side="right") - 1, 0, 14)] * s
+    assert np.all(np.abs(mean - m1) <= 4.5 * gap / 2 / np.sqrt(seeds) + 1e-6 * s)
+
+
+def test_v_update_rtn_takes_the_level_nearer_in_preconditioner_space():
+    # Ablation flag V_UPDATE_RTN under ZIP-SR: of the two Dyn4 levels around v',
+    # the stored one has the preconditioner nearer to r(v') (listing page
+    # Table 1, Update-RTN), checked in float64 up to FP32 rounding.
+    rng = np.random.default_rng(21)
+    n = 640
+    g = _bf16(rng.normal(0, 1e-3, n) * np.exp(rng.uniform(-6, 2, n)))
+    gf = _from_bf16(g).astype(np.float64)
+    th = rng.normal(0, 0.02, n).astype(np.float32)
+    t = O.OracleTensor.zeros_state(th, 0, recipe="zip_sr")
+    t.step(g, H["lr"], H["beta1"], H["beta2"], H["eps"], H["wd"], 1, 0, "zip_sr", O.V_UPDATE_RTN)
+    h = O.host_scalars(H["lr"], H["beta1"], H["beta2"], H["wd"], 1)
+    v1 = np.float32(h["omb2"]) * gf * gf
+    c2, eps = float(h["c2"]), float(np.float32(H["eps"]))
+    rf = lambda v: 1.0 / (np.sqrt(v) * c2 + eps)
+    L = O.codebooks()["dyn4"].astype(np.float64)
+    q = _codes(t.v_codes, n)
+    for b in range(O.nblocks(n)):
+        sl = slice(128 * b, 128 * b + 128)
+        s = v1[sl].max()
+        a = L * s
+        k = np.clip(np.searchsorted(a, v1[sl], side="right") - 1, 0, 15)
+        k1 = np.minimum(k + 1, 15)
+        r = rf(v1[sl])
+        d_lo, d_hi = np.abs(rf(a[k]) - r), np.abs(rf(a[k1]) - r)
+        got = q[sl]
+        assert np.all((got == k) | (got == k1))
+        chosen = np.where(got == k, d_lo, d_hi)
+        assert np.all(chosen <= np.minimum(d_lo, d_hi) * (1 + 1e-5) + 1e-7 * r)
