@@ -16,14 +16,15 @@ import numpy as np
 import torch
 
 from . import _native
-from ._native import (BLOCK, Q4_LM_HEAD_SR_ACTIVE, Q4_T_FACTORED, Q4_T_LM_HEAD, RECIPES, Q4Error, Q4Header,
+from ._native import (BLOCK, Q4_LM_HEAD_SR_ACTIVE, Q4_M_SR_ALL, Q4_T_FACTORED, Q4_T_LM_HEAD, Q4_V_UPDATE_RTN,
+                      RECIPES, Q4Error, Q4Header,
                       Q4Tensor, lib)
 
 __all__ = ["q4adamw_version", "q4adamw_strerror", "q4adamw_state_bytes", "q4adamw_workspace_bytes",
            "q4adamw_state_init", "q4adamw_header_check", "q4adamw_step", "q4adamw_step_noalloc",
            "q4adamw_dequant_state", "q4adamw_step_status",
            "q4adamw_codebook", "Q4State", "Q4Tensor", "Q4Header", "Q4Error", "RECIPES", "Q4_T_LM_HEAD",
-           "Q4_T_FACTORED", "Q4_LM_HEAD_SR_ACTIVE", "BLOCK"]
+           "Q4_T_FACTORED", "Q4_LM_HEAD_SR_ACTIVE", "Q4_M_SR_ALL", "Q4_V_UPDATE_RTN", "BLOCK"]
 
 
 def _recipe(r) -> int:

@@ -21,10 +21,12 @@ Q4_EVERSION = -5
 Q4_ECUDA = -6
 Q4_EWORKSPACE = -7
 
-RECIPES = {"zip_sr": 0, "ze_eden": 1, "factored": 2}
+RECIPES = {"zip_sr": 0, "ze_eden": 1, "factored": 2, "torchao": 3}
 Q4_T_LM_HEAD = 0x1
 Q4_T_FACTORED = 0x2
 Q4_LM_HEAD_SR_ACTIVE = 0x1
+Q4_M_SR_ALL = 0x2
+Q4_V_UPDATE_RTN = 0x4
 Q4_STATUS_STAGE_TIMEOUT = 0x1
 BLOCK = 128
 NOALLOC_SCRATCH_BYTES = 4 * 1024 * 1024

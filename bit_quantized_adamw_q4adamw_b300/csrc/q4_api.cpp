@@ -30,9 +30,16 @@ bool is_factored(const q4adamw_tensor_t& t, int recipe) {
 }
 
 int check_recipe(int recipe) {
-    return (recipe == Q4_RECIPE_ZIP_SR || recipe == Q4_RECIPE_ZE_EDEN || recipe == Q4_RECIPE_FACTORED)
+    return (recipe == Q4_RECIPE_ZIP_SR || recipe == Q4_RECIPE_ZE_EDEN || recipe == Q4_RECIPE_FACTORED ||
+            recipe == Q4_RECIPE_TORCHAO)
                ? Q4_OK
                : Q4_ERECIPE;
+}
+
+// Codebook ids of a recipe's moments (listing page Table 2).
+int m_book(int recipe) { return recipe == Q4_RECIPE_TORCHAO ? 3 : 0; }
+int v_book(int recipe) {
+    return recipe == Q4_RECIPE_ZIP_SR ? 1 : recipe == Q4_RECIPE_TORCHAO ? 4 : 2;
 }
 
 // Shape-only checks (host-only entry points).
@@ -124,21 +131,21 @@ Scalars host_scalars(float lr, float beta1, float beta2, float wd, int64_t step)
     return s;
 }
 
-q4::Tables* g_tabs[3] = {nullptr, nullptr, nullptr};
+q4::Tables* g_tabs[4] = {nullptr, nullptr, nullptr, nullptr};
 std::once_flag g_tabs_once;
 
 void build_all_tables() {
-    for (int vb = 1; vb <= 2; ++vb) {
+    for (int r = 0; r < 4; ++r) {
         q4::Tables* t = new (std::nothrow) q4::Tables;
-        if (t && q4::build_tables(vb, t)) g_tabs[vb] = t;
+        if (t && q4::build_tables(m_book(r), v_book(r), t)) g_tabs[r] = t;
         else delete t;
     }
 }
 
-// One immutable table set per v codebook (1 = Dyn4, 2 = Dyn4-NZ), built once.
+// One immutable table set per recipe, built once.
 q4::Tables* tables_for(int recipe) {
     std::call_once(g_tabs_once, build_all_tables);
-    return g_tabs[recipe == Q4_RECIPE_ZIP_SR ? 1 : 2];
+    return g_tabs[recipe];
 }
 
 DevTensor make_dev(const q4adamw_tensor_t& t, int recipe, uint32_t call_flags) {
@@ -158,7 +165,11 @@ DevTensor make_dev(const q4adamw_tensor_t& t, int recipe, uint32_t call_flags) {
     d.elem_offset = t.elem_offset;
     d.tensor_id = t.tensor_id;
     d.flags = 0;
-    if ((t.flags & Q4_T_LM_HEAD) && (call_flags & Q4_LM_HEAD_SR_ACTIVE)) d.flags |= q4::DF_M_SR;
+    // listing page Table 2: LM-head SR in the final phase, except in the TorchAO
+    // baseline; the Q4_M_SR_ALL variant rounds every first moment stochastically
+    if (((t.flags & Q4_T_LM_HEAD) && (call_flags & Q4_LM_HEAD_SR_ACTIVE) && recipe != Q4_RECIPE_TORCHAO) ||
+        (call_flags & Q4_M_SR_ALL))
+        d.flags |= q4::DF_M_SR;
     if (is_factored(t, recipe)) {
         d.flags |= q4::DF_FACTORED;
         if (d.cols % 8 == 0 && aligned(t.v_col, 16)) d.flags |= q4::DF_CVEC;
@@ -275,6 +286,8 @@ int q4adamw_step(const q4adamw_tensor_t* t, int n, float lr, float beta1, float 
     if (n < 0 || (n > 0 && !t)) return Q4_EINVAL;
     if (int rc = check_recipe(recipe)) return rc;
     if (step < 1 || step > 0xFFFFFFFFll) return Q4_EINVAL;
+    if (flags & ~(Q4_LM_HEAD_SR_ACTIVE | Q4_M_SR_ALL | Q4_V_UPDATE_RTN)) return Q4_EINVAL;
+    if ((flags & Q4_V_UPDATE_RTN) && recipe != Q4_RECIPE_ZIP_SR) return Q4_EINVAL;
     if (!(beta1 >= 0.f && beta1 < 1.f) || !(beta2 >= 0.f && beta2 < 1.f)) return Q4_EINVAL;
     if (!(eps > 0.f) || !std::isfinite(eps) || !std::isfinite(lr) || !std::isfinite(weight_decay)) return Q4_EINVAL;
     for (int i = 0; i < n; ++i)
@@ -357,6 +370,7 @@ int q4adamw_step(const q4adamw_tensor_t* t, int n, float lr, float beta1, float 
     // [2^-126, 2^126); with v' <= FLT_MAX and c2 <= 2^12 (beta2 < 1 in FP32)
     // that holds whenever eps lies in [2^-100, 2^60].
     p.fast_math = (eps >= 0x1p-100f && eps <= 0x1p60f) ? 1 : 0;
+    p.v_update_rtn = (flags & Q4_V_UPDATE_RTN) ? 1 : 0;
     p.x2_beta1 = make_float2(p.beta1, p.beta1);
     p.x2_beta2 = make_float2(p.beta2, p.beta2);
     p.x2_omb1 = make_float2(p.omb1, p.omb1);
@@ -397,15 +411,15 @@ int q4adamw_dequant_state(const q4adamw_tensor_t* t, int recipe, float* m_out, f
     if (int rc = check_tensor(*t, recipe, false)) return rc;
     if (t->numel == 0 || (!m_out && !v_out)) return Q4_OK;
     const DevTensor d = make_dev(*t, recipe, 0);
-    const q4::Codebook& nf4 = q4::codebook(0);
-    const q4::Codebook& vb = q4::codebook(recipe == Q4_RECIPE_ZIP_SR ? 1 : 2);
+    const q4::Codebook& nf4 = q4::codebook(m_book(recipe));
+    const q4::Codebook& vb = q4::codebook(v_book(recipe));
     if (int ce = q4::launch_dequant(d, recipe, nf4.levels, vb.levels, m_out, v_out, stream))
         return cuda_fail((cudaError_t)ce);
     return Q4_OK;
 }
 
 int q4adamw_codebook(int which, float* levels, float* thresholds) {
-    if (which < 0 || which > 2) return Q4_ERECIPE;
+    if (which < 0 || which > 4) return Q4_ERECIPE;
     const q4::Codebook& c = q4::codebook(which);
     if (levels) std::memcpy(levels, c.levels, sizeof c.levels);
     if (thresholds) std::memcpy(thresholds, c.thresholds, sizeof c.thresholds);

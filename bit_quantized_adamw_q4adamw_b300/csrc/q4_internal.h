@@ -53,8 +53,8 @@ enum : uint32_t { ST_STAGE_TIMEOUT = 1u };
 
 // Codebooks and candidate tables (built on the host by q4_tables.cpp).
 struct Tables {
-    float nf4[16];      // NF4 levels, ascending
-    float nf4_t[16];    // NF4 RTN thresholds (index 15 unused)
+    float nf4[16];      // m levels, ascending (NF4; SDyn4 for the TorchAO recipe)
+    float nf4_t[16];    // m RTN thresholds (index 15 unused)
     float vl[16];       // v levels for this launch (Dyn4 or Dyn4-NZ)
     float vt[16];       // v RTN thresholds (index 15 unused)
     uint8_t lut_nf4_t[64];   // NF4 threshold candidate by linear bucket
@@ -62,17 +62,19 @@ struct Tables {
     uint8_t lut_v_l[kVLut];  // v level (cell) candidate by log bucket
     uint8_t lut_v_t[kVLut];  // v threshold candidate by log bucket
     float2 nf4_bucket[64];   // NF4 RTN by linear bucket: {threshold of the candidate, candidate}
+    int m_lut;               // 1 when the linear-bucket tables are valid for the m codebook
 };
 
-// Host-side tables: 0 = NF4, 1 = Dyn4, 2 = Dyn4-NZ.
+// Host-side tables: 0 = NF4, 1 = Dyn4, 2 = Dyn4-NZ, 3 = SDyn4, 4 = Lin4-NZ.
 struct Codebook {
     float levels[16];
     float thresholds[15];
 };
 const Codebook& codebook(int which);
-// Fills t for the v codebook `vbook` (1 or 2).  Returns false if a candidate
-// table cannot be built (never for the shipped codebooks).
-bool build_tables(int vbook, Tables* t);
+// Fills t for the m codebook `mbook` (0 or 3) and the v codebook `vbook`
+// (1, 2 or 4).  Returns false if a v candidate table cannot be built (never
+// for the shipped codebooks).
+bool build_tables(int mbook, int vbook, Tables* t);
 
 struct StepParams {
     const DevTensor* tensors;
@@ -84,6 +86,7 @@ struct StepParams {
     float beta1, beta2, omb1, omb2, c2, eps, decay, step_size;
     uint32_t step;
     int fast_math;                // eps and c2 keep 1/(sqrt(v) c2 + eps) in the fast domain
+    int v_update_rtn;             // ZIP-SR with Update-RTN in place of Update-SR
     // the step scalars broadcast to pairs, for the paired FP32 instructions
     float2 x2_beta1, x2_beta2, x2_omb1, x2_omb2, x2_c2, x2_eps, x2_decay, x2_neg_step;
     uint32_t round_keys[20];      // Philox key schedule: (k0, k1) for rounds 0..9

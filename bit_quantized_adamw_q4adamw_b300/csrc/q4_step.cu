@@ -335,7 +335,7 @@ __device__ __forceinline__ uint32_t pack8(const uint32_t c[8]) {
 // numel already zeroed), the new scales s_m, s_v and r (ZIP-SR).  Handles
 // every case: partial blocks, LM-head stochastic rounding, scales outside the
 // fast range (exact sequential searches).
-template <int RECIPE>
+template <int RECIPE, bool URTN>
 __device__ __forceinline__ void requant_general(const StepParams& P, const DevTensor& d, const SmemAll& sm,
                                                 WarpTables& wt, int lane, int64_t blk, bool blk_ok, int64_t e0,
                                                 int nvalid, bool fact, bool m_sr, const float m1[8],
@@ -358,7 +358,10 @@ __device__ __forceinline__ void requant_general(const StepParams& P, const DevTe
     // ---- m codes ----------------------------------------------------------
     uint32_t cm = 0;
     {
-        const bool fast = scale_in_fast_range(s_m);
+        const bool in_range = scale_in_fast_range(s_m);
+        // linear-bucket candidate tables: NF4 only (the TorchAO SDyn4 map has
+        // several thresholds per bucket near zero)
+        const bool fast = in_range && RECIPE != Q4_RECIPE_TORCHAO;
         const float rho16 = __fmul_rn(16.f, __frcp_rn(s_m));
         uint32_t w[8];
         if (m_sr) draws8(d.elem_offset + (uint64_t)e0, 0u, d.tensor_id, P.step, P.round_keys, w);
@@ -371,6 +374,14 @@ __device__ __forceinline__ void requant_general(const StepParams& P, const DevTe
                     const uint32_t bi = __float_as_uint(__fmaf_rn(x, rho16, kMagic + 16.f)) & 63u;
                     const int c = sm.lut_nf4_t[bi];
                     code = c + (x > wt.tm[hb + c] ? 1 : 0);
+                } else if (RECIPE == Q4_RECIPE_TORCHAO && in_range) {
+                    // #{k : x > T_k} by binary search over the ascending scaled
+                    // thresholds (normal scale: T_k is non-decreasing in k)
+                    int pos = (x > wt.tm[hb + 7]) ? 8 : 0;
+                    pos += (x > wt.tm[hb + pos + 3]) ? 4 : 0;
+                    pos += (x > wt.tm[hb + pos + 1]) ? 2 : 0;
+                    pos += (x > wt.tm[hb + pos]) ? 1 : 0;
+                    code = pos;
                 } else {
                     code = 0;
 #pragma unroll 1
@@ -409,7 +420,7 @@ __device__ __forceinline__ void requant_general(const StepParams& P, const DevTe
         const float rho = __frcp_rn(s_v);
         if (RECIPE == Q4_RECIPE_ZIP_SR) {
             uint32_t w[8];
-            draws8(d.elem_offset + (uint64_t)e0, 1u, d.tensor_id, P.step, P.round_keys, w);
+            if (!URTN) draws8(d.elem_offset + (uint64_t)e0, 1u, d.tensor_id, P.step, P.round_keys, w);
 #pragma unroll
             for (int i = 0; i < 8; ++i) {
                 const float x = v1[i];
@@ -425,8 +436,15 @@ __device__ __forceinline__ void requant_general(const StepParams& P, const DevTe
                         if (wt.av[hb + q] <= x) k = q;
                 }
                 const float2 e = wt.rd[hb + k];
-                // u * (r_k - r_{k+1}) with u = (w >> 8) 2^-24, as (w >> 8) * ((r_k - r_{k+1}) 2^-24)
-                int code = k + (__fmul_rn((float)(w[i] >> 8), e.y) < __fsub_rn(e.x, r[i]) ? 1 : 0);
+                int code;
+                if (URTN) {
+                    // Update-RTN: the neighbour whose preconditioner is nearer
+                    // to r (a tie keeps k)
+                    code = k == 15 ? 15 : k + (__fsub_rn(r[i], wt.rd[hb + k + 1].x) < __fsub_rn(e.x, r[i]) ? 1 : 0);
+                } else {
+                    // u * (r_k - r_{k+1}) with u = (w >> 8) 2^-24, as (w >> 8) * ((r_k - r_{k+1}) 2^-24)
+                    code = k + (__fmul_rn((float)(w[i] >> 8), e.y) < __fsub_rn(e.x, r[i]) ? 1 : 0);
+                }
                 if (i >= nvalid) code = 0;
                 cv |= (uint32_t)code << (4 * i);
             }
@@ -565,7 +583,7 @@ __device__ __forceinline__ void moments_and_update(const StepParams& P, const fl
 
 // ----------------------------------------------------------------- one tile, general path
 // `st` is the staged tile or nullptr (ragged tail: read from global memory).
-template <int RECIPE>
+template <int RECIPE, bool URTN>
 __device__ __forceinline__ void compute_tile(const StepParams& P, const DevTensor& d, int64_t pair,
                                              const Stage* st, int lane, SmemAll& sm, WarpTables& wt,
                                              const float my_nf4, const float my_nf4t, const float my_vl,
@@ -671,8 +689,8 @@ __device__ __forceinline__ void compute_tile(const StepParams& P, const DevTenso
 
     const float s_m = half_max(amax, half);
     const float s_v = fact ? 0.f : half_max(vmax, half);
-    requant_general<RECIPE>(P, d, sm, wt, lane, blk, blk_ok, e0, nvalid, fact, m_sr, m1, v1, r, s_m, s_v, my_nf4,
-                            my_nf4t, my_vl, my_vt);
+    requant_general<RECIPE, URTN>(P, d, sm, wt, lane, blk, blk_ok, e0, nvalid, fact, m_sr, m1, v1, r, s_m, s_v,
+                                  my_nf4, my_nf4t, my_vl, my_vt);
 }
 
 // ----------------------------------------------------------------- one tile, fast path
@@ -681,7 +699,7 @@ __device__ __forceinline__ void compute_tile(const StepParams& P, const DevTenso
 // when neither block needs the general requantisation (LM-head stochastic
 // rounding, or a new scale outside the fast range) the codes come from
 // per-bucket entries that carry everything one comparison needs.
-template <int RECIPE>
+template <int RECIPE, bool URTN>
 __device__ __forceinline__ void compute_tile_full(const StepParams& P, const DevTensor& d, int64_t pair,
                                                   const Stage& st, int lane, SmemAll& sm, WarpTables& wt,
                                                   const float my_nf4, const float my_nf4t, const float my_vl,
@@ -764,8 +782,8 @@ __device__ __forceinline__ void compute_tile_full(const StepParams& P, const Dev
     const float s_m = half_max(amax, half);
     const float s_v = fact ? 0.f : half_max(vmax_lane, half);
 
-    const bool fast = __all_sync(0xffffffffu, !m_sr && scale_in_fast_range(s_m) &&
-                                                  (fact || scale_in_fast_range(s_v)));
+    const bool fast = RECIPE != Q4_RECIPE_TORCHAO && !URTN &&
+                      __all_sync(0xffffffffu, !m_sr && scale_in_fast_range(s_m) && (fact || scale_in_fast_range(s_v)));
     if (!fast) {
         float m1s[8], v1s[8], rs[8];
 #pragma unroll
@@ -774,8 +792,8 @@ __device__ __forceinline__ void compute_tile_full(const StepParams& P, const Dev
             v1s[2 * k] = v1[k].x; v1s[2 * k + 1] = v1[k].y;
             rs[2 * k] = r[k].x; rs[2 * k + 1] = r[k].y;
         }
-        requant_general<RECIPE>(P, d, sm, wt, lane, blk, true, e0, 8, fact, m_sr, m1s, v1s, rs, s_m, s_v, my_nf4,
-                                my_nf4t, my_vl, my_vt);
+        requant_general<RECIPE, URTN>(P, d, sm, wt, lane, blk, true, e0, 8, fact, m_sr, m1s, v1s, rs, s_m, s_v,
+                                      my_nf4, my_nf4t, my_vl, my_vt);
         return;
     }
 
@@ -908,7 +926,9 @@ __device__ __forceinline__ void compute_tile_full(const StepParams& P, const Dev
 }
 
 // ----------------------------------------------------------------- the kernel
-template <int RECIPE>
+// URTN: the Update-RTN rounding variant of ZIP-SR (a separate instantiation,
+// so that the main kernels carry none of its code).
+template <int RECIPE, bool URTN>
 __global__ void __launch_bounds__(kStepThreads, 1) step_kernel(const __grid_constant__ StepParams P) {
     extern __shared__ unsigned char smem_raw[];
     // the tables need 256-byte alignment; the launch adds 256 bytes of slack
@@ -1106,12 +1126,12 @@ __global__ void __launch_bounds__(kStepThreads, 1) step_kernel(const __grid_cons
         }
         const bool full = c_p < c_n - 1 || ws.desc.numel - c_p * 2 * kBlock >= 2 * kBlock;
         if (full) {
-            compute_tile_full<RECIPE>(P, ws.desc, c_p, ws.st[s], lane, sm, ws.wt, my_nf4, my_nf4t, my_vl, my_vt,
-                                      my_vl1);
+            compute_tile_full<RECIPE, URTN>(P, ws.desc, c_p, ws.st[s], lane, sm, ws.wt, my_nf4, my_nf4t, my_vl,
+                                            my_vt, my_vl1);
         } else {
             const int64_t left = ws.desc.numel - c_p * 2 * kBlock;
-            compute_tile<RECIPE>(P, ws.desc, c_p, (left & 7) == 0 ? &ws.st[s] : nullptr, lane, sm, ws.wt, my_nf4,
-                                 my_nf4t, my_vl, my_vt);
+            compute_tile<RECIPE, URTN>(P, ws.desc, c_p, (left & 7) == 0 ? &ws.st[s] : nullptr, lane, sm, ws.wt,
+                                       my_nf4, my_nf4t, my_vl, my_vt);
         }
         ++c_p;
         ++c_tile;
@@ -1122,13 +1142,13 @@ __global__ void __launch_bounds__(kStepThreads, 1) step_kernel(const __grid_cons
 
 size_t step_smem_bytes() { return sizeof(SmemAll) + 256; }
 
-template <int RECIPE>
+template <int RECIPE, bool URTN>
 int configure(int device) {
     static bool done[64] = {false};
     if (device < 0 || device >= 64) device = 0;
     if (done[device]) return 0;
-    const cudaError_t e = cudaFuncSetAttribute(step_kernel<RECIPE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                               (int)step_smem_bytes());
+    const cudaError_t e = cudaFuncSetAttribute(step_kernel<RECIPE, URTN>,
+                                               cudaFuncAttributeMaxDynamicSharedMemorySize, (int)step_smem_bytes());
     if (e == cudaSuccess) done[device] = true;
     return (int)e;
 }
@@ -1155,20 +1175,21 @@ int launch_step(const StepParams& p, int grid, void* stream) {
     if (e != cudaSuccess) return (int)e;
     const size_t smem = step_smem_bytes();
     int ce = 0;
+#define Q4_LAUNCH(R, U)                                                         \
+    do {                                                                        \
+        if ((ce = configure<R, U>(dev))) return ce;                             \
+        step_kernel<R, U><<<grid, kStepThreads, smem, s>>>(p);                  \
+    } while (0)
     switch (p.recipe) {
         case Q4_RECIPE_ZIP_SR:
-            if ((ce = configure<Q4_RECIPE_ZIP_SR>(dev))) return ce;
-            step_kernel<Q4_RECIPE_ZIP_SR><<<grid, kStepThreads, smem, s>>>(p);
+            if (p.v_update_rtn) Q4_LAUNCH(Q4_RECIPE_ZIP_SR, true);
+            else Q4_LAUNCH(Q4_RECIPE_ZIP_SR, false);
             break;
-        case Q4_RECIPE_ZE_EDEN:
-            if ((ce = configure<Q4_RECIPE_ZE_EDEN>(dev))) return ce;
-            step_kernel<Q4_RECIPE_ZE_EDEN><<<grid, kStepThreads, smem, s>>>(p);
-            break;
-        default:
-            if ((ce = configure<Q4_RECIPE_FACTORED>(dev))) return ce;
-            step_kernel<Q4_RECIPE_FACTORED><<<grid, kStepThreads, smem, s>>>(p);
-            break;
+        case Q4_RECIPE_ZE_EDEN: Q4_LAUNCH(Q4_RECIPE_ZE_EDEN, false); break;
+        case Q4_RECIPE_TORCHAO: Q4_LAUNCH(Q4_RECIPE_TORCHAO, false); break;
+        default: Q4_LAUNCH(Q4_RECIPE_FACTORED, false); break;
     }
+#undef Q4_LAUNCH
     return (int)cudaGetLastError();
 }
 

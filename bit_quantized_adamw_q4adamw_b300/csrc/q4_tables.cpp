@@ -14,6 +14,11 @@
 //              (e = 0..3), an indicator bit, f = 3 - e fraction bits;
 //              value (2^f + 9(j+1)) / (10^(e+1) 2^f); the all-zero code is 0.
 //   Dyn4-NZ -- as Dyn4 with the all-zero code at 10^-4 (no zero level).
+//   SDyn4   -- signed 4-bit dynamic-exponent map (the TorchAO baseline's first
+//              moment): on rung i = 0, 1, 2, the midpoints of 2^i equal parts
+//              of [1/10, 1] scaled by 10^(i-2), with both signs, plus 0 and 1.
+//   Lin4-NZ -- linear zero-excluding map k/16, k = 1..16 (TorchAO's second
+//              moment).
 // RTN thresholds are FP32 roundings of double midpoints of adjacent levels.
 //
 // Candidate tables.  The kernel finds a code by a table lookup on a cheap
@@ -154,13 +159,43 @@ bool build_log(const float* pts, int np, bool levels, uint8_t* lut) {
     return true;
 }
 
-Codebook g_books[3];
+Codebook make_sdyn4() {
+    double v[16];
+    int n = 0;
+    double rung = 0.01;
+    for (int i = 0; i < 3; ++i, rung *= 10.0) {
+        const int parts = 1 << i;
+        for (int j = 0; j < parts; ++j) {
+            const double mid = 0.1 + 0.9 * (2.0 * j + 1.0) / (2.0 * parts);
+            v[n++] = rung * mid;
+            v[n++] = -rung * mid;
+        }
+    }
+    v[n++] = 0.0;
+    v[n++] = 1.0;
+    std::sort(v, v + 16);
+    Codebook c{};
+    for (int k = 0; k < 16; ++k) c.levels[k] = (float)v[k];
+    fill_thresholds(c);
+    return c;
+}
+
+Codebook make_lin4nz() {
+    Codebook c{};
+    for (int k = 0; k < 16; ++k) c.levels[k] = (float)(k + 1) / 16.0f;
+    fill_thresholds(c);
+    return c;
+}
+
+Codebook g_books[5];
 std::once_flag g_once;
 
 void init_books() {
     g_books[0] = make_nf4();
     g_books[1] = make_dyn4(false);
     g_books[2] = make_dyn4(true);
+    g_books[3] = make_sdyn4();
+    g_books[4] = make_lin4nz();
 }
 
 }  // namespace
@@ -170,8 +205,8 @@ const Codebook& codebook(int which) {
     return g_books[which];
 }
 
-bool build_tables(int vbook, Tables* t) {
-    const Codebook& nf4 = codebook(0);
+bool build_tables(int mbook, int vbook, Tables* t) {
+    const Codebook& nf4 = codebook(mbook);
     const Codebook& v = codebook(vbook);
     std::memset(t, 0, sizeof(*t));
     for (int k = 0; k < 16; ++k) {
@@ -184,8 +219,10 @@ bool build_tables(int vbook, Tables* t) {
     }
     t->nf4_t[15] = INFINITY;
     t->vt[15] = INFINITY;
-    if (!build_linear(nf4.thresholds, 15, false, t->lut_nf4_t)) return false;
-    if (!build_linear(nf4.levels, 16, true, t->lut_nf4_l)) return false;
+    // Linear buckets suit NF4; a codebook with several thresholds in one
+    // bucket (SDyn4 near zero) is searched by the kernel without them.
+    t->m_lut = build_linear(nf4.thresholds, 15, false, t->lut_nf4_t) &&
+               build_linear(nf4.levels, 16, true, t->lut_nf4_l) ? 1 : 0;
     if (!build_log(v.levels, 16, true, t->lut_v_l)) return false;
     if (!build_log(v.thresholds, 15, false, t->lut_v_t)) return false;
     for (int i = 0; i < 64; ++i) {

@@ -123,6 +123,12 @@ WORKLOADS = {
     "llama8b_zipsr": Workload("llama8b_zipsr", _llama_8b(), "zip_sr", "tensor_scaled", sigma_range=(1e-6, 1e-2)),
     "llama8b_zeeden": Workload("llama8b_zeeden", _llama_8b(), "ze_eden", "tensor_scaled",
                                sigma_range=(1e-6, 1e-2)),
+    # The paper's TorchAO 4-bit baseline (SDyn4-RTN m, Lin4-NZ State-RTN v) on
+    # the same parameter sets, for comparison.
+    "llama8b_torchao": Workload("llama8b_torchao", _llama_8b(), "torchao", "tensor_scaled",
+                                sigma_range=(1e-6, 1e-2)),
+    "gpt1p4b_torchao": Workload("gpt1p4b_torchao", _gpt_1p4b(), "torchao", "tensor_scaled", first_step=9001,
+                                lm_head_sr=True, sigma_range=(1e-5, 1e-2)),
 }
 
 

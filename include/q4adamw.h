@@ -64,7 +64,11 @@ typedef enum q4_status {
 typedef enum q4_recipe {
     Q4_RECIPE_ZIP_SR = 0,   /* listing page Table 2, row "ZIP-SR 4-bit" */
     Q4_RECIPE_ZE_EDEN = 1,  /* listing page Table 2, row "ZE-EDEN 4-bit" */
-    Q4_RECIPE_FACTORED = 2  /* AReno docs, State representation */
+    Q4_RECIPE_FACTORED = 2, /* AReno docs, State representation */
+    Q4_RECIPE_TORCHAO = 3   /* listing page Table 2, row "TorchAO 4-bit": the
+                               paper's baseline -- SDyn4 State-RTN first moment
+                               (LM head included), Lin4-NZ State-RTN second
+                               moment, no EDEN */
 } q4_recipe;
 
 /* Per-tensor flags (q4adamw_tensor_t.flags). */
@@ -76,7 +80,14 @@ typedef enum q4_recipe {
 
 /* Per-call flags (q4adamw_step). */
 #define Q4_LM_HEAD_SR_ACTIVE 0x1u /* the final 10% phase of the schedule: the
-                                     caller sets it when step > 0.9 * total */
+                                     caller sets it when step > 0.9 * total
+                                     (no effect under Q4_RECIPE_TORCHAO) */
+#define Q4_M_SR_ALL 0x2u          /* rounding variant (listing page Tables 1,
+                                     11): State-SR for the first moment of
+                                     every tensor, in every phase */
+#define Q4_V_UPDATE_RTN 0x4u      /* rounding variant (Table 1): Update-RTN in
+                                     place of Update-SR for the second moment;
+                                     Q4_RECIPE_ZIP_SR only, Q4_EINVAL otherwise */
 
 /*
  * One parameter tensor and its optimizer state.  All pointers are device
@@ -196,6 +207,8 @@ int q4adamw_header_check(const q4adamw_header_t* h, int recipe);
 int q4adamw_step(const q4adamw_tensor_t* t, int n, float lr, float beta1, float beta2, float eps, float weight_decay,
                  int64_t step, uint64_t seed, int recipe, uint32_t flags, void* workspace, int64_t workspace_bytes,
                  void* stream);
+/* (flags: any bit outside Q4_LM_HEAD_SR_ACTIVE | Q4_M_SR_ALL | Q4_V_UPDATE_RTN,
+ * or Q4_V_UPDATE_RTN with a recipe other than ZIP-SR, returns Q4_EINVAL.) */
 
 /*
  * Status word of the most recent q4adamw_step that used `workspace`
@@ -212,7 +225,7 @@ int q4adamw_step_status(const void* workspace, uint32_t* status, void* stream);
 /*
  * Decode the state of one tensor into FP32 device buffers of numel floats
  * (either may be NULL): m_out = NF4[qm]*s_m; v_out = V[qv]*s_v for packed v
- * (V = Dyn4 for ZIP-SR, Dyn4-NZ otherwise) or R_i*C_j/mean(R) for a factored
+ * (V = Dyn4 for ZIP-SR, Lin4-NZ for TorchAO, Dyn4-NZ otherwise; m in SDyn4 for TorchAO) or R_i*C_j/mean(R) for a factored
  * tensor.  Asynchronous on stream.
  */
 int q4adamw_dequant_state(const q4adamw_tensor_t* t, int recipe, float* m_out, float* v_out, void* stream);
@@ -244,7 +257,8 @@ int q4adamw_step_noalloc(const q4adamw_tensor_t* t, int n, float lr, float beta1
 
 /*
  * The library's own codebook tables (host-only).  which: 0 = NF4, 1 = Dyn4
- * (zero-inclusive), 2 = Dyn4-NZ (zero-excluding).  levels: 16 ascending FP32
+ * (zero-inclusive), 2 = Dyn4-NZ (zero-excluding), 3 = SDyn4 (signed dynamic
+ * exponent), 4 = Lin4-NZ (k/16, k = 1..16).  levels: 16 ascending FP32
  * levels; thresholds: the 15 FP32 RTN decision points (rounded double
  * midpoints).  Either pointer may be NULL.
  */

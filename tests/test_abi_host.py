@@ -47,14 +47,14 @@ def test_version_and_strerror():
     assert q4.q4adamw_strerror(-99) == "unknown status"
 
 
-@pytest.mark.parametrize("which,name", [(0, "nf4"), (1, "dyn4"), (2, "dyn4nz")])
+@pytest.mark.parametrize("which,name", [(0, "nf4"), (1, "dyn4"), (2, "dyn4nz"), (3, "sdyn4"), (4, "lin4nz")])
 def test_library_codebooks_match_oracle_bitwise(which, name):
     lv, th = q4.q4adamw_codebook(which)
     cb = O.codebooks()
     assert np.array_equal(lv.view(np.uint32), cb[name].view(np.uint32))
     assert np.array_equal(th.view(np.uint32), cb[name + "_t"].view(np.uint32))
     with pytest.raises(q4.Q4Error):
-        q4.q4adamw_codebook(3)
+        q4.q4adamw_codebook(5)
 
 
 def _t(numel, rows=1, flags=0, **kw):
@@ -115,6 +115,8 @@ def test_step_validation_happens_before_any_device_work():
                               a["recipe"], a["flags"], ws, wsb, None)
 
     assert call(recipe=9) == _native.Q4_ERECIPE
+    assert call(flags=0x8) == _native.Q4_EINVAL                       # unknown flag bit
+    assert call(recipe=1, flags=_native.Q4_V_UPDATE_RTN) == _native.Q4_EINVAL   # ZIP-SR only
     assert call(step=0) == _native.Q4_EINVAL
     assert call(b1=1.0) == _native.Q4_EINVAL
     assert call(b2=-0.1) == _native.Q4_EINVAL

@@ -11,6 +11,7 @@ import numpy as np
 import pytest
 import torch
 
+import bit_quantized_adamw_q4adamw_b300 as q4
 from bit_quantized_adamw_q4adamw_b300 import workloads as W
 from parity_util import HYPER, Pair, grads_for
 
@@ -58,7 +59,7 @@ RAGGED = [(1,), (5,), (127,), (128,), (129,), (255,), (256,), (1000,), (3, 129),
           (7, 128), (128 * 13 + 17,)]
 
 
-@pytest.mark.parametrize("recipe", ["zip_sr", "ze_eden"])
+@pytest.mark.parametrize("recipe", ["zip_sr", "ze_eden", "torchao"])
 @pytest.mark.parametrize("sr", [False, True])
 def test_ragged_tensor_list(recipe, sr):
     flags = [W.T_LM_HEAD if i % 3 == 0 else 0 for i in range(len(RAGGED))]
@@ -88,7 +89,7 @@ def test_degenerate_values():
     n = 128 * 12
     w = W.custom("deg", [(n,)], "zip_sr")
     rng = np.random.default_rng(5)
-    for recipe in ("zip_sr", "ze_eden", "factored"):
+    for recipe in ("zip_sr", "ze_eden", "factored", "torchao"):
         p = Pair(w.tensors, recipe)
         for t in range(1, 5):
             g = rng.normal(0, 1, n).astype(np.float32)
@@ -135,7 +136,7 @@ def test_sharded_tensor_matches_whole():
                            torch.cat([split.gpu.view(0, "v_codes").cpu(), split.gpu.view(1, "v_codes").cpu()]))
 
 
-@pytest.mark.parametrize("recipe", ["zip_sr", "ze_eden", "factored"])
+@pytest.mark.parametrize("recipe", ["zip_sr", "ze_eden", "factored", "torchao"])
 def test_dequant_state_matches_oracle(recipe):
     shapes = [(40, 64), (200,), (3, 129)]
     w = W.custom("dq", shapes, recipe)
@@ -145,7 +146,7 @@ def test_dequant_state_matches_oracle(recipe):
     for i, o in enumerate(p.ora):
         m, v = p.gpu.dequant(i)
         torch.cuda.synchronize()
-        assert np.array_equal(m.cpu().numpy(), o.m_dequant())
+        assert np.array_equal(m.cpu().numpy(), o.m_dequant(recipe))
         vo = o.v_dequant(recipe)
         if o.factored:
             assert np.allclose(v.cpu().numpy(), vo, rtol=3e-5, atol=0)
@@ -161,3 +162,36 @@ def test_state_init_header_and_zero_state():
     assert h.n_tensors == 2 and h.numel_total == 300 + 64 * 64
     for name in ("m_codes", "m_scale"):
         assert int(getattr(p.gpu, name).abs().sum()) == 0
+
+
+@pytest.mark.parametrize("recipe", ["zip_sr", "ze_eden", "torchao"])
+def test_m_sr_all_variant(recipe):
+    # Rounding variant: State-SR for every tensor's first moment (flag 0x2).
+    w = W.custom("msr", RAGGED, recipe, flags=[0] * len(RAGGED), grad="normal", sigma=(1e-3, 1e-3))
+    p = Pair(w.tensors, recipe)
+    for t in range(1, 6):
+        p.step(t, grads_for(w, t), seed=11, flags=q4.Q4_M_SR_ALL)
+        _assert_exact(p.compare(), t)
+
+
+def test_v_update_rtn_variant():
+    # Rounding variant: Update-RTN in place of ZIP-SR's Update-SR (flag 0x4),
+    # with mixed-magnitude gradients so that both neighbours occur.
+    shapes = [(4096,), (300,), (64, 130)]
+    w = W.custom("urtn", shapes, "zip_sr", flags=[W.T_LM_HEAD, 0, 0], grad="tensor_scaled", sigma=(1e-6, 1e-2))
+    p = Pair(w.tensors, "zip_sr")
+    for t in range(1, 8):
+        p.step(t, grads_for(w, t), seed=2, flags=q4.Q4_V_UPDATE_RTN | q4.Q4_LM_HEAD_SR_ACTIVE)
+        _assert_exact(p.compare(), t)
+
+
+def test_torchao_tensor_scaled_multistep():
+    # The TorchAO baseline on a GPT-like list with per-tensor gradient scales in
+    # [1e-5, 1e-2], LM head flagged and the final phase active (stays RTN).
+    shapes = [(512, 256), (256,), (768, 256), (256,), (1000,)]
+    flags = [W.T_LM_HEAD, 0, 0, 0, 0]
+    w = W.custom("tao", shapes, "torchao", flags=flags, grad="tensor_scaled", sigma=(1e-5, 1e-2))
+    p = Pair(w.tensors, "torchao")
+    for t in range(9001, 9011):
+        p.step(t, grads_for(w, t), seed=3, flags=q4.Q4_LM_HEAD_SR_ACTIVE)
+        _assert_exact(p.compare(), t)
