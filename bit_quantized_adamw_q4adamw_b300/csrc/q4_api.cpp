@@ -371,6 +371,8 @@ int q4adamw_step(const q4adamw_tensor_t* t, int n, float lr, float beta1, float 
     // that holds whenever eps lies in [2^-100, 2^60].
     p.fast_math = (eps >= 0x1p-100f && eps <= 0x1p60f) ? 1 : 0;
     p.v_update_rtn = (flags & Q4_V_UPDATE_RTN) ? 1 : 0;
+    p.has_m_sr = 0;
+    for (int i = 0; i < n; ++i) p.has_m_sr |= (desc[i].flags & q4::DF_M_SR) ? 1 : 0;
     p.x2_beta1 = make_float2(p.beta1, p.beta1);
     p.x2_beta2 = make_float2(p.beta2, p.beta2);
     p.x2_omb1 = make_float2(p.omb1, p.omb1);

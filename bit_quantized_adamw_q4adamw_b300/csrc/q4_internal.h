@@ -87,6 +87,7 @@ struct StepParams {
     uint32_t step;
     int fast_math;                // eps and c2 keep 1/(sqrt(v) c2 + eps) in the fast domain
     int v_update_rtn;             // ZIP-SR with Update-RTN in place of Update-SR
+    int has_m_sr;                 // some tensor rounds its first moment stochastically
     // the step scalars broadcast to pairs, for the paired FP32 instructions
     float2 x2_beta1, x2_beta2, x2_omb1, x2_omb2, x2_c2, x2_eps, x2_decay, x2_neg_step;
     uint32_t round_keys[20];      // Philox key schedule: (k0, k1) for rounds 0..9

@@ -699,7 +699,7 @@ __device__ __forceinline__ void compute_tile(const StepParams& P, const DevTenso
 // when neither block needs the general requantisation (LM-head stochastic
 // rounding, or a new scale outside the fast range) the codes come from
 // per-bucket entries that carry everything one comparison needs.
-template <int RECIPE, bool URTN>
+template <int RECIPE, bool URTN, bool MSR>
 __device__ __forceinline__ void compute_tile_full(const StepParams& P, const DevTensor& d, int64_t pair,
                                                   const Stage& st, int lane, SmemAll& sm, WarpTables& wt,
                                                   const float my_nf4, const float my_nf4t, const float my_vl,
@@ -783,7 +783,8 @@ __device__ __forceinline__ void compute_tile_full(const StepParams& P, const Dev
     const float s_v = fact ? 0.f : half_max(vmax_lane, half);
 
     const bool fast = RECIPE != Q4_RECIPE_TORCHAO && !URTN &&
-                      __all_sync(0xffffffffu, !m_sr && scale_in_fast_range(s_m) && (fact || scale_in_fast_range(s_v)));
+                      __all_sync(0xffffffffu, (MSR || !m_sr) && scale_in_fast_range(s_m) &&
+                                                  (fact || scale_in_fast_range(s_v)));
     if (!fast) {
         float m1s[8], v1s[8], rs[8];
 #pragma unroll
@@ -798,9 +799,18 @@ __device__ __forceinline__ void compute_tile_full(const StepParams& P, const Dev
     }
 
     // ---- fast tables at the new scales ------------------------------------
-    // mt[half][b] = {t_c * s_m, c} for the linear bucket b (c its candidate);
-    // buckets 0..32 occur for |m'| <= s_m.
-    {
+    // RTN: mt[half][b] = {t_c * s_m, c} for the linear bucket b (c its
+    // candidate); buckets 0..32 occur for |m'| <= s_m.
+    // State-SR (LM head in the final phase): a_k = level k at the new scale;
+    // the cell search reads a_{c+1} (floats 0..15 of mt[half]), then
+    // (a_k, d_k) with d_k = (a_{k+1} - a_k) 2^-24 (float2 8..23).
+    if (MSR && m_sr) {
+        const float a = __fmul_rn(my_nf4, s_m);
+        const float a1 = __shfl_down_sync(0xffffffffu, a, 1);
+        float* mb = reinterpret_cast<float*>(&wt.mt[half][0]);
+        mb[j] = a1;
+        reinterpret_cast<float2*>(mb + 16)[j] = make_float2(a, j < 15 ? __fmul_rn(__fsub_rn(a1, a), kTwoM24) : 0.f);
+    } else {
         const float2 e1 = sm.nf4_bucket[j];
         const float2 e2 = sm.nf4_bucket[j + 16];
         wt.mt[half][j] = make_float2(__fmul_rn(e1.x, s_m), e1.y);
@@ -828,9 +838,32 @@ __device__ __forceinline__ void compute_tile_full(const StepParams& P, const Dev
     }
     __syncwarp();
 
-    // ---- m codes: NF4 RTN ---------------------------------------------------
+    // ---- m codes: NF4 RTN, or NF4 State-SR -----------------------------------
     uint32_t cm;
-    {
+    if (MSR && m_sr) {
+        const float rho16 = __fmul_rn(16.f, rcp_rn_normal<1>(s_m));
+        const uint32_t mt_base = tb + (uint32_t)((char*)&wt.mt[half][0] - (char*)&wt);
+        const uint32_t lut = smem_addr(sm.lut_nf4_l);
+        uint32_t w[8], c[8];
+        draws8(d.elem_offset + (uint64_t)e0, 0u, d.tensor_id, P.step, P.round_keys, w);
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            const float2 z = fma2_rn(m1[k], make_float2(rho16, rho16), make_float2(kMagic + 16.f, kMagic + 16.f));
+            const uint32_t c0 = lds_u8(lut + (__float_as_uint(z.x) & 63u));
+            const uint32_t c1 = lds_u8(lut + (__float_as_uint(z.y) & 63u));
+            const uint32_t k0 = c0 + (lds_f32(mt_base + c0 * 4u) <= m1[k].x ? 1u : 0u);
+            const uint32_t k1 = c1 + (lds_f32(mt_base + c1 * 4u) <= m1[k].y ? 1u : 0u);
+            const float2 e0v = lds_f32x2(mt_base + 64u + k0 * 8u);
+            const float2 e1v = lds_f32x2(mt_base + 64u + k1 * 8u);
+            // u (a_{k+1} - a_k) with u = (w >> 8) 2^-24, as (w >> 8) ((a_{k+1} - a_k) 2^-24)
+            const float2 t = mul2_rn(make_float2((float)(w[2 * k] >> 8), (float)(w[2 * k + 1] >> 8)),
+                                     make_float2(e0v.y, e1v.y));
+            const float2 gap = add2_rn(m1[k], make_float2(-e0v.x, -e1v.x));
+            c[2 * k] = k0 + (t.x < gap.x ? 1u : 0u);
+            c[2 * k + 1] = k1 + (t.y < gap.y ? 1u : 0u);
+        }
+        cm = pack8(c);
+    } else {
         const float rho16 = __fmul_rn(16.f, rcp_rn_normal<1>(s_m));
         const uint32_t mt_base = tb + (uint32_t)((char*)&wt.mt[half][0] - (char*)&wt);
         uint32_t c[8];
@@ -926,9 +959,11 @@ __device__ __forceinline__ void compute_tile_full(const StepParams& P, const Dev
 }
 
 // ----------------------------------------------------------------- the kernel
-// URTN: the Update-RTN rounding variant of ZIP-SR (a separate instantiation,
-// so that the main kernels carry none of its code).
-template <int RECIPE, bool URTN>
+// URTN: the Update-RTN rounding variant of ZIP-SR; MSR: some tensor rounds
+// its first moment stochastically (the LM head in the final phase), which the
+// fast path then handles too.  Separate instantiations, so that the main
+// kernels carry none of that code.
+template <int RECIPE, bool URTN, bool MSR>
 __global__ void __launch_bounds__(kStepThreads, 1) step_kernel(const __grid_constant__ StepParams P) {
     extern __shared__ unsigned char smem_raw[];
     // the tables need 256-byte alignment; the launch adds 256 bytes of slack
@@ -1126,8 +1161,8 @@ __global__ void __launch_bounds__(kStepThreads, 1) step_kernel(const __grid_cons
         }
         const bool full = c_p < c_n - 1 || ws.desc.numel - c_p * 2 * kBlock >= 2 * kBlock;
         if (full) {
-            compute_tile_full<RECIPE, URTN>(P, ws.desc, c_p, ws.st[s], lane, sm, ws.wt, my_nf4, my_nf4t, my_vl,
-                                            my_vt, my_vl1);
+            compute_tile_full<RECIPE, URTN, MSR>(P, ws.desc, c_p, ws.st[s], lane, sm, ws.wt, my_nf4, my_nf4t,
+                                                 my_vl, my_vt, my_vl1);
         } else {
             const int64_t left = ws.desc.numel - c_p * 2 * kBlock;
             compute_tile<RECIPE, URTN>(P, ws.desc, c_p, (left & 7) == 0 ? &ws.st[s] : nullptr, lane, sm, ws.wt,
@@ -1142,12 +1177,12 @@ __global__ void __launch_bounds__(kStepThreads, 1) step_kernel(const __grid_cons
 
 size_t step_smem_bytes() { return sizeof(SmemAll) + 256; }
 
-template <int RECIPE, bool URTN>
+template <int RECIPE, bool URTN, bool MSR>
 int configure(int device) {
     static bool done[64] = {false};
     if (device < 0 || device >= 64) device = 0;
     if (done[device]) return 0;
-    const cudaError_t e = cudaFuncSetAttribute(step_kernel<RECIPE, URTN>,
+    const cudaError_t e = cudaFuncSetAttribute(step_kernel<RECIPE, URTN, MSR>,
                                                cudaFuncAttributeMaxDynamicSharedMemorySize, (int)step_smem_bytes());
     if (e == cudaSuccess) done[device] = true;
     return (int)e;
@@ -1175,19 +1210,23 @@ int launch_step(const StepParams& p, int grid, void* stream) {
     if (e != cudaSuccess) return (int)e;
     const size_t smem = step_smem_bytes();
     int ce = 0;
-#define Q4_LAUNCH(R, U)                                                         \
+#define Q4_LAUNCH(R, U, M)                                                      \
     do {                                                                        \
-        if ((ce = configure<R, U>(dev))) return ce;                             \
-        step_kernel<R, U><<<grid, kStepThreads, smem, s>>>(p);                  \
+        if ((ce = configure<R, U, M>(dev))) return ce;                          \
+        step_kernel<R, U, M><<<grid, kStepThreads, smem, s>>>(p);               \
     } while (0)
     switch (p.recipe) {
         case Q4_RECIPE_ZIP_SR:
-            if (p.v_update_rtn) Q4_LAUNCH(Q4_RECIPE_ZIP_SR, true);
-            else Q4_LAUNCH(Q4_RECIPE_ZIP_SR, false);
+            if (p.v_update_rtn) Q4_LAUNCH(Q4_RECIPE_ZIP_SR, true, false);
+            else if (p.has_m_sr) Q4_LAUNCH(Q4_RECIPE_ZIP_SR, false, true);
+            else Q4_LAUNCH(Q4_RECIPE_ZIP_SR, false, false);
             break;
-        case Q4_RECIPE_ZE_EDEN: Q4_LAUNCH(Q4_RECIPE_ZE_EDEN, false); break;
-        case Q4_RECIPE_TORCHAO: Q4_LAUNCH(Q4_RECIPE_TORCHAO, false); break;
-        default: Q4_LAUNCH(Q4_RECIPE_FACTORED, false); break;
+        case Q4_RECIPE_ZE_EDEN:
+            if (p.has_m_sr) Q4_LAUNCH(Q4_RECIPE_ZE_EDEN, false, true);
+            else Q4_LAUNCH(Q4_RECIPE_ZE_EDEN, false, false);
+            break;
+        case Q4_RECIPE_TORCHAO: Q4_LAUNCH(Q4_RECIPE_TORCHAO, false, false); break;
+        default: Q4_LAUNCH(Q4_RECIPE_FACTORED, false, false); break;
     }
 #undef Q4_LAUNCH
     return (int)cudaGetLastError();
