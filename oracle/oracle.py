@@ -28,6 +28,10 @@ What pins each function (tests under tests/test_oracle_*.py):
   * ZE-EDEN scale -- the closed form |y|^2 / <y, yhat> in float64; exactly
     1 on blocks that sit on codebook levels.
   * Factored v -- brute-force float64 row/column means; rank-1 exactness.
+  * Gradient-norm clipping -- the sum of squares against textbook recursive
+    pairwise summation (numpy, level by level) and a float64 error bound;
+    the factor against torch.nn.utils.clip_grad_norm_ on exact-norm cases;
+    the clipped step against the plain step on exactly pre-scaled gradients.
   * Storage -- 1.0625 bytes/param and 8 / 1.0625 = 7.53x, the figures the
     news page (paragraph 4) prints.
 """
@@ -119,6 +123,12 @@ def lib():
         L.oracle_adamw_fp32.argtypes = [P, P, P, P, I64, F, F, F, F, F, I64]
         L.oracle_step_tensor.argtypes = [P, P, F, F, F, F, F, I64, U64, ctypes.c_int, U32]
         L.oracle_step_tensor.restype = ctypes.c_int
+        L.oracle_step_tensor_clip.argtypes = [P, P, F, F, F, F, F, I64, U64, ctypes.c_int, U32, F]
+        L.oracle_step_tensor_clip.restype = ctypes.c_int
+        L.oracle_grad_sqnorm.argtypes = [P, ctypes.c_int, P]
+        L.oracle_grad_sqnorm.restype = F
+        L.oracle_clip_factor.argtypes = [F, F]
+        L.oracle_clip_factor.restype = F
         L.oracle_bf16_round.argtypes = [P, I64, P]
         _lib = L
     return _lib
@@ -212,6 +222,26 @@ def bf16_round(x) -> np.ndarray:
     return out
 
 
+# ------------------------------------------------- gradient-norm clipping
+def grad_sqnorm(grads) -> np.float32:
+    """Sum of squares of a list of BF16 gradients (uint16 bit arrays) in the
+    canonical FP32 order of q4_oracle.c (tile butterfly, per-tensor pairwise
+    tree over tiles, tensors left to right)."""
+    gs = [np.ascontiguousarray(g, dtype=np.uint16).reshape(-1) for g in grads]
+    arr = (_Tensor * max(1, len(gs)))()
+    for i, g in enumerate(gs):
+        arr[i].grad = _ptr(g)
+        arr[i].numel = g.size
+    tiles = max([1] + [(g.size + 255) // 256 for g in gs])
+    scratch = np.zeros(tiles, np.float32)
+    return np.float32(lib().oracle_grad_sqnorm(ctypes.addressof(arr), len(gs), _ptr(scratch)))
+
+
+def clip_factor(sqnorm, max_norm) -> np.float32:
+    """min(1, max_norm / (sqrt(sqnorm) + 1e-6)) in FP32."""
+    return np.float32(lib().oracle_clip_factor(np.float32(sqnorm), np.float32(max_norm)))
+
+
 # ---------------------------------------------------------------- state
 def nblocks(numel: int) -> int:
     return (numel + BLOCK - 1) // BLOCK
@@ -256,7 +286,8 @@ class OracleTensor:
         return t
 
     def step(self, grad_bf16: np.ndarray, lr, beta1, beta2, eps, wd, step, seed, recipe: str,
-             call_flags: int = 0) -> None:
+             call_flags: int = 0, clip: float | None = None) -> None:
+        """One step; ``clip`` (a clip_factor() value) scales every gradient."""
         g = np.ascontiguousarray(grad_bf16, dtype=np.uint16)
         assert g.size == self.param.size
         d = _Tensor()
@@ -275,8 +306,12 @@ class OracleTensor:
         d.tensor_id = self.tensor_id
         d.flags = self.flags
         cbs = _cb_struct()
-        rc = lib().oracle_step_tensor(ctypes.addressof(cbs), ctypes.addressof(d), lr, beta1, beta2, eps, wd,
-                                      step, seed, RECIPES[recipe], call_flags)
+        if clip is None:
+            rc = lib().oracle_step_tensor(ctypes.addressof(cbs), ctypes.addressof(d), lr, beta1, beta2, eps, wd,
+                                          step, seed, RECIPES[recipe], call_flags)
+        else:
+            rc = lib().oracle_step_tensor_clip(ctypes.addressof(cbs), ctypes.addressof(d), lr, beta1, beta2, eps,
+                                               wd, step, seed, RECIPES[recipe], call_flags, clip)
         if rc != 0:
             raise ValueError(f"oracle_step_tensor failed: {rc}")
 

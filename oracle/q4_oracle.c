@@ -320,12 +320,17 @@ void oracle_adamw_fp32(float* theta, const float* grad, float* m, float* v, int6
 /* g^2 as exponential averages; vhat_ij = R_i * C_j / mean_i(R_i).        */
 /* Sums run in double (exact per-term g^2 of BF16 inputs), rounded once. */
 /* ------------------------------------------------------------------ */
+static double clipped(uint16_t h, float clip) {
+    float g = bf16_to_f32(h);
+    return (double)(clip != 1.0f ? g * clip : g);
+}
+
 static void factored_update(const scal_t* s, const uint16_t* grad, int64_t rows, int64_t cols, float* R, float* C,
-                            float* rbar_out) {
+                            float* rbar_out, float clip) {
     for (int64_t i = 0; i < rows; ++i) {
         double acc = 0.0;
         for (int64_t j = 0; j < cols; ++j) {
-            double g = bf16_to_f32(grad[i * cols + j]);
+            double g = clipped(grad[i * cols + j], clip);
             acc += g * g;
         }
         float mean = (float)(acc / (double)cols);
@@ -334,7 +339,7 @@ static void factored_update(const scal_t* s, const uint16_t* grad, int64_t rows,
     for (int64_t j = 0; j < cols; ++j) {
         double acc = 0.0;
         for (int64_t i = 0; i < rows; ++i) {
-            double g = bf16_to_f32(grad[i * cols + j]);
+            double g = clipped(grad[i * cols + j], clip);
             acc += g * g;
         }
         float mean = (float)(acc / (double)rows);
@@ -371,8 +376,91 @@ typedef struct {
     float lin4nz[16], lin4nz_t[15];
 } oracle_codebooks;
 
+/* Global gradient-norm clipping (AReno docs "State representation": norm and
+ * clipping run directly on the BF16 gradient shards; listing page: global
+ * gradient-clipping events).  Reading: torch.nn.utils.clip_grad_norm_ with
+ * the 2-norm, clip = min(1, max_norm * (1 / (norm + 1e-6))), every operation
+ * in FP32 as torch rounds it, norm = sqrt of the sum of squares below, and
+ * the factor multiplies the FP32 value of each BF16 gradient inside the step
+ * (before the moments, the factored statistics included).
+ * The sum of squares runs in one canonical FP32 order:
+ *   tile (elements [256 i, 256 i + 256) of a tensor; missing elements 0): lane
+ *     l = 0..31 sums the squares of its 8 elements 8l..8l+7 pairwise,
+ *     ((s0+s1)+(s2+s3))+((s4+s5)+(s6+s7)); then an xor butterfly over the
+ *     lanes with offsets 1, 2, 4, 8, 16; the result is lane 0's value;
+ *   tensor: the tile sums in a complete binary tree over the tile index
+ *     (padded with zeros to a power of two, adjacent pairs at every level);
+ *   list: the tensor sums left to right in list order, from 0.           */
+static float tile_sqsum(const uint16_t* grad, int64_t numel, int64_t tile) {
+    float q[32];
+    for (int l = 0; l < 32; ++l) {
+        float sq[8];
+        for (int k = 0; k < 8; ++k) {
+            int64_t e = tile * 256 + 8 * l + k;
+            float g = (e < numel) ? bf16_to_f32(grad[e]) : 0.0f;
+            sq[k] = g * g;
+        }
+        q[l] = ((sq[0] + sq[1]) + (sq[2] + sq[3])) + ((sq[4] + sq[5]) + (sq[6] + sq[7]));
+    }
+    for (int o = 1; o < 32; o <<= 1) {
+        float nq[32];
+        for (int l = 0; l < 32; ++l) nq[l] = q[l] + q[l ^ o];
+        memcpy(q, nq, sizeof q);
+    }
+    return q[0];
+}
+
+static float pow2_tree(float* a, int64_t n) {
+    if (n == 0) return 0.0f;
+    int64_t p = 1;
+    while (p < n) p <<= 1;
+    for (int64_t w = 1; w < p; w <<= 1)
+        for (int64_t i = 0; i + w < p; i += 2 * w) {
+            float x = (i < n) ? a[i] : 0.0f;
+            float y = (i + w < n) ? a[i + w] : 0.0f;
+            if (i < n) a[i] = x + y;
+        }
+    return a[0];
+}
+
+float oracle_grad_sqnorm(const oracle_tensor* T, int n, float* scratch) {
+    float total = 0.0f;
+    for (int t = 0; t < n; ++t) {
+        int64_t tiles = (T[t].numel + 255) / 256;
+        for (int64_t i = 0; i < tiles; ++i) scratch[i] = tile_sqsum(T[t].grad, T[t].numel, i);
+        total = total + pow2_tree(scratch, tiles);
+    }
+    return total;
+}
+
+/* torch's coefficient: max_norm times the FP32 reciprocal of (norm + 1e-6)
+ * (two roundings), clamped above at 1; a NaN norm gives a NaN factor. */
+float oracle_clip_factor(float sqnorm, float max_norm) {
+    float norm = sqrtf(sqnorm);
+    float rcp = 1.0f / (norm + 1e-6f);
+    float c = max_norm * rcp;
+    return (c >= 1.0f) ? 1.0f : c;
+}
+
+static int step_tensor(const oracle_codebooks* cb, const oracle_tensor* T, float lr, float beta1, float beta2,
+                       float eps, float wd, int64_t step, uint64_t seed, int recipe, uint32_t call_flags,
+                       float clip);
+
 int oracle_step_tensor(const oracle_codebooks* cb, const oracle_tensor* T, float lr, float beta1, float beta2,
                        float eps, float wd, int64_t step, uint64_t seed, int recipe, uint32_t call_flags) {
+    return step_tensor(cb, T, lr, beta1, beta2, eps, wd, step, seed, recipe, call_flags, 1.0f);
+}
+
+/* The step with gradients scaled by `clip` (oracle_clip_factor). */
+int oracle_step_tensor_clip(const oracle_codebooks* cb, const oracle_tensor* T, float lr, float beta1, float beta2,
+                            float eps, float wd, int64_t step, uint64_t seed, int recipe, uint32_t call_flags,
+                            float clip) {
+    return step_tensor(cb, T, lr, beta1, beta2, eps, wd, step, seed, recipe, call_flags, clip);
+}
+
+static int step_tensor(const oracle_codebooks* cb, const oracle_tensor* T, float lr, float beta1, float beta2,
+                       float eps, float wd, int64_t step, uint64_t seed, int recipe, uint32_t call_flags,
+                       float clip) {
     if (step < 1 || T->numel < 0) return -1;
     scal_t s = make_scalars(lr, beta1, beta2, eps, wd, step);
     const int factored = (recipe == OR_FACTORED) && (T->flags & OT_FACTORED);
@@ -386,7 +474,7 @@ int oracle_step_tensor(const oracle_codebooks* cb, const oracle_tensor* T, float
     if (factored) {
         if (T->rows < 1 || T->numel % T->rows) return -3;
         cols = T->numel / T->rows;
-        factored_update(&s, T->grad, T->rows, cols, T->v_row, T->v_col, &rbar);
+        factored_update(&s, T->grad, T->rows, cols, T->v_row, T->v_col, &rbar, clip);
     }
     /* Listing page Table 2: ZIP-SR v in Dyn4, ZE-EDEN v in Dyn4-NZ, TorchAO
      * v in Lin4-NZ and m in SDyn4; AReno docs: factored 1-D v excludes zero. */
@@ -406,6 +494,7 @@ int oracle_step_tensor(const oracle_codebooks* cb, const oracle_tensor* T, float
         for (int i = 0; i < n; ++i) {
             int64_t e = e0 + i;
             float g = bf16_to_f32(T->grad[e]);
+            if (clip != 1.0f) g = g * clip;
             float m = Lm[code_at(T->m_codes, e)] * sm_old;
             float mm = fmaf(s.beta1, m, s.omb1 * g);
             float vv;
