@@ -53,6 +53,8 @@ def parse():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0, help="target oracle time of the CPU sample")
+    ap.add_argument("--max-grad-norm", type=float, default=None,
+                    help="time the step with global gradient-norm clipping (sum-of-squares pass + clipped step)")
     ap.add_argument("--tensors", type=int, default=0,
                     help="keep only the first N tensors of the workload (small cases for profiling)")
     ap.add_argument("--tensor-slice", default="",
@@ -195,8 +197,22 @@ def algorithmic_bytes(st, recipe) -> float:
     return total
 
 
-def launches_per_step(st) -> int:
-    return 1 + (4 if any(st.is_factored(s) for s in st.slots) else 0)
+def launches_per_step(st, clip: bool = False) -> int:
+    # step kernel; factored statistics (3 kernels); clipping's sum of squares (3 kernels)
+    return 1 + (3 if any(st.is_factored(s) for s in st.slots) else 0) + (3 if clip else 0)
+
+
+def time_sqnorm(st, stream, iters: int) -> float:
+    """Mean duration (ms) of one q4adamw_grad_sqnorm call (its three kernels)."""
+    import torch
+    st.grad_sqnorm(stream)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(iters):
+        st.grad_sqnorm(stream)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    return e0.elapsed_time(e1) / iters
 
 
 # ---------------------------------------------------------------- CPU oracle sample
@@ -300,8 +316,11 @@ def run_ours(args, rank, world, local):
     st = build_state(w, dev)
     stream = torch.cuda.current_stream(dev)
 
+    mgn = args.max_grad_norm
+
     def one_step(t):
-        st.step(t, h["lr"], h["beta1"], h["beta2"], h["eps"], h["weight_decay"], seed=0, flags=flags, stream=stream)
+        st.step(t, h["lr"], h["beta1"], h["beta2"], h["eps"], h["weight_decay"], seed=0, flags=flags, stream=stream,
+                max_grad_norm=mgn)
 
     t = w.first_step
     for _ in range(args.warmup):
@@ -337,9 +356,10 @@ def run_ours(args, rank, world, local):
         e2e = run_e2e(args, st, w, dev, stream, t)
         t += args.e2e_steps + 1
 
+    sq_ms = time_sqnorm(st, stream, max(3, args.steps)) if mgn is not None else None
     if rank != 0:
         return
-    alg = algorithmic_bytes(st, w.recipe)
+    alg = algorithmic_bytes(st, w.recipe) + (2.0 * w.numel if mgn is not None else 0.0)
     peak, peak_kind = peaks()
     mean_ms = statistics.mean(per)
     achieved = alg / (mean_ms / 1e3) / 1e9
@@ -359,9 +379,18 @@ def run_ours(args, rank, world, local):
                      "traffic": (tr["dram_bytes_per_param"] * w.numel) if tr else None,
                      "algorithmic_bytes": alg, "kernel": "step_kernel (one launch per step)",
                      "frac_of_nominal_8tbs": achieved / NOMINAL_HBM_GBS},
-        "gpu_launches": launches_per_step(st) * args.steps,
+        "gpu_launches": launches_per_step(st, mgn is not None) * args.steps,
         "clocks": clocks,
     }
+    if mgn is not None:
+        # the timed step is the sum-of-squares pass plus the clipped step: the
+        # roofline above covers both (2 more bytes per parameter); the pass is
+        # also timed alone here
+        line["config"]["max_grad_norm"] = mgn
+        line["roofline"]["kernel"] = "sqnorm pass (3 kernels) + step_kernel, per step"
+        line["sqnorm_pass"] = {"ms": sq_ms, "bytes": 2.0 * w.numel,
+                               "achieved_gbs": 2.0 * w.numel / (sq_ms / 1e3) / 1e9,
+                               "frac": 2.0 * w.numel / (sq_ms / 1e3) / 1e9 / peak}
     if e2e:
         line["e2e"] = e2e
     if not args.no_cpu_baseline:
@@ -388,8 +417,9 @@ def run_e2e(args, st, w, dev, stream, t0):
     flags = 1 if w.lm_head_sr else 0
     t = t0
     # one untimed round trip
+    mgn = args.max_grad_norm
     st.grad.copy_(g_host, non_blocking=True)
-    st.step(t, h["lr"], h["beta1"], h["beta2"], h["eps"], h["weight_decay"], 0, flags, stream)
+    st.step(t, h["lr"], h["beta1"], h["beta2"], h["eps"], h["weight_decay"], 0, flags, stream, max_grad_norm=mgn)
     out_host.copy_(st.param_bf16, non_blocking=True)
     torch.cuda.synchronize()
     t += 1
@@ -397,7 +427,7 @@ def run_e2e(args, st, w, dev, stream, t0):
     ev0.record(stream)
     for _ in range(args.e2e_steps):
         st.grad.copy_(g_host, non_blocking=True)
-        st.step(t, h["lr"], h["beta1"], h["beta2"], h["eps"], h["weight_decay"], 0, flags, stream)
+        st.step(t, h["lr"], h["beta1"], h["beta2"], h["eps"], h["weight_decay"], 0, flags, stream, max_grad_norm=mgn)
         out_host.copy_(st.param_bf16, non_blocking=True)
         t += 1
     ev1.record(stream)

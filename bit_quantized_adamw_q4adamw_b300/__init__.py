@@ -22,7 +22,7 @@ from ._native import (BLOCK, Q4_LM_HEAD_SR_ACTIVE, Q4_M_SR_ALL, Q4_T_FACTORED, Q
 
 __all__ = ["q4adamw_version", "q4adamw_strerror", "q4adamw_state_bytes", "q4adamw_workspace_bytes",
            "q4adamw_state_init", "q4adamw_header_check", "q4adamw_step", "q4adamw_step_noalloc",
-           "q4adamw_dequant_state", "q4adamw_step_status",
+           "q4adamw_dequant_state", "q4adamw_step_status", "q4adamw_grad_sqnorm", "q4adamw_step_clip",
            "q4adamw_codebook", "Q4State", "Q4Tensor", "Q4Header", "Q4Error", "RECIPES", "Q4_T_LM_HEAD",
            "Q4_T_FACTORED", "Q4_LM_HEAD_SR_ACTIVE", "Q4_M_SR_ALL", "Q4_V_UPDATE_RTN", "BLOCK"]
 
@@ -92,6 +92,29 @@ def q4adamw_step(tensors, lr, beta1, beta2, eps, weight_decay, step, seed, recip
     _check(lib().q4adamw_step(arr, n, lr, beta1, beta2, eps, weight_decay, int(step), int(seed) & (2 ** 64 - 1),
                               _recipe(recipe), int(flags), ctypes.c_void_p(workspace.data_ptr()),
                               workspace.numel() * workspace.element_size(), _stream(stream)), "q4adamw_step")
+
+
+def q4adamw_grad_sqnorm(tensors, out: torch.Tensor, workspace: torch.Tensor, stream=None) -> None:
+    """Sum of squares of the BF16 gradients into out (a device float32 tensor
+    of one element), in the library's fixed pairwise order."""
+    assert out.dtype == torch.float32 and out.numel() >= 1 and out.is_cuda
+    arr, n = _array(tensors)
+    _check(lib().q4adamw_grad_sqnorm(arr, n, ctypes.c_void_p(out.data_ptr()), ctypes.c_void_p(workspace.data_ptr()),
+                                     workspace.numel() * workspace.element_size(), _stream(stream)),
+           "q4adamw_grad_sqnorm")
+
+
+def q4adamw_step_clip(tensors, lr, beta1, beta2, eps, weight_decay, step, seed, recipe, flags, max_grad_norm,
+                      sqnorm: torch.Tensor, workspace: torch.Tensor, stream=None) -> None:
+    """q4adamw_step with the gradients scaled by the global-norm clip factor
+    min(1, max_grad_norm / (sqrt(sqnorm) + 1e-6)); sqnorm is a device float32."""
+    assert sqnorm.dtype == torch.float32 and sqnorm.is_cuda
+    arr, n = _array(tensors)
+    _check(lib().q4adamw_step_clip(arr, n, lr, beta1, beta2, eps, weight_decay, int(step), int(seed) & (2 ** 64 - 1),
+                                   _recipe(recipe), int(flags), float(max_grad_norm),
+                                   ctypes.c_void_p(sqnorm.data_ptr()), ctypes.c_void_p(workspace.data_ptr()),
+                                   workspace.numel() * workspace.element_size(), _stream(stream)),
+           "q4adamw_step_clip")
 
 
 def q4adamw_step_noalloc(tensors, lr, beta1, beta2, eps, weight_decay, step, seed, recipe, flags,
@@ -187,6 +210,7 @@ class Q4State:
             self.descs[i] = self._desc(sl)
         self.workspace = torch.empty(max(q4adamw_workspace_bytes(self.descs, recipe), 256), dtype=torch.uint8,
                                      device=dev)
+        self.sqnorm = torch.zeros(1, dtype=torch.float32, device=dev)
         self.header = None
 
     def is_factored(self, sl) -> bool:
@@ -237,9 +261,24 @@ class Q4State:
         self.header = q4adamw_state_init(self.descs, self.recipe, stream)
         return self.header
 
-    def step(self, step, lr, beta1, beta2, eps, weight_decay, seed=0, flags=0, stream=None) -> None:
-        q4adamw_step(self.descs, lr, beta1, beta2, eps, weight_decay, step, seed, self.recipe, flags,
-                     self.workspace, stream)
+    def grad_sqnorm(self, stream=None) -> torch.Tensor:
+        """Device float32 sum of squares of the gradient arena's tensors."""
+        q4adamw_grad_sqnorm(self.descs, self.sqnorm, self.workspace, stream)
+        return self.sqnorm
+
+    def step(self, step, lr, beta1, beta2, eps, weight_decay, seed=0, flags=0, stream=None,
+             max_grad_norm=None, sqnorm=None) -> None:
+        """One fused step.  With max_grad_norm the gradients are clipped to that
+        global 2-norm: the sum of squares is `sqnorm` (a device float32, e.g.
+        all-reduced over data-parallel ranks) or, when None, computed here."""
+        if max_grad_norm is None:
+            q4adamw_step(self.descs, lr, beta1, beta2, eps, weight_decay, step, seed, self.recipe, flags,
+                         self.workspace, stream)
+            return
+        if sqnorm is None:
+            sqnorm = self.grad_sqnorm(stream)
+        q4adamw_step_clip(self.descs, lr, beta1, beta2, eps, weight_decay, step, seed, self.recipe, flags,
+                          max_grad_norm, sqnorm, self.workspace, stream)
 
     def status(self, stream=None) -> int:
         """Status word of the last step (0 = completed); synchronises."""

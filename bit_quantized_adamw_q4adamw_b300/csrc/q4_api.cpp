@@ -114,6 +114,34 @@ Layout make_layout(const q4adamw_tensor_t* t, int n, int recipe) {
     return L;
 }
 
+// Workspace layout of q4adamw_grad_sqnorm (same status word at offset 0).
+struct NormLayout {
+    int64_t status, desc, prefix;                  // uploaded part
+    int64_t upload_bytes;
+    int64_t partials, tsums;                       // device-only part
+    int64_t total;
+    int64_t chunks;
+};
+
+int64_t norm_chunks(int64_t numel) {
+    const int64_t tiles = (numel + 255) / 256;
+    return (tiles + q4::kNormChunkTiles - 1) / q4::kNormChunkTiles;
+}
+
+NormLayout make_norm_layout(const q4adamw_tensor_t* t, int n) {
+    NormLayout L{};
+    int64_t off = 0;
+    L.status = off; off = round_up(off + 4, 256);
+    L.desc = off;   off = round_up(off + (int64_t)(n > 0 ? n : 1) * (int64_t)sizeof(q4::NormTensor), 256);
+    L.prefix = off; off = round_up(off + (int64_t)(n + 1) * 8, 256);
+    L.upload_bytes = off;
+    for (int i = 0; i < n; ++i) L.chunks += norm_chunks(t[i].numel);
+    L.partials = off; off = round_up(off + (L.chunks > 0 ? L.chunks : 1) * 4, 256);
+    L.tsums = off;    off = round_up(off + (int64_t)(n > 0 ? n : 1) * 4, 256);
+    L.total = off;
+    return L;
+}
+
 // Host scalars of step t, each computed in double and rounded once to FP32.
 struct Scalars {
     float c2, step_size, decay, omb1, omb2;
@@ -232,7 +260,8 @@ int q4adamw_workspace_bytes(const q4adamw_tensor_t* t, int n, int recipe, int64_
     if (int rc = check_recipe(recipe)) return rc;
     for (int i = 0; i < n; ++i)
         if (int rc = check_shape(t[i], recipe)) return rc;
-    *bytes = make_layout(t, n, recipe).total;
+    const int64_t a = make_layout(t, n, recipe).total, b = make_norm_layout(t, n).total;
+    *bytes = a > b ? a : b;
     return Q4_OK;
 }
 
@@ -280,9 +309,14 @@ int q4adamw_state_init(const q4adamw_tensor_t* t, int n, int recipe, q4adamw_hea
     return Q4_OK;
 }
 
-int q4adamw_step(const q4adamw_tensor_t* t, int n, float lr, float beta1, float beta2, float eps, float weight_decay,
-                 int64_t step, uint64_t seed, int recipe, uint32_t flags, void* workspace, int64_t workspace_bytes,
-                 void* stream) {
+}  // extern "C"
+
+namespace {
+
+// q4adamw_step and q4adamw_step_clip: sqnorm NULL means no clipping.
+int step_impl(const q4adamw_tensor_t* t, int n, float lr, float beta1, float beta2, float eps, float weight_decay,
+              int64_t step, uint64_t seed, int recipe, uint32_t flags, const float* sqnorm, float max_norm,
+              void* workspace, int64_t workspace_bytes, void* stream) {
     if (n < 0 || (n > 0 && !t)) return Q4_EINVAL;
     if (int rc = check_recipe(recipe)) return rc;
     if (step < 1 || step > 0xFFFFFFFFll) return Q4_EINVAL;
@@ -347,6 +381,8 @@ int q4adamw_step(const q4adamw_tensor_t* t, int n, float lr, float beta1, float 
         fp.total_cols = cols[n];
         fp.beta2 = beta2;
         fp.omb2 = hs.omb2;
+        fp.sqnorm = sqnorm;
+        fp.max_norm = max_norm;
         if (int ce = q4::launch_factored(fp, stream)) return cuda_fail((cudaError_t)ce);
     }
 
@@ -372,6 +408,8 @@ int q4adamw_step(const q4adamw_tensor_t* t, int n, float lr, float beta1, float 
     p.fast_math = (eps >= 0x1p-100f && eps <= 0x1p60f) ? 1 : 0;
     p.v_update_rtn = (flags & Q4_V_UPDATE_RTN) ? 1 : 0;
     p.has_m_sr = 0;
+    p.sqnorm = sqnorm;
+    p.max_norm = max_norm;
     for (int i = 0; i < n; ++i) p.has_m_sr |= (desc[i].flags & q4::DF_M_SR) ? 1 : 0;
     p.x2_beta1 = make_float2(p.beta1, p.beta1);
     p.x2_beta2 = make_float2(p.beta2, p.beta2);
@@ -392,6 +430,66 @@ int q4adamw_step(const q4adamw_tensor_t* t, int n, float lr, float beta1, float 
     if ((e = cudaGetDevice(&dev)) != cudaSuccess) return cuda_fail(e);
     const int grid = q4::step_grid_size(dev, p.total_pairs);
     if (int ce = q4::launch_step(p, grid, stream)) return cuda_fail((cudaError_t)ce);
+    return Q4_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int q4adamw_step(const q4adamw_tensor_t* t, int n, float lr, float beta1, float beta2, float eps, float weight_decay,
+                 int64_t step, uint64_t seed, int recipe, uint32_t flags, void* workspace, int64_t workspace_bytes,
+                 void* stream) {
+    return step_impl(t, n, lr, beta1, beta2, eps, weight_decay, step, seed, recipe, flags, nullptr, 1.f, workspace,
+                     workspace_bytes, stream);
+}
+
+int q4adamw_step_clip(const q4adamw_tensor_t* t, int n, float lr, float beta1, float beta2, float eps,
+                      float weight_decay, int64_t step, uint64_t seed, int recipe, uint32_t flags,
+                      float max_grad_norm, const float* sqnorm, void* workspace, int64_t workspace_bytes,
+                      void* stream) {
+    if (!sqnorm || !aligned(sqnorm, 4)) return sqnorm ? Q4_EALIGN : Q4_EINVAL;
+    if (!(max_grad_norm > 0.f) || !std::isfinite(max_grad_norm)) return Q4_EINVAL;
+    return step_impl(t, n, lr, beta1, beta2, eps, weight_decay, step, seed, recipe, flags, sqnorm, max_grad_norm,
+                     workspace, workspace_bytes, stream);
+}
+
+int q4adamw_grad_sqnorm(const q4adamw_tensor_t* t, int n, float* sqnorm, void* workspace, int64_t workspace_bytes,
+                        void* stream) {
+    if (n < 0 || (n > 0 && !t) || !sqnorm) return Q4_EINVAL;
+    if (!aligned(sqnorm, 4)) return Q4_EALIGN;
+    for (int i = 0; i < n; ++i) {
+        if (t[i].numel < 0) return Q4_ESHAPE;
+        if (t[i].numel > 0 && !t[i].grad) return Q4_EINVAL;
+        if (t[i].grad && !aligned(t[i].grad, 16)) return Q4_EALIGN;
+    }
+    const NormLayout L = make_norm_layout(t, n);
+    if (!workspace || !aligned(workspace, 256) || workspace_bytes < L.total) return Q4_EWORKSPACE;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    thread_local std::vector<unsigned char> img;
+    img.assign((size_t)L.upload_bytes, 0);
+    q4::NormTensor* desc = reinterpret_cast<q4::NormTensor*>(img.data() + L.desc);
+    int64_t* prefix = reinterpret_cast<int64_t*>(img.data() + L.prefix);
+    prefix[0] = 0;
+    for (int i = 0; i < n; ++i) {
+        desc[i].grad = t[i].grad;
+        desc[i].numel = t[i].numel;
+        prefix[i + 1] = prefix[i] + norm_chunks(t[i].numel);
+    }
+    cudaError_t e = cudaMemcpyAsync(workspace, img.data(), (size_t)L.upload_bytes, cudaMemcpyHostToDevice, s);
+    if (e != cudaSuccess) return cuda_fail(e);
+    char* ws = static_cast<char*>(workspace);
+    q4::NormParams p{};
+    p.tensors = reinterpret_cast<const q4::NormTensor*>(ws + L.desc);
+    p.chunk_prefix = reinterpret_cast<const int64_t*>(ws + L.prefix);
+    p.n_tensors = n;
+    p.total_chunks = L.chunks;
+    p.partials = reinterpret_cast<float*>(ws + L.partials);
+    p.tensor_sums = reinterpret_cast<float*>(ws + L.tsums);
+    p.out = sqnorm;
+    int dev = 0;
+    if ((e = cudaGetDevice(&dev)) != cudaSuccess) return cuda_fail(e);
+    if (int ce = q4::launch_grad_sqnorm(p, dev, stream)) return cuda_fail((cudaError_t)ce);
     return Q4_OK;
 }
 

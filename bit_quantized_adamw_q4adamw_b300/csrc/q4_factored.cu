@@ -28,16 +28,6 @@
 
 namespace q4 {
 
-// Index of the tensor whose prefix range [prefix[t], prefix[t+1]) holds idx.
-__device__ __forceinline__ int find_tensor(const int64_t* prefix, int n, int64_t idx) {
-    int lo = 0, hi = n - 1;
-    while (lo < hi) {
-        const int mid = (lo + hi + 1) >> 1;
-        if (__ldg(prefix + mid) <= idx) lo = mid; else hi = mid - 1;
-    }
-    return lo;
-}
-
 namespace {
 
 constexpr int kStatsWarps = kSlabRows / 32;   // 8 warps, 32 rows each
@@ -47,6 +37,7 @@ __device__ __forceinline__ float bf16f(uint32_t h) { return __uint_as_float(h <<
 __global__ void __launch_bounds__(kStatsWarps * 32) stats_kernel(const __grid_constant__ FactoredParams P) {
     __shared__ float colsum[kStatsWarps][kSegCols];
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const float clip = clip_factor(P.sqnorm, P.max_norm);   // 1 without clipping
     for (int64_t tile = blockIdx.x; tile < P.total_tiles; tile += gridDim.x) {
         const int t = find_tensor(P.tile_prefix, P.n_tensors, tile);
         const DevTensor& d = P.tensors[t];
@@ -71,7 +62,8 @@ __global__ void __launch_bounds__(kStatsWarps * 32) stats_kernel(const __grid_co
                     const uint32_t h[4] = {w.x, w.y, w.z, w.w};
 #pragma unroll
                     for (int k = 0; k < 4; ++k) {
-                        const float lo = bf16f(h[k] & 0xffffu), hi = bf16f(h[k] >> 16);
+                        const float lo = __fmul_rn(bf16f(h[k] & 0xffffu), clip);
+                        const float hi = __fmul_rn(bf16f(h[k] >> 16), clip);
                         sq[2 * k] = __fmul_rn(lo, lo);
                         sq[2 * k + 1] = __fmul_rn(hi, hi);
                     }
@@ -79,7 +71,7 @@ __global__ void __launch_bounds__(kStatsWarps * 32) stats_kernel(const __grid_co
 #pragma unroll
                     for (int k = 0; k < 8; ++k) {
                         if (k < nc) {
-                            const float x = bf16f(g[k]);
+                            const float x = __fmul_rn(bf16f(g[k]), clip);
                             sq[k] = __fmul_rn(x, x);
                         }
                     }

@@ -88,6 +88,8 @@ struct StepParams {
     int fast_math;                // eps and c2 keep 1/(sqrt(v) c2 + eps) in the fast domain
     int v_update_rtn;             // ZIP-SR with Update-RTN in place of Update-SR
     int has_m_sr;                 // some tensor rounds its first moment stochastically
+    const float* sqnorm;          // global-norm clipping: device sum of squares, or NULL
+    float max_norm;               //   and the clipping threshold
     // the step scalars broadcast to pairs, for the paired FP32 instructions
     float2 x2_beta1, x2_beta2, x2_omb1, x2_omb2, x2_c2, x2_eps, x2_decay, x2_neg_step;
     uint32_t round_keys[20];      // Philox key schedule: (k0, k1) for rounds 0..9
@@ -104,6 +106,27 @@ struct FactoredParams {
     int n_factored;
     int64_t total_rows, total_tiles, total_cols;
     float beta2, omb2;
+    const float* sqnorm;          // as StepParams
+    float max_norm;
+};
+
+// Gradient sum of squares (global-norm clipping).  Chunks are aligned runs of
+// kNormChunkTiles 256-element tiles of one tensor.
+struct NormTensor {
+    const uint16_t* grad;
+    int64_t numel;
+};
+constexpr int kNormWarps = 8;
+constexpr int kNormGroupsPerWarp = 8;                              // 32 tiles per group
+constexpr int64_t kNormChunkTiles = kNormWarps * kNormGroupsPerWarp * 32;   // 2048
+struct NormParams {
+    const NormTensor* tensors;
+    const int64_t* chunk_prefix;  // n+1: chunks of each tensor
+    int n_tensors;
+    int64_t total_chunks;
+    float* partials;              // total_chunks: chunk sums, reduced in place
+    float* tensor_sums;           // n
+    float* out;                   // the sum of squares
 };
 
 constexpr int kSlabRows = 256;     // rows per column-partial slab (8 warps x 32 rows)
@@ -116,6 +139,7 @@ int record_cuda_error(int cuda_error);
 int launch_step(const StepParams& p, int grid, void* stream);
 int step_grid_size(int device, int64_t total_pairs);
 int launch_factored(const FactoredParams& p, void* stream);
+int launch_grad_sqnorm(const NormParams& p, int device, void* stream);
 int launch_dequant(const DevTensor& d, int recipe, const float* nf4, const float* vl, float* m_out, float* v_out,
                    void* stream);
 

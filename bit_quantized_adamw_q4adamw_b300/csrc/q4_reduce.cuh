@@ -1,5 +1,5 @@
-// Deterministic reductions shared by the factored-statistics and the decoding
-// kernels of the q4adamw library.
+// Deterministic reductions and small helpers shared by the step, factored-
+// statistics, gradient-norm and decoding kernels of the q4adamw library.
 #pragma once
 
 #include <cuda_runtime.h>
@@ -7,6 +7,28 @@
 #include <cstdint>
 
 namespace q4 {
+
+// Index of the tensor whose prefix range [prefix[t], prefix[t+1]) holds idx
+// (the last such t when empty ranges share the start).
+__device__ __forceinline__ int find_tensor(const int64_t* prefix, int n, int64_t idx) {
+    int lo = 0, hi = n - 1;
+    while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (__ldg(prefix + mid) <= idx) lo = mid; else hi = mid - 1;
+    }
+    return lo;
+}
+
+// Global-norm clipping factor from the device sum of squares (NULL: 1): the
+// coefficient of torch.nn.utils.clip_grad_norm_, max_norm * (1 / (norm +
+// 1e-6)) with each operation correctly rounded in FP32, clamped above at 1
+// (a NaN sum gives NaN).
+__device__ __forceinline__ float clip_factor(const float* sqnorm, float max_norm) {
+    if (sqnorm == nullptr) return 1.f;
+    const float norm = __fsqrt_rn(__ldg(sqnorm));
+    const float c = __fmul_rn(max_norm, __frcp_rn(__fadd_rn(norm, 1e-6f)));
+    return c >= 1.f ? 1.f : c;
+}
 
 // Mean of R[0..rows) by one CTA of exactly 256 threads in a fixed order:
 // thread t sums R[t], R[t+256], ... left to right, then a binary tree over the

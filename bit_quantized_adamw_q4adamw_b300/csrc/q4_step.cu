@@ -46,6 +46,7 @@
 
 #include "q4_fastmath.cuh"
 #include "q4_internal.h"
+#include "q4_reduce.cuh"
 
 namespace q4 {
 namespace {
@@ -587,7 +588,7 @@ template <int RECIPE, bool URTN>
 __device__ __forceinline__ void compute_tile(const StepParams& P, const DevTensor& d, int64_t pair,
                                              const Stage* st, int lane, SmemAll& sm, WarpTables& wt,
                                              const float my_nf4, const float my_nf4t, const float my_vl,
-                                             const float my_vt) {
+                                             const float my_vt, const float clip) {
     const int half = lane >> 4, j = lane & 15, hb = half * 16;
     const int64_t numel = d.numel;
     const int64_t nblk = (numel + kBlock - 1) / kBlock;
@@ -644,6 +645,10 @@ __device__ __forceinline__ void compute_tile(const StepParams& P, const DevTenso
             }
         }
     }
+
+    // global-norm clipping scales the FP32 gradient first (1 when off)
+#pragma unroll
+    for (int i = 0; i < 8; ++i) g[i] = __fmul_rn(g[i], clip);
 
     // ---- dequantisation (old scales) and update --------------------------
     wt.deqm[hb + j] = __fmul_rn(my_nf4, sm_old);
@@ -703,7 +708,7 @@ template <int RECIPE, bool URTN, bool MSR>
 __device__ __forceinline__ void compute_tile_full(const StepParams& P, const DevTensor& d, int64_t pair,
                                                   const Stage& st, int lane, SmemAll& sm, WarpTables& wt,
                                                   const float my_nf4, const float my_nf4t, const float my_vl,
-                                                  const float my_vt, const float my_vl1) {
+                                                  const float my_vt, const float my_vl1, const float clip) {
     const int half = lane >> 4, j = lane & 15, hb = half * 16;
     const int64_t blk = pair * 2 + half;
     const int64_t e0 = blk * kBlock + j * 8;
@@ -726,6 +731,9 @@ __device__ __forceinline__ void compute_tile_full(const StepParams& P, const Dev
         g[1] = make_float2(bf16lo(gw.y), bf16hi(gw.y));
         g[2] = make_float2(bf16lo(gw.z), bf16hi(gw.z));
         g[3] = make_float2(bf16lo(gw.w), bf16hi(gw.w));
+        const float2 clip2 = make_float2(clip, clip);   // global-norm clipping (1 when off)
+#pragma unroll
+        for (int k = 0; k < 4; ++k) g[k] = mul2_rn(g[k], clip2);
         th[0] = make_float2(t0.x, t0.y);
         th[1] = make_float2(t0.z, t0.w);
         th[2] = make_float2(t1.x, t1.y);
@@ -995,6 +1003,7 @@ __global__ void __launch_bounds__(kStepThreads, 1) step_kernel(const __grid_cons
     const float my_nf4 = P.tab.nf4[j], my_nf4t = P.tab.nf4_t[j];
     const float my_vl = P.tab.vl[j], my_vt = P.tab.vt[j];
     const float my_vl1 = P.tab.vl[j < 15 ? j + 1 : 15];
+    const float clip = clip_factor(P.sqnorm, P.max_norm);
     const uint64_t policy = evict_first_policy();
 
     // Work split: the global tile list is cut into chunks of kChunk consecutive
@@ -1162,11 +1171,11 @@ __global__ void __launch_bounds__(kStepThreads, 1) step_kernel(const __grid_cons
         const bool full = c_p < c_n - 1 || ws.desc.numel - c_p * 2 * kBlock >= 2 * kBlock;
         if (full) {
             compute_tile_full<RECIPE, URTN, MSR>(P, ws.desc, c_p, ws.st[s], lane, sm, ws.wt, my_nf4, my_nf4t,
-                                                 my_vl, my_vt, my_vl1);
+                                                 my_vl, my_vt, my_vl1, clip);
         } else {
             const int64_t left = ws.desc.numel - c_p * 2 * kBlock;
             compute_tile<RECIPE, URTN>(P, ws.desc, c_p, (left & 7) == 0 ? &ws.st[s] : nullptr, lane, sm, ws.wt,
-                                       my_nf4, my_nf4t, my_vl, my_vt);
+                                       my_nf4, my_nf4t, my_vl, my_vt, clip);
         }
         ++c_p;
         ++c_tile;

@@ -163,9 +163,10 @@ int q4adamw_last_cuda_error(void);
 int q4adamw_state_bytes(const q4adamw_tensor_t* t, int n, int recipe, int64_t* quantized, int64_t* scale_meta,
                         int64_t* total);
 
-/* Device workspace q4adamw_step needs for this tensor list (host-only).  The
- * workspace holds the descriptor table and, for factored tensors, the
- * partial row/column sums.  It must be 256-B aligned. */
+/* Device workspace q4adamw_step, q4adamw_step_clip and q4adamw_grad_sqnorm
+ * need for this tensor list (host-only).  The workspace holds the descriptor
+ * table, for factored tensors the partial row/column sums, and the
+ * gradient-norm partial sums.  It must be 256-B aligned. */
 int q4adamw_workspace_bytes(const q4adamw_tensor_t* t, int n, int recipe, int64_t* bytes);
 
 /*
@@ -209,6 +210,37 @@ int q4adamw_step(const q4adamw_tensor_t* t, int n, float lr, float beta1, float 
                  void* stream);
 /* (flags: any bit outside Q4_LM_HEAD_SR_ACTIVE | Q4_M_SR_ALL | Q4_V_UPDATE_RTN,
  * or Q4_V_UPDATE_RTN with a recipe other than ZIP-SR, returns Q4_EINVAL.) */
+
+/*
+ * Global gradient-norm clipping (AReno docs "4-bit AdamW", section "State
+ * representation": gradient norm and clipping operate directly on the BF16
+ * gradient shards), in two calls on one stream:
+ *
+ * q4adamw_grad_sqnorm writes to *sqnorm (one device float, 4-B aligned,
+ * caller-owned) the FP32 sum of squares of the BF16 gradients of t[0..n):
+ * per tensor, recursive pairwise summation of the squares (the tensor padded
+ * with zeros to a power of two, adjacent pairs added at every level), then
+ * the tensor sums added left to right from 0.  The result does not depend on
+ * launch geometry.  Reads grad and numel of each tensor only (grad 16-B
+ * aligned, may be NULL when numel is 0).  workspace as for q4adamw_step
+ * (q4adamw_workspace_bytes covers both calls; the calls must not overlap on
+ * it).  A data-parallel caller sums *sqnorm over the ranks (for instance an
+ * all-reduce) before the step.
+ *
+ * q4adamw_step_clip is q4adamw_step with every FP32 gradient first multiplied
+ * by clip = min(1, max_grad_norm * (1 / (sqrt(*sqnorm) + 1e-6))), each
+ * operation correctly rounded in FP32 -- the coefficient of PyTorch's
+ * clip_grad_norm_ for the 2-norm.  The factor applies before the moments and
+ * the factored statistics.  *sqnorm is read on the device when the step runs.
+ * max_grad_norm must be finite and > 0 (else Q4_EINVAL); sqnorm NULL is
+ * Q4_EINVAL, misaligned Q4_EALIGN.  A NaN sum of squares gives NaN updates.
+ */
+int q4adamw_grad_sqnorm(const q4adamw_tensor_t* t, int n, float* sqnorm, void* workspace, int64_t workspace_bytes,
+                        void* stream);
+int q4adamw_step_clip(const q4adamw_tensor_t* t, int n, float lr, float beta1, float beta2, float eps,
+                      float weight_decay, int64_t step, uint64_t seed, int recipe, uint32_t flags,
+                      float max_grad_norm, const float* sqnorm, void* workspace, int64_t workspace_bytes,
+                      void* stream);
 
 /*
  * Status word of the most recent q4adamw_step that used `workspace`

@@ -55,15 +55,25 @@ class Pair:
         self.gpu.init()
         torch.cuda.synchronize()
 
-    def step(self, t, grads, seed=0, flags=0, hyper=HYPER):
-        """grads: list of CPU bfloat16 tensors (one per tensor)."""
+    def step(self, t, grads, seed=0, flags=0, hyper=HYPER, max_grad_norm=None):
+        """grads: list of CPU bfloat16 tensors (one per tensor).  With
+        max_grad_norm both sides clip by the global norm; the GPU's sum of
+        squares must then equal the oracle's bit for bit (asserted)."""
         for i, g in enumerate(grads):
             self.gpu.view(i, "grad").copy_(g)
         self.gpu.step(t, hyper["lr"], hyper["beta1"], hyper["beta2"], hyper["eps"], hyper["weight_decay"], seed,
-                      flags)
+                      flags, max_grad_norm=max_grad_norm)
+        clip = None
+        if max_grad_norm is not None:
+            bits = [bf16_bits(g) for g in grads]
+            sq = O.grad_sqnorm(bits)
+            got = np.float32(self.gpu.sqnorm.cpu().numpy()[0])
+            assert got.view(np.uint32) == sq.view(np.uint32), (t, got, sq)
+            clip = O.clip_factor(sq, max_grad_norm)
+            self.last_clip = float(clip)
         for i, g in enumerate(grads):
             self.ora[i].step(bf16_bits(g), hyper["lr"], hyper["beta1"], hyper["beta2"], hyper["eps"],
-                             hyper["weight_decay"], t, seed, self.recipe, flags)
+                             hyper["weight_decay"], t, seed, self.recipe, flags, clip=clip)
         torch.cuda.synchronize()
 
     def compare(self, exact_theta=True, rc_rtol=1e-5, theta_tol=1e-6):

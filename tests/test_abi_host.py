@@ -137,6 +137,55 @@ def test_step_validation_happens_before_any_device_work():
     assert call(arr=nog) == _native.Q4_EINVAL
 
 
+def test_clip_entry_points_validate_before_any_device_work():
+    L = _native.lib()
+    ws = ctypes.c_void_p(1 << 41)
+    arr = (q4.Q4Tensor * 1)(_valid_fake_tensor())
+    sq = ctypes.c_void_p((1 << 41) + (1 << 30))
+
+    def clip(max_norm=1.0, sqnorm=sq, arr=arr, flags=0, wsb=1 << 20):
+        return L.q4adamw_step_clip(arr, 1, 1e-3, 0.9, 0.999, 1e-8, 0.1, 1, 0, 0, flags, max_norm, sqnorm, ws, wsb,
+                                   None)
+
+    assert clip(max_norm=0.0) == _native.Q4_EINVAL
+    assert clip(max_norm=-1.0) == _native.Q4_EINVAL
+    assert clip(max_norm=float("nan")) == _native.Q4_EINVAL
+    assert clip(max_norm=float("inf")) == _native.Q4_EINVAL
+    assert clip(sqnorm=ctypes.c_void_p(0)) == _native.Q4_EINVAL
+    assert clip(sqnorm=ctypes.c_void_p((1 << 41) + 2)) == _native.Q4_EALIGN
+    assert clip(flags=0x8) == _native.Q4_EINVAL
+    assert clip(wsb=16) == _native.Q4_EWORKSPACE
+
+    def norm(arr=arr, n=1, out=sq, ws=ws, wsb=1 << 20):
+        return L.q4adamw_grad_sqnorm(arr, n, out, ws, wsb, None)
+
+    assert norm(out=ctypes.c_void_p(0)) == _native.Q4_EINVAL
+    assert norm(out=ctypes.c_void_p((1 << 41) + 1)) == _native.Q4_EALIGN
+    assert norm(n=-1) == _native.Q4_EINVAL
+    assert norm(ws=ctypes.c_void_p(0)) == _native.Q4_EWORKSPACE
+    assert norm(ws=ctypes.c_void_p((1 << 41) + 16)) == _native.Q4_EWORKSPACE
+    assert norm(wsb=16) == _native.Q4_EWORKSPACE
+    mis = (q4.Q4Tensor * 1)(_valid_fake_tensor())
+    mis[0].grad = mis[0].grad + 2
+    assert norm(arr=mis) == _native.Q4_EALIGN
+    nog = (q4.Q4Tensor * 1)(_valid_fake_tensor())
+    nog[0].grad = 0
+    assert norm(arr=nog) == _native.Q4_EINVAL
+    neg = (q4.Q4Tensor * 1)(_valid_fake_tensor())
+    neg[0].numel = -1
+    assert norm(arr=neg) == _native.Q4_ESHAPE
+
+
+def test_workspace_covers_the_norm_partials():
+    # one huge tensor: few descriptors, many 2048-tile chunk partials
+    L = _native.lib()
+    n = ctypes.c_int64()
+    big = (q4.Q4Tensor * 1)(_t(1 << 34, rows=1))
+    assert L.q4adamw_workspace_bytes(big, 1, 0, ctypes.byref(n)) == 0
+    chunks = (1 << 34) // (256 * 2048)
+    assert n.value >= chunks * 4
+
+
 @pytest.mark.skipif(torch.cuda.is_available(), reason="checks the no-GPU behaviour")
 def test_valid_step_without_gpu_fails_loudly():
     # No CPU fallback: a well-formed call on a machine without a GPU is a CUDA error.

@@ -59,7 +59,7 @@ def _free(st):
     torch.cuda.empty_cache()
 
 
-def _run_packed(w, steps, flags, tensor_filter=None):
+def _run_packed(w, steps, flags, tensor_filter=None, max_grad_norm=None):
     """Step the whole workload on the GPU; check sampled blocks of the tensors
     tensor_filter accepts (all packed ones by default) against the oracle."""
     dev = torch.device("cuda", 0)
@@ -88,12 +88,22 @@ def _run_packed(w, steps, flags, tensor_filter=None):
             lo = b * BLOCK
             hi = lo + o.param.size
             host_g[(i, b)] = bf16_bits(grads[i][lo:hi])
-        st.step(t, h["lr"], h["beta1"], h["beta2"], h["eps"], h["weight_decay"], seed=0, flags=flags)
+        clip = None
+        if max_grad_norm is not None:
+            # the oracle's global sum of squares over every gradient of the workload
+            sq = O.grad_sqnorm([bf16_bits(st.view(i, "grad")) for i in range(len(w.tensors))])
+            clip = O.clip_factor(sq, max_grad_norm)
+        st.step(t, h["lr"], h["beta1"], h["beta2"], h["eps"], h["weight_decay"], seed=0, flags=flags,
+                max_grad_norm=max_grad_norm)
         torch.cuda.synchronize()
         assert st.status() == 0
+        if max_grad_norm is not None:
+            got = np.float32(st.sqnorm.cpu().numpy()[0])
+            assert got.view(np.uint32) == sq.view(np.uint32), (w.name, t, got, sq)
+            assert float(clip) < 1.0
         for i, b, o in samples:
             o.step(host_g[(i, b)], h["lr"], h["beta1"], h["beta2"], h["eps"], h["weight_decay"], t, 0, w.recipe,
-                   flags)
+                   flags, clip=clip)
             lo, n = b * BLOCK, o.param.size
             th = st.view(i, "param")[lo:lo + n].cpu().numpy()
             assert not neq_f32(th, o.param).any(), (w.name, i, b, t, "param")
@@ -114,6 +124,15 @@ def _run_packed(w, steps, flags, tensor_filter=None):
 def test_gpt1p4b_zipsr_lm_head_sr_sampled_blocks():
     w = W.WORKLOADS["gpt1p4b_zipsr"]
     n = _run_packed(w, 2, q4.Q4_LM_HEAD_SR_ACTIVE)
+    assert n >= 2 * 4 * 100
+
+
+def test_gpt1p4b_zipsr_clipped_sampled_blocks():
+    # global-norm clipping at the full 1.4B size: the GPU's sum of squares over
+    # all 1.4B gradients equals the oracle's bit for bit, and sampled blocks of
+    # the clipped step match
+    w = W.WORKLOADS["gpt1p4b_zipsr"]
+    n = _run_packed(w, 2, q4.Q4_LM_HEAD_SR_ACTIVE, max_grad_norm=1e-3)
     assert n >= 2 * 4 * 100
 
 
