@@ -102,3 +102,71 @@ def test_partition_covers_every_block_once():
                     assert key not in seen
                     seen[key] = r
         assert len(seen) == sum(numels)
+
+
+def _clip_worker(rank, world, port, q):
+    """Data-parallel global-norm clipping: each rank sums the squares of its
+    own shards' gradients, one all-reduce (SUM) gives every rank the same
+    total, and each rank steps its shards with the resulting factor."""
+    from oracle import oracle as O
+    os.environ["MASTER_ADDR"] = "127.0.0.1"
+    os.environ["MASTER_PORT"] = str(port)
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    try:
+        w = W.custom("mr", SHAPES, "zip_sr", flags=FLAGS)
+        shards = sharding.partition([int(np.prod(s)) for s in SHAPES], world, rank)
+        grads = [W.draw_grad(w, w.tensors[sh.tensor], sh.tensor, 1)[sh.start:sh.start + sh.numel].contiguous()
+                 .view(torch.int16).numpy().view(np.uint16) for sh in shards]
+        local = torch.tensor([float(O.grad_sqnorm(grads))], dtype=torch.float32)
+        dist.all_reduce(local)
+        clip = O.clip_factor(np.float32(local.item()), 0.05)
+        h = W.HYPER
+        outs = []
+        for sh, g in zip(shards, grads):
+            spec = w.tensors[sh.tensor]
+            th = W.init_param(spec, sh.tensor).numpy()[sh.start:sh.start + sh.numel]
+            t = O.OracleTensor.zeros_state(th, sh.tensor, flags=spec.flags, elem_offset=sh.elem_offset)
+            t.step(g, h["lr"], h["beta1"], h["beta2"], h["eps"], h["weight_decay"], 1, 11, "zip_sr", 0, clip=clip)
+            outs.append((sh.tensor, sh.start, t.param.copy()))
+        gathered = [None] * world
+        dist.all_gather_object(gathered, (float(local.item()), float(clip), outs))
+        if rank == 0:
+            q.put(gathered)
+    finally:
+        dist.destroy_process_group()
+
+
+def test_two_rank_global_norm_clipping():
+    from oracle import oracle as O
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    port = _free_port()
+    procs = [ctx.Process(target=_clip_worker, args=(r, 2, port, q)) for r in range(2)]
+    for p in procs:
+        p.start()
+    gathered = q.get(timeout=300)
+    for p in procs:
+        p.join(timeout=60)
+        assert p.exitcode == 0
+    totals = {g[0] for g in gathered}
+    clips = {g[1] for g in gathered}
+    assert len(totals) == 1 and len(clips) == 1            # every rank clips with the same factor
+    total, clip = totals.pop(), clips.pop()
+    # the all-reduced sum differs from the single-rank order only by rounding
+    w = W.custom("mr", SHAPES, "zip_sr", flags=FLAGS)
+    whole_g = [W.draw_grad(w, s, i, 1).view(torch.int16).numpy().view(np.uint16) for i, s in enumerate(w.tensors)]
+    single = float(O.grad_sqnorm(whole_g))
+    assert abs(total - single) <= 32 * 2.0 ** -24 * single
+    assert clip < 1.0
+    # with one factor the sharded step equals the whole-tensor step bit for bit
+    h = W.HYPER
+    parts = {}
+    for _, _, outs in gathered:
+        for tensor, start, th in outs:
+            parts.setdefault(tensor, []).append((start, th))
+    for i, s in enumerate(w.tensors):
+        t = O.OracleTensor.zeros_state(W.init_param(s, i).numpy(), i, flags=s.flags)
+        t.step(whole_g[i], h["lr"], h["beta1"], h["beta2"], h["eps"], h["weight_decay"], 1, 11, "zip_sr", 0,
+               clip=np.float32(clip))
+        ps = sorted(parts[i], key=lambda x: x[0])
+        assert np.array_equal(np.concatenate([p[1] for p in ps]), t.param)
