@@ -58,6 +58,7 @@ T_FACTORED = 2
 LM_HEAD_SR_ACTIVE = 1
 M_SR_ALL = 2          # State-SR for the first moment of every tensor (ablation)
 V_UPDATE_RTN = 4      # Update-RTN instead of Update-SR under ZIP-SR (ablation)
+V_NEXT_R = 8          # ZIP-SR rounds in the next step's zero-gradient preconditioner (ablation)
 PURPOSE_M_SR = 0
 PURPOSE_V_SR = 1
 RULES = {"state_rtn": 0, "state_sr": 1, "update_rtn": 2, "update_sr": 3}
@@ -117,6 +118,8 @@ def lib():
         L.oracle_host_scalars.argtypes = [F, F, F, F, I64, P]
         L.oracle_quant_block.argtypes = [P, P, P, ctypes.c_int, ctypes.c_int, P, F, F, P]
         L.oracle_quant_block.restype = F
+        L.oracle_quant_block_r.argtypes = [P, P, P, ctypes.c_int, ctypes.c_int, P, F, F, F, P]
+        L.oracle_quant_block_r.restype = F
         L.oracle_eden_scale.argtypes = [P, P, ctypes.c_int, P, F]
         L.oracle_eden_scale.restype = F
         L.oracle_dequant.argtypes = [P, P, P, I64, P]
@@ -179,8 +182,11 @@ def host_scalars(lr, beta1, beta2, weight_decay, step) -> dict:
     return dict(zip(("bc1", "c2", "step_size", "decay", "omb1", "omb2"), out.tolist()))
 
 
-def quant_block(levels, thresholds, x, rule: str, words=None, c2=1.0, eps=1e-8):
-    """Quantise one block (len <= 128) with one of the four Table 1 rules."""
+def quant_block(levels, thresholds, x, rule: str, words=None, c2=1.0, eps=1e-8, rbeta=None):
+    """Quantise one block (len <= 128) with one of the four Table 1 rules.
+    The Update rules round in r(x) = 1/(sqrt(x) c2 + eps), or with rbeta in
+    r(x) = 1/(sqrt(rbeta x) c2 + eps) (the next-step variant: rbeta = beta2,
+    c2 of step t+1)."""
     x = np.ascontiguousarray(x, dtype=np.float32)
     n = x.size
     assert n <= BLOCK
@@ -188,7 +194,11 @@ def quant_block(levels, thresholds, x, rule: str, words=None, c2=1.0, eps=1e-8):
     t = np.ascontiguousarray(thresholds, dtype=np.float32)
     w = np.zeros(max(n, 1), np.uint32) if words is None else np.ascontiguousarray(words, dtype=np.uint32)
     codes = np.zeros(max(n, 1), dtype=np.uint8)
-    s = lib().oracle_quant_block(_ptr(L), _ptr(t), _ptr(x), n, RULES[rule], _ptr(w), c2, eps, _ptr(codes))
+    if rbeta is None:
+        s = lib().oracle_quant_block(_ptr(L), _ptr(t), _ptr(x), n, RULES[rule], _ptr(w), c2, eps, _ptr(codes))
+    else:
+        s = lib().oracle_quant_block_r(_ptr(L), _ptr(t), _ptr(x), n, RULES[rule], _ptr(w), rbeta, c2, eps,
+                                       _ptr(codes))
     return codes[:n], np.float32(s)
 
 

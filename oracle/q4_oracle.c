@@ -40,7 +40,7 @@ enum { OT_LM_HEAD = 1u, OT_FACTORED = 2u };
  * variants of the listing page's ablations: State-SR for the first moment of
  * every tensor, and Update-RTN in place of Update-SR under ZIP-SR (Table 1
  * rules). */
-enum { OS_LM_HEAD_SR_ACTIVE = 1u, OS_M_SR_ALL = 2u, OS_V_UPDATE_RTN = 4u };
+enum { OS_LM_HEAD_SR_ACTIVE = 1u, OS_M_SR_ALL = 2u, OS_V_UPDATE_RTN = 4u, OS_V_NEXT_R = 8u };
 enum { OP_M_SR = 0u, OP_V_SR = 1u };
 
 /* ------------------------------------------------------------------ */
@@ -121,6 +121,7 @@ void oracle_host_scalars(float lr, float beta1, float beta2, float weight_decay,
 typedef struct {
     float beta1, beta2, eps;
     float c2, step_size, decay, omb1, omb2;
+    float rb, rc;   /* the rules' preconditioner space: r(x) = 1 / (sqrt(rb * x) * rc + eps) */
 } scal_t;
 
 static scal_t make_scalars(float lr, float beta1, float beta2, float eps, float wd, int64_t t) {
@@ -129,6 +130,7 @@ static scal_t make_scalars(float lr, float beta1, float beta2, float eps, float 
     scal_t s;
     s.beta1 = beta1; s.beta2 = beta2; s.eps = eps;
     s.c2 = h[1]; s.step_size = h[2]; s.decay = h[3]; s.omb1 = h[4]; s.omb2 = h[5];
+    s.rb = 1.0f; s.rc = s.c2;
     return s;
 }
 
@@ -136,6 +138,14 @@ static scal_t make_scalars(float lr, float beta1, float beta2, float eps, float 
  * ZIP-SR chooses its rounding probabilities (listing page Abstract,
  * Table 1 "Precond. error"). */
 static float precond(float x, const scal_t* s) { return 1.0f / (sqrtf(x) * s->c2 + s->eps); }
+
+/* The preconditioner in which the Update rules round.  By default rb = 1,
+ * rc = c2, so rule_r(x) = precond(x) exactly (1 * x is exact): the r the
+ * update of the same step used.  The next-step variant (Table 1 evaluates
+ * the preconditioner error at step t+1 with |g_{t+1}| = O(eps)) takes the
+ * next step's zero-gradient preconditioner: rb = beta2, rc = 1 /
+ * sqrt(1 - beta2^(t+1)). */
+static float rule_r(float x, const scal_t* s) { return 1.0f / (sqrtf(s->rb * x) * s->rc + s->eps); }
 
 /* ------------------------------------------------------------------ */
 /* Rounding rules on one value, given the block's scaled levels          */
@@ -174,8 +184,8 @@ static int rule_state_sr(const float a[16], float x, float u) {
 static int rule_update_sr(const float a[16], float x, float r, float u, const scal_t* s) {
     int k = cell_of(a, x);
     if (k == 15) return 15;
-    float rk = precond(a[k], s);
-    float rk1 = precond(a[k + 1], s);
+    float rk = rule_r(a[k], s);
+    float rk1 = rule_r(a[k + 1], s);
     return (u * (rk - rk1) < (rk - r)) ? k + 1 : k;
 }
 
@@ -184,8 +194,8 @@ static int rule_update_sr(const float a[16], float x, float r, float u, const sc
 static int rule_update_rtn(const float a[16], float x, float r, const scal_t* s) {
     int k = cell_of(a, x);
     if (k == 15) return 15;
-    float rk = precond(a[k], s);
-    float rk1 = precond(a[k + 1], s);
+    float rk = rule_r(a[k], s);
+    float rk1 = rule_r(a[k + 1], s);
     return ((r - rk1) < (rk - r)) ? k + 1 : k;
 }
 
@@ -265,12 +275,14 @@ static int code_at(const uint8_t* packed, int64_t e) {
  * t for RTN).  words[i] are the 32-bit draws for SR rules; c2/eps define
  * r for the Update rules (lr etc. do not enter).  Writes codes[0..n) and
  * returns the block scale s = max|x|. */
-float oracle_quant_block(const float L[16], const float t[15], const float* x, int n, int rule,
-                         const uint32_t* words, float c2, float eps, uint8_t* codes) {
+float oracle_quant_block_r(const float L[16], const float t[15], const float* x, int n, int rule,
+                           const uint32_t* words, float rb, float rc, float eps, uint8_t* codes) {
     scal_t sc;
     memset(&sc, 0, sizeof sc);
-    sc.c2 = c2;
+    sc.c2 = rc;
     sc.eps = eps;
+    sc.rb = rb;
+    sc.rc = rc;
     float s = block_absmax(x, n);
     float a[16], T[15];
     scale_tables(L, t, s, a, T);
@@ -279,13 +291,20 @@ float oracle_quant_block(const float L[16], const float t[15], const float* x, i
         switch (rule) {
             case RULE_STATE_RTN: c = rule_state_rtn(T, x[i]); break;
             case RULE_STATE_SR: c = rule_state_sr(a, x[i], oracle_uniform(words[i])); break;
-            case RULE_UPDATE_RTN: c = rule_update_rtn(a, x[i], precond(x[i], &sc), &sc); break;
-            case RULE_UPDATE_SR: c = rule_update_sr(a, x[i], precond(x[i], &sc), oracle_uniform(words[i]), &sc); break;
+            case RULE_UPDATE_RTN: c = rule_update_rtn(a, x[i], rule_r(x[i], &sc), &sc); break;
+            case RULE_UPDATE_SR: c = rule_update_sr(a, x[i], rule_r(x[i], &sc), oracle_uniform(words[i]), &sc); break;
             default: c = 0;
         }
         codes[i] = (uint8_t)c;
     }
     return s;
+}
+
+/* As oracle_quant_block_r with the Update rules in the same-step space
+ * r(x) = 1 / (sqrt(x) * c2 + eps). */
+float oracle_quant_block(const float L[16], const float t[15], const float* x, int n, int rule,
+                         const uint32_t* words, float c2, float eps, uint8_t* codes) {
+    return oracle_quant_block_r(L, t, x, n, rule, words, 1.0f, c2, eps, codes);
 }
 
 float oracle_eden_scale(const float* v, const uint8_t* q, int n, const float L[16], float s) {
@@ -469,6 +488,13 @@ static int step_tensor(const oracle_codebooks* cb, const oracle_tensor* T, float
     const int m_sr = ((T->flags & OT_LM_HEAD) && (call_flags & OS_LM_HEAD_SR_ACTIVE) && recipe != OR_TORCHAO) ||
                      (call_flags & OS_M_SR_ALL);
     const int v_update_rtn = (recipe == OR_ZIP_SR) && (call_flags & OS_V_UPDATE_RTN);
+    const int v_next_r = (recipe == OR_ZIP_SR) && (call_flags & OS_V_NEXT_R);
+    if (v_next_r) {
+        float hn[6];
+        oracle_host_scalars(lr, beta1, beta2, wd, step + 1, hn);
+        s.rb = beta2;
+        s.rc = hn[1];
+    }
     int64_t cols = 0;
     float rbar = 0.0f;
     if (factored) {
@@ -536,6 +562,8 @@ static int step_tensor(const oracle_codebooks* cb, const oracle_tensor* T, float
         float sv = block_absmax(v1, n);
         float av[16], Tv[15];
         scale_tables(Lv, tv, sv, av, Tv);
+        if (recipe == OR_ZIP_SR && v_next_r)
+            for (int i = 0; i < n; ++i) r[i] = rule_r(v1[i], &s);
         if (recipe == OR_ZIP_SR && v_update_rtn) {
             for (int i = 0; i < n; ++i) qv[i] = (uint8_t)rule_update_rtn(av, v1[i], r[i], &s);
         } else if (recipe == OR_ZIP_SR) {

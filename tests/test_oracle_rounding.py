@@ -188,3 +188,55 @@ def test_zero_block_codes():
         assert np.all(c == 15)
         c, _ = O.quant_block(L, t, x, "state_sr", words=O.draws(1, 1, 0, 0, 128, 1))
         assert np.all(c == 15)
+
+
+def r_next(x, b2, c2n, eps):
+    """Next-step zero-gradient preconditioner 1/(sqrt(b2 x) c2n + eps), float64."""
+    return 1.0 / (np.sqrt(b2 * np.asarray(x, np.float64)) * c2n + eps)
+
+
+def test_next_step_update_sr_is_unbiased_in_next_step_r():
+    # the next-step variant of ZIP-SR: E[r'(Q)] = r'(v) for r' evaluated at
+    # step t+1 with a zero gradient (beta2 = 0.8, step t = 2)
+    rng = np.random.default_rng(4)
+    L, t = O.codebooks()["dyn4"], O.codebooks()["dyn4_t"]
+    b2, eps = 0.8, 1e-2
+    c2n = float(np.float32(1.0 / np.sqrt(1.0 - b2 ** 3)))
+    x = np.minimum(np.abs(rng.normal(0, 0.5, 16)) ** 3, 1.9).astype(np.float32)
+    x[0] = 2.0
+    x[1] = 2e-4
+    n = 40000
+    w_all = O.draws(12, 1, 0, 0, n * 16, 1).reshape(n, 16)
+    rs = np.zeros(16)
+    rs2 = np.zeros(16)
+    for i in range(n):
+        cu, s = O.quant_block(L, t, x, "update_sr", words=w_all[i], c2=c2n, eps=eps, rbeta=b2)
+        rq = r_next(L[cu].astype(np.float64) * float(s), b2, c2n, eps)
+        rs += rq
+        rs2 += rq * rq
+    mr = rs / n
+    sr = np.sqrt(np.maximum(rs2 / n - mr ** 2, 0) / n)
+    xr = r_next(x, b2, c2n, eps)
+    assert np.all(np.abs(mr - xr) <= 4.5 * sr + 1e-5 * xr)
+
+
+@pytest.mark.parametrize("eps", [1e-3, 1e-4])
+def test_next_step_update_sr_near_zero_probability(eps):
+    # Table 1's cell next to zero in the next-step space: P(Q=0) =
+    # (r'(v) - r'(b)) / (r'(0) - r'(b)), still Theta(eps)
+    L, t, x, b = _near_zero_block(0.1)
+    b2, c2n = 0.9, 1.25
+    n = 60000
+    w = O.draws(5, 1, 0, 0, n, 1)
+    codes = np.empty(n, np.uint8)
+    for i in range(n):
+        c, _ = O.quant_block(L, t, x, "update_sr", words=np.array([w[i], 0], np.uint32), c2=c2n, eps=eps,
+                             rbeta=b2)
+        codes[i] = c[0]
+    p0 = (codes == 0).mean()
+    v = float(x[0])
+    r_v, r_b, r_0 = r_next(v, b2, c2n, eps), r_next(b, b2, c2n, eps), 1.0 / eps
+    p_exact = (r_v - r_b) / (r_0 - r_b)
+    assert abs(p0 - p_exact) < 4.5 * np.sqrt(p_exact * (1 - p_exact) / n) + 1e-6
+    lim = (1.0 / np.sqrt(v) - 1.0 / np.sqrt(b)) / (np.sqrt(b2) * c2n)
+    assert 0.3 < p_exact / (eps * lim) < 1.7

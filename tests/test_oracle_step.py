@@ -327,3 +327,43 @@ def test_v_update_rtn_takes_the_level_nearer_in_preconditioner_space():
         assert np.all((got == k) | (got == k1))
         chosen = np.where(got == k, d_lo, d_hi)
         assert np.all(chosen <= np.minimum(d_lo, d_hi) * (1 + 1e-5) + 1e-7 * r)
+
+
+def test_v_next_r_rounds_in_the_next_steps_zero_gradient_preconditioner():
+    # Ablation flag V_NEXT_R (with V_UPDATE_RTN, so the choice is deterministic):
+    # the stored level is the one nearer to v' in r'(q) = 1/(sqrt(beta2 q) c2' + eps)
+    # with c2' = 1/sqrt(1 - beta2^(t+1)) -- the preconditioner step t+1 would
+    # use with a zero gradient (listing page Table 1 evaluates the error there).
+    # beta2 = 0.5 makes r' differ from r well beyond rounding.
+    rng = np.random.default_rng(22)
+    n = 1280
+    g = _bf16(rng.normal(0, 1e-3, n) * np.exp(rng.uniform(-6, 2, n)))
+    gf = _from_bf16(g).astype(np.float64)
+    th = rng.normal(0, 0.02, n).astype(np.float32)
+    b2, eps = 0.5, 1e-3
+    L = O.codebooks()["dyn4"].astype(np.float64)
+    t_next = O.OracleTensor.zeros_state(th, 0, recipe="zip_sr")
+    t_same = O.OracleTensor.zeros_state(th, 0, recipe="zip_sr")
+    flags = O.V_UPDATE_RTN | O.V_NEXT_R
+    t_next.step(g, H["lr"], H["beta1"], b2, eps, H["wd"], 1, 0, "zip_sr", flags)
+    t_same.step(g, H["lr"], H["beta1"], b2, eps, H["wd"], 1, 0, "zip_sr", O.V_UPDATE_RTN)
+    assert np.array_equal(t_next.param.view(np.uint32), t_same.param.view(np.uint32))   # the update is unchanged
+    h1 = O.host_scalars(H["lr"], H["beta1"], b2, H["wd"], 1)
+    v1 = np.float32(h1["omb2"]) * gf * gf
+    c2n = 1.0 / np.sqrt(1.0 - b2 ** 2)
+    epsf = float(np.float32(eps))
+    rn = lambda v: 1.0 / (np.sqrt(b2 * v) * c2n + epsf)
+    q = _codes(t_next.v_codes, n)
+    for b in range(O.nblocks(n)):
+        sl = slice(128 * b, 128 * b + 128)
+        a = L * v1[sl].max()
+        k = np.clip(np.searchsorted(a, v1[sl], side="right") - 1, 0, 15)
+        k1 = np.minimum(k + 1, 15)
+        r = rn(v1[sl])
+        d_lo, d_hi = np.abs(rn(a[k]) - r), np.abs(rn(a[k1]) - r)
+        got = q[sl]
+        assert np.all((got == k) | (got == k1))
+        chosen = np.where(got == k, d_lo, d_hi)
+        assert np.all(chosen <= np.minimum(d_lo, d_hi) * (1 + 1e-5) + 1e-7 * r)
+    # the two preconditioner spaces disagree on some elements
+    assert (q != _codes(t_same.v_codes, n)).any()
