@@ -40,6 +40,8 @@ sys.path.insert(0, ROOT)
 BYTES_PER_PARAM = 2 + 4 + 4 + 2 + 2 * 1.0625           # packed (non-factored) tensors
 BYTES_PER_PARAM_FACTORED = 2 + 4 + 4 + 2 + 2 * 0.53125  # rank >= 2 tensors, factored v (m only)
 NOMINAL_HBM_GBS = 8000.0
+# rounding-variant call flags (Q4_M_SR_ALL, Q4_V_UPDATE_RTN, Q4_V_NEXT_R)
+VARIANT_FLAGS = {"none": 0, "m_sr_all": 0x2, "v_update_rtn": 0x4, "v_next_r": 0x8, "v_next_r_rtn": 0xC}
 
 
 def parse():
@@ -53,6 +55,8 @@ def parse():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0, help="target oracle time of the CPU sample")
+    ap.add_argument("--variant", default="none", choices=sorted(VARIANT_FLAGS),
+                    help="rounding variant (call flag) to time instead of the recipe's own rules")
     ap.add_argument("--max-grad-norm", type=float, default=None,
                     help="time the step with global gradient-norm clipping (sum-of-squares pass + clipped step)")
     ap.add_argument("--tensors", type=int, default=0,
@@ -312,7 +316,7 @@ def run_ours(args, rank, world, local):
     dev = torch.device("cuda", local)
     w = get_workload(args)
     h = W.HYPER
-    flags = 1 if w.lm_head_sr else 0
+    flags = (1 if w.lm_head_sr else 0) | VARIANT_FLAGS[args.variant]
     st = build_state(w, dev)
     stream = torch.cuda.current_stream(dev)
 
@@ -382,6 +386,8 @@ def run_ours(args, rank, world, local):
         "gpu_launches": launches_per_step(st, mgn is not None) * args.steps,
         "clocks": clocks,
     }
+    if args.variant != "none":
+        line["config"]["variant"] = args.variant
     if mgn is not None:
         # the timed step is the sum-of-squares pass plus the clipped step: the
         # roofline above covers both (2 more bytes per parameter); the pass is
@@ -414,7 +420,7 @@ def run_e2e(args, st, w, dev, stream, t0):
         return {"value": None, "unit": "params/s", "error": f"pinned allocation failed: {e}"[:200]}
     g_host.copy_(st.grad)
     torch.cuda.synchronize()
-    flags = 1 if w.lm_head_sr else 0
+    flags = (1 if w.lm_head_sr else 0) | VARIANT_FLAGS[args.variant]
     t = t0
     # one untimed round trip
     mgn = args.max_grad_norm

@@ -16,7 +16,8 @@ import numpy as np
 import torch
 
 from . import _native
-from ._native import (BLOCK, Q4_LM_HEAD_SR_ACTIVE, Q4_M_SR_ALL, Q4_T_FACTORED, Q4_T_LM_HEAD, Q4_V_UPDATE_RTN,
+from ._native import (BLOCK, Q4_LM_HEAD_SR_ACTIVE, Q4_M_SR_ALL, Q4_T_FACTORED, Q4_T_LM_HEAD, Q4_V_NEXT_R,
+                      Q4_V_UPDATE_RTN,
                       RECIPES, Q4Error, Q4Header,
                       Q4Tensor, lib)
 
@@ -24,7 +25,7 @@ __all__ = ["q4adamw_version", "q4adamw_strerror", "q4adamw_state_bytes", "q4adam
            "q4adamw_state_init", "q4adamw_header_check", "q4adamw_step", "q4adamw_step_noalloc",
            "q4adamw_dequant_state", "q4adamw_step_status", "q4adamw_grad_sqnorm", "q4adamw_step_clip",
            "q4adamw_codebook", "Q4State", "Q4Tensor", "Q4Header", "Q4Error", "RECIPES", "Q4_T_LM_HEAD",
-           "Q4_T_FACTORED", "Q4_LM_HEAD_SR_ACTIVE", "Q4_M_SR_ALL", "Q4_V_UPDATE_RTN", "BLOCK"]
+           "Q4_T_FACTORED", "Q4_LM_HEAD_SR_ACTIVE", "Q4_M_SR_ALL", "Q4_V_UPDATE_RTN", "Q4_V_NEXT_R", "BLOCK"]
 
 
 def _recipe(r) -> int:

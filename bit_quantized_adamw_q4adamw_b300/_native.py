@@ -27,6 +27,7 @@ Q4_T_FACTORED = 0x2
 Q4_LM_HEAD_SR_ACTIVE = 0x1
 Q4_M_SR_ALL = 0x2
 Q4_V_UPDATE_RTN = 0x4
+Q4_V_NEXT_R = 0x8
 Q4_STATUS_STAGE_TIMEOUT = 0x1
 BLOCK = 128
 NOALLOC_SCRATCH_BYTES = 4 * 1024 * 1024

@@ -320,8 +320,8 @@ int step_impl(const q4adamw_tensor_t* t, int n, float lr, float beta1, float bet
     if (n < 0 || (n > 0 && !t)) return Q4_EINVAL;
     if (int rc = check_recipe(recipe)) return rc;
     if (step < 1 || step > 0xFFFFFFFFll) return Q4_EINVAL;
-    if (flags & ~(Q4_LM_HEAD_SR_ACTIVE | Q4_M_SR_ALL | Q4_V_UPDATE_RTN)) return Q4_EINVAL;
-    if ((flags & Q4_V_UPDATE_RTN) && recipe != Q4_RECIPE_ZIP_SR) return Q4_EINVAL;
+    if (flags & ~(Q4_LM_HEAD_SR_ACTIVE | Q4_M_SR_ALL | Q4_V_UPDATE_RTN | Q4_V_NEXT_R)) return Q4_EINVAL;
+    if ((flags & (Q4_V_UPDATE_RTN | Q4_V_NEXT_R)) && recipe != Q4_RECIPE_ZIP_SR) return Q4_EINVAL;
     if (!(beta1 >= 0.f && beta1 < 1.f) || !(beta2 >= 0.f && beta2 < 1.f)) return Q4_EINVAL;
     if (!(eps > 0.f) || !std::isfinite(eps) || !std::isfinite(lr) || !std::isfinite(weight_decay)) return Q4_EINVAL;
     for (int i = 0; i < n; ++i)
@@ -407,6 +407,8 @@ int step_impl(const q4adamw_tensor_t* t, int n, float lr, float beta1, float bet
     // that holds whenever eps lies in [2^-100, 2^60].
     p.fast_math = (eps >= 0x1p-100f && eps <= 0x1p60f) ? 1 : 0;
     p.v_update_rtn = (flags & Q4_V_UPDATE_RTN) ? 1 : 0;
+    p.v_next_r = (flags & Q4_V_NEXT_R) ? 1 : 0;
+    p.c2_next = host_scalars(lr, beta1, beta2, weight_decay, step + 1).c2;
     p.has_m_sr = 0;
     p.sqnorm = sqnorm;
     p.max_norm = max_norm;

@@ -87,6 +87,8 @@ struct StepParams {
     uint32_t step;
     int fast_math;                // eps and c2 keep 1/(sqrt(v) c2 + eps) in the fast domain
     int v_update_rtn;             // ZIP-SR with Update-RTN in place of Update-SR
+    int v_next_r;                 // ZIP-SR rounds in the next step's zero-gradient preconditioner
+    float c2_next;                //   its 1/sqrt(1 - beta2^(t+1))
     int has_m_sr;                 // some tensor rounds its first moment stochastically
     const float* sqnorm;          // global-norm clipping: device sum of squares, or NULL
     float max_norm;               //   and the clipping threshold

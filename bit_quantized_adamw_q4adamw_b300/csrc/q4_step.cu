@@ -260,6 +260,12 @@ __device__ __forceinline__ float precond(const StepParams& P, float v1) {
     return __frcp_rn(__fadd_rn(__fmul_rn(__fsqrt_rn(v1), P.c2), P.eps));
 }
 
+// Next-step zero-gradient preconditioner 1/(sqrt(beta2 x) c2(t+1) + eps), the
+// rounding space of the next-step ZIP-SR variant (IEEE operations only).
+__device__ __forceinline__ float precond_next(const StepParams& P, float x) {
+    return __frcp_rn(__fadd_rn(__fmul_rn(__fsqrt_rn(__fmul_rn(P.beta2, x)), P.c2_next), P.eps));
+}
+
 // The update of 8 elements: r_i and theta'_i.
 template <bool FAST>
 __device__ __forceinline__ void update8(const StepParams& P, const float m1[8], const float v1[8], float th[8],
@@ -336,7 +342,7 @@ __device__ __forceinline__ uint32_t pack8(const uint32_t c[8]) {
 // numel already zeroed), the new scales s_m, s_v and r (ZIP-SR).  Handles
 // every case: partial blocks, LM-head stochastic rounding, scales outside the
 // fast range (exact sequential searches).
-template <int RECIPE, bool URTN>
+template <int RECIPE, bool URTN, bool NEXTR>
 __device__ __forceinline__ void requant_general(const StepParams& P, const DevTensor& d, const SmemAll& sm,
                                                 WarpTables& wt, int lane, int64_t blk, bool blk_ok, int64_t e0,
                                                 int nvalid, bool fact, bool m_sr, const float m1[8],
@@ -347,7 +353,8 @@ __device__ __forceinline__ void requant_general(const StepParams& P, const DevTe
     if (m_sr) wt.am[hb + j] = __fmul_rn(my_nf4, s_m);
     if (RECIPE == Q4_RECIPE_ZIP_SR) {
         const float a = __fmul_rn(my_vl, s_v);
-        const float rk = (P.fast_math && scale_in_fast_range(s_v)) ? precond<true>(P, a) : precond<false>(P, a);
+        const float rk = NEXTR ? precond_next(P, a)
+                               : (P.fast_math && scale_in_fast_range(s_v)) ? precond<true>(P, a) : precond<false>(P, a);
         const float rk1 = __shfl_down_sync(0xffffffffu, rk, 1);
         wt.av[hb + j] = a;
         wt.rd[hb + j] = make_float2(rk, j < 15 ? __fmul_rn(__fsub_rn(rk, rk1), kTwoM24) : 0.f);
@@ -437,14 +444,16 @@ __device__ __forceinline__ void requant_general(const StepParams& P, const DevTe
                         if (wt.av[hb + q] <= x) k = q;
                 }
                 const float2 e = wt.rd[hb + k];
+                // the r being rounded: the update's, or the next step's
+                const float ri = NEXTR ? precond_next(P, x) : r[i];
                 int code;
                 if (URTN) {
                     // Update-RTN: the neighbour whose preconditioner is nearer
                     // to r (a tie keeps k)
-                    code = k == 15 ? 15 : k + (__fsub_rn(r[i], wt.rd[hb + k + 1].x) < __fsub_rn(e.x, r[i]) ? 1 : 0);
+                    code = k == 15 ? 15 : k + (__fsub_rn(ri, wt.rd[hb + k + 1].x) < __fsub_rn(e.x, ri) ? 1 : 0);
                 } else {
                     // u * (r_k - r_{k+1}) with u = (w >> 8) 2^-24, as (w >> 8) * ((r_k - r_{k+1}) 2^-24)
-                    code = k + (__fmul_rn((float)(w[i] >> 8), e.y) < __fsub_rn(e.x, r[i]) ? 1 : 0);
+                    code = k + (__fmul_rn((float)(w[i] >> 8), e.y) < __fsub_rn(e.x, ri) ? 1 : 0);
                 }
                 if (i >= nvalid) code = 0;
                 cv |= (uint32_t)code << (4 * i);
@@ -584,7 +593,7 @@ __device__ __forceinline__ void moments_and_update(const StepParams& P, const fl
 
 // ----------------------------------------------------------------- one tile, general path
 // `st` is the staged tile or nullptr (ragged tail: read from global memory).
-template <int RECIPE, bool URTN>
+template <int RECIPE, bool URTN, bool NEXTR>
 __device__ __forceinline__ void compute_tile(const StepParams& P, const DevTensor& d, int64_t pair,
                                              const Stage* st, int lane, SmemAll& sm, WarpTables& wt,
                                              const float my_nf4, const float my_nf4t, const float my_vl,
@@ -694,7 +703,7 @@ __device__ __forceinline__ void compute_tile(const StepParams& P, const DevTenso
 
     const float s_m = half_max(amax, half);
     const float s_v = fact ? 0.f : half_max(vmax, half);
-    requant_general<RECIPE, URTN>(P, d, sm, wt, lane, blk, blk_ok, e0, nvalid, fact, m_sr, m1, v1, r, s_m, s_v,
+    requant_general<RECIPE, URTN, NEXTR>(P, d, sm, wt, lane, blk, blk_ok, e0, nvalid, fact, m_sr, m1, v1, r, s_m, s_v,
                                   my_nf4, my_nf4t, my_vl, my_vt);
 }
 
@@ -801,7 +810,7 @@ __device__ __forceinline__ void compute_tile_full(const StepParams& P, const Dev
             v1s[2 * k] = v1[k].x; v1s[2 * k + 1] = v1[k].y;
             rs[2 * k] = r[k].x; rs[2 * k + 1] = r[k].y;
         }
-        requant_general<RECIPE, URTN>(P, d, sm, wt, lane, blk, true, e0, 8, fact, m_sr, m1s, v1s, rs, s_m, s_v,
+        requant_general<RECIPE, URTN, false>(P, d, sm, wt, lane, blk, true, e0, 8, fact, m_sr, m1s, v1s, rs, s_m, s_v,
                                       my_nf4, my_nf4t, my_vl, my_vt);
         return;
     }
@@ -971,7 +980,8 @@ __device__ __forceinline__ void compute_tile_full(const StepParams& P, const Dev
 // its first moment stochastically (the LM head in the final phase), which the
 // fast path then handles too.  Separate instantiations, so that the main
 // kernels carry none of that code.
-template <int RECIPE, bool URTN, bool MSR>
+// NEXTR (the next-step ZIP-SR variant) runs every tile on the general path.
+template <int RECIPE, bool URTN, bool MSR, bool NEXTR>
 __global__ void __launch_bounds__(kStepThreads, 1) step_kernel(const __grid_constant__ StepParams P) {
     extern __shared__ unsigned char smem_raw[];
     // the tables need 256-byte alignment; the launch adds 256 bytes of slack
@@ -1169,13 +1179,13 @@ __global__ void __launch_bounds__(kStepThreads, 1) step_kernel(const __grid_cons
             __syncwarp();
         }
         const bool full = c_p < c_n - 1 || ws.desc.numel - c_p * 2 * kBlock >= 2 * kBlock;
-        if (full) {
+        if (full && !NEXTR) {
             compute_tile_full<RECIPE, URTN, MSR>(P, ws.desc, c_p, ws.st[s], lane, sm, ws.wt, my_nf4, my_nf4t,
                                                  my_vl, my_vt, my_vl1, clip);
         } else {
             const int64_t left = ws.desc.numel - c_p * 2 * kBlock;
-            compute_tile<RECIPE, URTN>(P, ws.desc, c_p, (left & 7) == 0 ? &ws.st[s] : nullptr, lane, sm, ws.wt,
-                                       my_nf4, my_nf4t, my_vl, my_vt, clip);
+            compute_tile<RECIPE, URTN, NEXTR>(P, ws.desc, c_p, (full || (left & 7) == 0) ? &ws.st[s] : nullptr,
+                                              lane, sm, ws.wt, my_nf4, my_nf4t, my_vl, my_vt, clip);
         }
         ++c_p;
         ++c_tile;
@@ -1186,12 +1196,12 @@ __global__ void __launch_bounds__(kStepThreads, 1) step_kernel(const __grid_cons
 
 size_t step_smem_bytes() { return sizeof(SmemAll) + 256; }
 
-template <int RECIPE, bool URTN, bool MSR>
+template <int RECIPE, bool URTN, bool MSR, bool NEXTR>
 int configure(int device) {
     static bool done[64] = {false};
     if (device < 0 || device >= 64) device = 0;
     if (done[device]) return 0;
-    const cudaError_t e = cudaFuncSetAttribute(step_kernel<RECIPE, URTN, MSR>,
+    const cudaError_t e = cudaFuncSetAttribute(step_kernel<RECIPE, URTN, MSR, NEXTR>,
                                                cudaFuncAttributeMaxDynamicSharedMemorySize, (int)step_smem_bytes());
     if (e == cudaSuccess) done[device] = true;
     return (int)e;
@@ -1219,23 +1229,25 @@ int launch_step(const StepParams& p, int grid, void* stream) {
     if (e != cudaSuccess) return (int)e;
     const size_t smem = step_smem_bytes();
     int ce = 0;
-#define Q4_LAUNCH(R, U, M)                                                      \
+#define Q4_LAUNCH(R, U, M, N)                                                   \
     do {                                                                        \
-        if ((ce = configure<R, U, M>(dev))) return ce;                          \
-        step_kernel<R, U, M><<<grid, kStepThreads, smem, s>>>(p);               \
+        if ((ce = configure<R, U, M, N>(dev))) return ce;                       \
+        step_kernel<R, U, M, N><<<grid, kStepThreads, smem, s>>>(p);            \
     } while (0)
     switch (p.recipe) {
         case Q4_RECIPE_ZIP_SR:
-            if (p.v_update_rtn) Q4_LAUNCH(Q4_RECIPE_ZIP_SR, true, false);
-            else if (p.has_m_sr) Q4_LAUNCH(Q4_RECIPE_ZIP_SR, false, true);
-            else Q4_LAUNCH(Q4_RECIPE_ZIP_SR, false, false);
+            if (p.v_next_r && p.v_update_rtn) Q4_LAUNCH(Q4_RECIPE_ZIP_SR, true, false, true);
+            else if (p.v_next_r) Q4_LAUNCH(Q4_RECIPE_ZIP_SR, false, false, true);
+            else if (p.v_update_rtn) Q4_LAUNCH(Q4_RECIPE_ZIP_SR, true, false, false);
+            else if (p.has_m_sr) Q4_LAUNCH(Q4_RECIPE_ZIP_SR, false, true, false);
+            else Q4_LAUNCH(Q4_RECIPE_ZIP_SR, false, false, false);
             break;
         case Q4_RECIPE_ZE_EDEN:
-            if (p.has_m_sr) Q4_LAUNCH(Q4_RECIPE_ZE_EDEN, false, true);
-            else Q4_LAUNCH(Q4_RECIPE_ZE_EDEN, false, false);
+            if (p.has_m_sr) Q4_LAUNCH(Q4_RECIPE_ZE_EDEN, false, true, false);
+            else Q4_LAUNCH(Q4_RECIPE_ZE_EDEN, false, false, false);
             break;
-        case Q4_RECIPE_TORCHAO: Q4_LAUNCH(Q4_RECIPE_TORCHAO, false, false); break;
-        default: Q4_LAUNCH(Q4_RECIPE_FACTORED, false, false); break;
+        case Q4_RECIPE_TORCHAO: Q4_LAUNCH(Q4_RECIPE_TORCHAO, false, false, false); break;
+        default: Q4_LAUNCH(Q4_RECIPE_FACTORED, false, false, false); break;
     }
 #undef Q4_LAUNCH
     return (int)cudaGetLastError();

@@ -88,6 +88,15 @@ typedef enum q4_recipe {
 #define Q4_V_UPDATE_RTN 0x4u      /* rounding variant (Table 1): Update-RTN in
                                      place of Update-SR for the second moment;
                                      Q4_RECIPE_ZIP_SR only, Q4_EINVAL otherwise */
+#define Q4_V_NEXT_R 0x8u          /* rounding variant (Table 1 evaluates the
+                                     preconditioner at step t+1 with a gradient
+                                     of order eps): the second moment's Update
+                                     rule (SR, or RTN with Q4_V_UPDATE_RTN)
+                                     works in r'(q) = 1/(sqrt(beta2 q) *
+                                     c2(t+1) + eps), c2(t+1) = 1/sqrt(1 -
+                                     beta2^(t+1)), instead of the same-step r;
+                                     Q4_RECIPE_ZIP_SR only.  Runs the general
+                                     (slower) kernel path. */
 
 /*
  * One parameter tensor and its optimizer state.  All pointers are device
@@ -208,8 +217,9 @@ int q4adamw_header_check(const q4adamw_header_t* h, int recipe);
 int q4adamw_step(const q4adamw_tensor_t* t, int n, float lr, float beta1, float beta2, float eps, float weight_decay,
                  int64_t step, uint64_t seed, int recipe, uint32_t flags, void* workspace, int64_t workspace_bytes,
                  void* stream);
-/* (flags: any bit outside Q4_LM_HEAD_SR_ACTIVE | Q4_M_SR_ALL | Q4_V_UPDATE_RTN,
- * or Q4_V_UPDATE_RTN with a recipe other than ZIP-SR, returns Q4_EINVAL.) */
+/* (flags: any bit outside Q4_LM_HEAD_SR_ACTIVE | Q4_M_SR_ALL | Q4_V_UPDATE_RTN |
+ * Q4_V_NEXT_R, or Q4_V_UPDATE_RTN / Q4_V_NEXT_R with a recipe other than
+ * ZIP-SR, returns Q4_EINVAL.) */
 
 /*
  * Global gradient-norm clipping (AReno docs "4-bit AdamW", section "State

@@ -115,8 +115,10 @@ def test_step_validation_happens_before_any_device_work():
                               a["recipe"], a["flags"], ws, wsb, None)
 
     assert call(recipe=9) == _native.Q4_ERECIPE
-    assert call(flags=0x8) == _native.Q4_EINVAL                       # unknown flag bit
+    assert call(flags=0x10) == _native.Q4_EINVAL                      # unknown flag bit
     assert call(recipe=1, flags=_native.Q4_V_UPDATE_RTN) == _native.Q4_EINVAL   # ZIP-SR only
+    assert call(recipe=1, flags=_native.Q4_V_NEXT_R) == _native.Q4_EINVAL       # ZIP-SR only
+    assert call(recipe=3, flags=_native.Q4_V_NEXT_R) == _native.Q4_EINVAL
     assert call(step=0) == _native.Q4_EINVAL
     assert call(b1=1.0) == _native.Q4_EINVAL
     assert call(b2=-0.1) == _native.Q4_EINVAL
@@ -153,7 +155,7 @@ def test_clip_entry_points_validate_before_any_device_work():
     assert clip(max_norm=float("inf")) == _native.Q4_EINVAL
     assert clip(sqnorm=ctypes.c_void_p(0)) == _native.Q4_EINVAL
     assert clip(sqnorm=ctypes.c_void_p((1 << 41) + 2)) == _native.Q4_EALIGN
-    assert clip(flags=0x8) == _native.Q4_EINVAL
+    assert clip(flags=0x10) == _native.Q4_EINVAL
     assert clip(wsb=16) == _native.Q4_EWORKSPACE
 
     def norm(arr=arr, n=1, out=sq, ws=ws, wsb=1 << 20):

@@ -185,6 +185,23 @@ def test_v_update_rtn_variant():
         _assert_exact(p.compare(), t)
 
 
+@pytest.mark.parametrize("urtn", [False, True])
+@pytest.mark.parametrize("beta2", [0.999, 0.5])
+def test_v_next_r_variant(urtn, beta2):
+    # Rounding variant: ZIP-SR's Update rule in the next step's zero-gradient
+    # preconditioner (flag 0x8), alone and with Update-RTN; beta2 = 0.5 moves
+    # r' far from the same-step r.  Full tiles, ragged tails, LM-head SR.
+    shapes = [(4096,), (300,), (64, 130), (128 * 13 + 17,), (2, 1024)]
+    w = W.custom("nextr", shapes, "zip_sr", flags=[W.T_LM_HEAD, 0, 0, 0, 0], grad="tensor_scaled",
+                 sigma=(1e-6, 1e-2))
+    p = Pair(w.tensors, "zip_sr")
+    hyper = dict(HYPER, beta2=beta2)
+    flags = q4.Q4_V_NEXT_R | q4.Q4_LM_HEAD_SR_ACTIVE | (q4.Q4_V_UPDATE_RTN if urtn else 0)
+    for t in range(1, 7):
+        p.step(t, grads_for(w, t), seed=4, flags=flags, hyper=hyper)
+        _assert_exact(p.compare(), t)
+
+
 def test_torchao_tensor_scaled_multistep():
     # The TorchAO baseline on a GPT-like list with per-tensor gradient scales in
     # [1e-5, 1e-2], LM head flagged and the final phase active (stays RTN).
