@@ -62,6 +62,7 @@ struct Tables {
     uint8_t lut_v_l[kVLut];  // v level (cell) candidate by log bucket
     uint8_t lut_v_t[kVLut];  // v threshold candidate by log bucket
     float2 nf4_bucket[64];   // NF4 RTN by linear bucket: {threshold of the candidate, candidate}
+    uint8_t lut_m_log[kVLut];  // SDyn4 RTN: lower bound of #{i : A_i <= |m|/s} by log bucket
     int m_lut;               // 1 when the linear-bucket tables are valid for the m codebook
 };
 

@@ -72,7 +72,8 @@ static_assert(sizeof(Stage) % 16 == 0, "stage buffers must keep 16-byte alignmen
 struct __align__(256) WarpTables {
     float deqm[32];        // [half][16] NF4 level * old s_m
     float deqv[32];        // [half][16] v level * old s_v
-    float2 mt[2][64];      // fast path: [half][linear bucket] {NF4 threshold of the candidate * new s_m, candidate}
+    float2 mt[2][64];      // fast path: [half][linear bucket] {NF4 threshold of the candidate * new s_m, candidate};
+                           // TorchAO: floats 0..8 of [half] = SDyn4 magnitudes A_0..A_7 * new s_m, +inf
     float4 ve[2][16];      // fast path, per half: ZIP-SR a_{c+1} by cell (floats 0..15) and (r_k, d_k)
                            // by cell (float2 8..23); RTN {t_c s_v, L_c, L_{c+1}} by cell
     float tm[32];          // general path: [half][16] NF4 threshold * new s_m
@@ -96,6 +97,7 @@ struct __align__(256) SmemAll {
     uint8_t lut_nf4_l[64];
     uint8_t lut_v_l[kVLut];
     uint8_t lut_v_t[kVLut];
+    uint8_t lut_m_log[kVLut];   // TorchAO: SDyn4 magnitude candidates
 };
 
 // ----------------------------------------------------------------- PTX helpers
@@ -717,7 +719,8 @@ template <int RECIPE, bool URTN, bool MSR>
 __device__ __forceinline__ void compute_tile_full(const StepParams& P, const DevTensor& d, int64_t pair,
                                                   const Stage& st, int lane, SmemAll& sm, WarpTables& wt,
                                                   const float my_nf4, const float my_nf4t, const float my_vl,
-                                                  const float my_vt, const float my_vl1, const float clip) {
+                                                  const float my_vt, const float my_vl1, const float my_mag,
+                                                  const float clip) {
     const int half = lane >> 4, j = lane & 15, hb = half * 16;
     const int64_t blk = pair * 2 + half;
     const int64_t e0 = blk * kBlock + j * 8;
@@ -799,9 +802,8 @@ __device__ __forceinline__ void compute_tile_full(const StepParams& P, const Dev
     const float s_m = half_max(amax, half);
     const float s_v = fact ? 0.f : half_max(vmax_lane, half);
 
-    const bool fast = RECIPE != Q4_RECIPE_TORCHAO && !URTN &&
-                      __all_sync(0xffffffffu, (MSR || !m_sr) && scale_in_fast_range(s_m) &&
-                                                  (fact || scale_in_fast_range(s_v)));
+    const bool fast = !URTN && __all_sync(0xffffffffu, (MSR || !m_sr) && scale_in_fast_range(s_m) &&
+                                                          (fact || scale_in_fast_range(s_v)));
     if (!fast) {
         float m1s[8], v1s[8], rs[8];
 #pragma unroll
@@ -821,7 +823,9 @@ __device__ __forceinline__ void compute_tile_full(const StepParams& P, const Dev
     // State-SR (LM head in the final phase): a_k = level k at the new scale;
     // the cell search reads a_{c+1} (floats 0..15 of mt[half]), then
     // (a_k, d_k) with d_k = (a_{k+1} - a_k) 2^-24 (float2 8..23).
-    if (MSR && m_sr) {
+    if (RECIPE == Q4_RECIPE_TORCHAO) {
+        reinterpret_cast<float*>(&wt.mt[half][0])[j] = __fmul_rn(my_mag, s_m);   // A_j s_m; +inf from j = 8
+    } else if (MSR && m_sr) {
         const float a = __fmul_rn(my_nf4, s_m);
         const float a1 = __shfl_down_sync(0xffffffffu, a, 1);
         float* mb = reinterpret_cast<float*>(&wt.mt[half][0]);
@@ -855,9 +859,31 @@ __device__ __forceinline__ void compute_tile_full(const StepParams& P, const Dev
     }
     __syncwarp();
 
-    // ---- m codes: NF4 RTN, or NF4 State-SR -----------------------------------
+    // ---- m codes: NF4 RTN, or NF4 State-SR; TorchAO SDyn4 RTN by magnitude ----
     uint32_t cm;
-    if (MSR && m_sr) {
+    if (RECIPE == Q4_RECIPE_TORCHAO) {
+        // count n = #{i : A_i s_m below |m'|} from the log-bucket lower bound c
+        // and one comparison with A_c s_m (strict for m' >= 0, non-strict for
+        // m' < 0); code = 7 + n, or 7 - min(n, 7) for m' < 0
+        const float rho = rcp_rn_normal<1>(s_m);
+        const uint32_t mt_base = tb + (uint32_t)((char*)&wt.mt[half][0] - (char*)&wt);
+        const uint32_t lut = smem_addr(sm.lut_m_log);
+        uint32_t c[8];
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            const float2 ax = make_float2(fabsf(m1[k].x), fabsf(m1[k].y));
+            const float2 y = mul2_rn(ax, make_float2(rho, rho));
+            const uint32_t c0 = lds_u8(lut + (__float_as_uint(y.x) >> 19));
+            const uint32_t c1 = lds_u8(lut + (__float_as_uint(y.y) >> 19));
+            const float a0 = lds_f32(mt_base + c0 * 4u), a1 = lds_f32(mt_base + c1 * 4u);
+            const bool neg0 = m1[k].x < 0.f, neg1 = m1[k].y < 0.f;
+            const uint32_t n0 = c0 + ((neg0 ? ax.x >= a0 : ax.x > a0) ? 1u : 0u);
+            const uint32_t n1 = c1 + ((neg1 ? ax.y >= a1 : ax.y > a1) ? 1u : 0u);
+            c[2 * k] = neg0 ? 7u - min(n0, 7u) : 7u + n0;
+            c[2 * k + 1] = neg1 ? 7u - min(n1, 7u) : 7u + n1;
+        }
+        cm = pack8(c);
+    } else if (MSR && m_sr) {
         const float rho16 = __fmul_rn(16.f, rcp_rn_normal<1>(s_m));
         const uint32_t mt_base = tb + (uint32_t)((char*)&wt.mt[half][0] - (char*)&wt);
         const uint32_t lut = smem_addr(sm.lut_nf4_l);
@@ -999,6 +1025,8 @@ __global__ void __launch_bounds__(kStepThreads, 1) step_kernel(const __grid_cons
     for (int i = threadIdx.x; i < kVLut / 4; i += blockDim.x) {
         reinterpret_cast<uint32_t*>(sm.lut_v_l)[i] = reinterpret_cast<const uint32_t*>(P.tab.lut_v_l)[i];
         reinterpret_cast<uint32_t*>(sm.lut_v_t)[i] = reinterpret_cast<const uint32_t*>(P.tab.lut_v_t)[i];
+        if (RECIPE == Q4_RECIPE_TORCHAO)
+            reinterpret_cast<uint32_t*>(sm.lut_m_log)[i] = reinterpret_cast<const uint32_t*>(P.tab.lut_m_log)[i];
     }
     if (lane == 0) {
         // count 5: the arrive.expect_tx of lane 0 and the arrives that
@@ -1013,6 +1041,8 @@ __global__ void __launch_bounds__(kStepThreads, 1) step_kernel(const __grid_cons
     const float my_nf4 = P.tab.nf4[j], my_nf4t = P.tab.nf4_t[j];
     const float my_vl = P.tab.vl[j], my_vt = P.tab.vt[j];
     const float my_vl1 = P.tab.vl[j < 15 ? j + 1 : 15];
+    // TorchAO: lane j holds the SDyn4 magnitude A_j = T_{7+j} (+inf for j >= 8)
+    const float my_mag = RECIPE == Q4_RECIPE_TORCHAO ? P.tab.nf4_t[j < 8 ? 7 + j : 15] : 0.f;
     const float clip = clip_factor(P.sqnorm, P.max_norm);
     const uint64_t policy = evict_first_policy();
 
@@ -1181,7 +1211,7 @@ __global__ void __launch_bounds__(kStepThreads, 1) step_kernel(const __grid_cons
         const bool full = c_p < c_n - 1 || ws.desc.numel - c_p * 2 * kBlock >= 2 * kBlock;
         if (full && !NEXTR) {
             compute_tile_full<RECIPE, URTN, MSR>(P, ws.desc, c_p, ws.st[s], lane, sm, ws.wt, my_nf4, my_nf4t,
-                                                 my_vl, my_vt, my_vl1, clip);
+                                                 my_vl, my_vt, my_vl1, my_mag, clip);
         } else {
             const int64_t left = ws.desc.numel - c_p * 2 * kBlock;
             compute_tile<RECIPE, URTN, NEXTR>(P, ws.desc, c_p, (full || (left & 7) == 0) ? &ws.st[s] : nullptr,

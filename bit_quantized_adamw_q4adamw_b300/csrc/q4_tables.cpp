@@ -159,6 +159,35 @@ bool build_log(const float* pts, int np, bool levels, uint8_t* lut) {
     return true;
 }
 
+// SDyn4 RTN by magnitude.  Its RTN thresholds are symmetric about zero,
+// T_k = -T_{13-k} for k = 0..6, with one more positive threshold T_14, so with
+// the magnitudes A_i = T_{7+i} (i = 0..7, ascending) the code of x is
+// 7 + #{i : x > A_i s} for x >= 0 and 7 - min(#{i : |x| >= A_i s}, 7) for
+// x < 0.  The table holds, per log bucket of |x|/s, a lower bound c of the
+// count with the exact count in {c, c+1} (for either comparison).
+bool build_m_log(const Codebook& c, uint8_t* lut) {
+    for (int k = 0; k < 7; ++k)
+        if (!(c.thresholds[k] == -c.thresholds[13 - k])) return false;
+    float mags[8];
+    for (int i = 0; i < 8; ++i) mags[i] = c.thresholds[7 + i];
+    if (!(mags[0] > 0.f)) return false;
+    for (int i = 0; i < kVLut; ++i) {
+        double lo = bits_to_float((uint32_t)i << 19);
+        double hi = (i + 1 < kVLut) ? bits_to_float((uint32_t)(i + 1) << 19) : INFINITY;
+        if (!std::isfinite(lo)) lo = 1e300;
+        const double w = std::ldexp(1.0, -20);
+        lo = lo * (1 - w);
+        hi = std::isfinite(hi) ? hi * (1 + w) : 1e300;
+        int below, und;
+        if (!classify(mags, 8, lo, hi, &below, &und)) {
+            if (lo > 2.0) { lut[i] = 8; continue; }   // |x|/s > 1 cannot occur
+            return false;
+        }
+        lut[i] = (uint8_t)below;
+    }
+    return true;
+}
+
 Codebook make_sdyn4() {
     double v[16];
     int n = 0;
@@ -223,6 +252,8 @@ bool build_tables(int mbook, int vbook, Tables* t) {
     // bucket (SDyn4 near zero) is searched by the kernel without them.
     t->m_lut = build_linear(nf4.thresholds, 15, false, t->lut_nf4_t) &&
                build_linear(nf4.levels, 16, true, t->lut_nf4_l) ? 1 : 0;
+    // the signed dynamic-exponent map (TorchAO's m) is searched by magnitude
+    if (mbook == 3 && !build_m_log(nf4, t->lut_m_log)) return false;
     if (!build_log(v.levels, 16, true, t->lut_v_l)) return false;
     if (!build_log(v.thresholds, 15, false, t->lut_v_t)) return false;
     for (int i = 0; i < 64; ++i) {

@@ -136,6 +136,14 @@ def test_gpt1p4b_zipsr_clipped_sampled_blocks():
     assert n >= 2 * 4 * 100
 
 
+def test_gpt1p4b_torchao_sampled_blocks():
+    # the TorchAO baseline recipe at the full 1.4B size (LM head flagged, final
+    # phase active: it stays RTN in this recipe)
+    w = W.WORKLOADS["gpt1p4b_torchao"]
+    n = _run_packed(w, 2, q4.Q4_LM_HEAD_SR_ACTIVE)
+    assert n >= 2 * 4 * 100
+
+
 @pytest.mark.parametrize("name", ["llama8b_zipsr", "llama8b_zeeden"])
 def test_llama8b_sampled_blocks(name):
     w = W.WORKLOADS[name]

@@ -202,6 +202,25 @@ def test_v_next_r_variant(urtn, beta2):
         _assert_exact(p.compare(), t)
 
 
+def test_torchao_mixed_magnitudes_every_sdyn4_rung():
+    # |m'|/s spread over four decades inside each block, so every SDyn4
+    # threshold (0.00275 .. 0.94375 of the scale, both signs) decides codes on
+    # the fast path; plus ragged tails and a zero block.
+    n = 128 * 40 + 77
+    w = W.custom("taomix", [(n,), (3, 129)], "torchao")
+    rng = np.random.default_rng(8)
+    p = Pair(w.tensors, "torchao")
+    for t in range(1, 9):
+        gs = []
+        for s in w.tensors:
+            g = rng.normal(0, 1, s.numel) * 10.0 ** rng.uniform(-4, 0, s.numel)
+            if s.numel == n:
+                g[:128] = 0.0
+            gs.append(torch.from_numpy(g.astype(np.float32)).to(torch.bfloat16))
+        p.step(t, gs, seed=t)
+        _assert_exact(p.compare(), t)
+
+
 def test_torchao_tensor_scaled_multistep():
     # The TorchAO baseline on a GPT-like list with per-tensor gradient scales in
     # [1e-5, 1e-2], LM head flagged and the final phase active (stays RTN).
