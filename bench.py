@@ -381,6 +381,7 @@ def run_ours(args, rank, world, local):
                      "peak_kind": f"{peak_kind} copy bandwidth (MEASURED_PEAKS.json hbm_gbs)"
                      if peak_kind == "measured" else "fallback 6.4 TB/s",
                      "traffic": (tr["dram_bytes_per_param"] * w.numel) if tr else None,
+                     "traffic_source": tr["measured_on"] if tr else "no ncu record for this kernel source",
                      "algorithmic_bytes": alg, "kernel": "step_kernel (one launch per step)",
                      "frac_of_nominal_8tbs": achieved / NOMINAL_HBM_GBS},
         "gpu_launches": launches_per_step(st, mgn is not None) * args.steps,
@@ -394,6 +395,9 @@ def run_ours(args, rank, world, local):
         # also timed alone here
         line["config"]["max_grad_norm"] = mgn
         line["roofline"]["kernel"] = "sqnorm pass (3 kernels) + step_kernel, per step"
+        sq_tr = traffic_record("sqnorm_chunk_kernel")
+        line["roofline"]["traffic"] = ((tr["dram_bytes_per_param"] + sq_tr["dram_bytes_per_param"]) * w.numel
+                                       if tr and sq_tr else None)
         line["sqnorm_pass"] = {"ms": sq_ms, "bytes": 2.0 * w.numel,
                                "achieved_gbs": 2.0 * w.numel / (sq_ms / 1e3) / 1e9,
                                "frac": 2.0 * w.numel / (sq_ms / 1e3) / 1e9 / peak}
