@@ -200,7 +200,11 @@ DevTensor make_dev(const q4adamw_tensor_t& t, int recipe, uint32_t call_flags) {
         d.flags |= q4::DF_M_SR;
     if (is_factored(t, recipe)) {
         d.flags |= q4::DF_FACTORED;
-        if (d.cols % 8 == 0 && aligned(t.v_col, 16)) d.flags |= q4::DF_CVEC;
+        // vector column loads and incremental (row, column) tracking in the step
+        // kernel: columns a multiple of 8 (16-B aligned float4 runs) and at
+        // least one tile (256) wide, rows within 32 bits
+        if (d.cols % 8 == 0 && d.cols >= 256 && d.rows <= 0xFFFFFFFFll && aligned(t.v_col, 16))
+            d.flags |= q4::DF_CVEC;
     }
     if (t.param_bf16) d.flags |= q4::DF_BF16;
     return d;

@@ -45,7 +45,7 @@ enum : uint32_t {
     DF_M_SR = 1u,        // NF4 stochastic rounding of m this step
     DF_FACTORED = 2u,    // factored v (row/column statistics)
     DF_BF16 = 4u,        // write the BF16 weight copy
-    DF_CVEC = 8u,        // factored with cols % 8 == 0 and 16-B aligned v_col
+    DF_CVEC = 8u,        // factored with cols % 8 == 0, cols >= 256, rows < 2^32, 16-B aligned v_col
 };
 
 // Bits of the step's device status word (first word of the workspace).

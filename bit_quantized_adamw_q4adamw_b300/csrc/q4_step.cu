@@ -530,9 +530,8 @@ __device__ __forceinline__ void factored_vhat(const DevTensor& d, int64_t e0, in
     const bool rb_ok = rb.x != 0.f && quot_range_ok(rb.x);
     float R[8], C[8];
     if (nvalid == 8 && (d.flags & DF_CVEC)) {
-        const uint32_t cols = (uint32_t)d.cols;
-        const uint32_t frow = (uint32_t)e0 / cols;
-        const uint32_t fcol = (uint32_t)e0 - frow * cols;
+        const int64_t frow = e0 / d.cols;
+        const int64_t fcol = e0 - frow * d.cols;
         const float Ri = __ldg(d.vrow + frow);
         const float4 c0 = __ldg(reinterpret_cast<const float4*>(d.vcol + fcol));
         const float4 c1 = __ldg(reinterpret_cast<const float4*>(d.vcol + fcol + 4));
@@ -591,6 +590,25 @@ __device__ __forceinline__ void moments_and_update(const StepParams& P, const fl
     }
     if (P.fast_math && !tiny && vmax < INFINITY) update8<true>(P, m1, v1, th, r);
     else update8<false>(P, m1, v1, th, r);
+}
+
+// vhat for 8 elements of one row from preloaded R_i, C_j (8 columns) and
+// {mean(R), RN(1/mean(R))}; the same operations and fallback as factored_vhat.
+__device__ __forceinline__ void factored_vhat_pre(const float Ri, const float4 c0, const float4 c1, const float2 rb,
+                                                  float v1[8]) {
+    const float C[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
+    bool q_fast = rb.x != 0.f && quot_range_ok(rb.x);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        const float p = __fmul_rn(Ri, C[i]);
+        const float q = div_rn_by_rcp(p, rb.x, rb.y);
+        q_fast = q_fast && quot_range_ok(p) && quot_range_ok(q);
+        v1[i] = (rb.x == 0.f) ? 0.f : q;
+    }
+    if (!q_fast) {
+#pragma unroll
+        for (int i = 0; i < 8; ++i) v1[i] = (rb.x == 0.f) ? 0.f : __fdiv_rn(__fmul_rn(Ri, C[i]), rb.x);
+    }
 }
 
 // ----------------------------------------------------------------- one tile, general path
@@ -720,7 +738,7 @@ __device__ __forceinline__ void compute_tile_full(const StepParams& P, const Dev
                                                   const Stage& st, int lane, SmemAll& sm, WarpTables& wt,
                                                   const float my_nf4, const float my_nf4t, const float my_vl,
                                                   const float my_vt, const float my_vl1, const float my_mag,
-                                                  const float clip) {
+                                                  const float clip, const uint32_t f_row, const uint32_t f_col) {
     const int half = lane >> 4, j = lane & 15, hb = half * 16;
     const int64_t blk = pair * 2 + half;
     const int64_t e0 = blk * kBlock + j * 8;
@@ -728,6 +746,24 @@ __device__ __forceinline__ void compute_tile_full(const StepParams& P, const Dev
     const bool fact = (RECIPE == Q4_RECIPE_FACTORED) && (flags & DF_FACTORED);
     const bool m_sr = (flags & DF_M_SR) != 0;
     const uint32_t tb = smem_addr(&wt);   // 256-byte aligned
+
+    // factored v (columns a multiple of 8, at least 256): R_i, the lane's 8
+    // C_j and mean(R) are loaded first, so that their latency overlaps the
+    // decoding; the tile starts at (f_row, f_col), the lane's 8 elements lie
+    // in one row
+    const bool fvec = fact && (flags & DF_CVEC);
+    float f_ri = 0.f;
+    float4 f_c0 = make_float4(0.f, 0.f, 0.f, 0.f), f_c1 = f_c0;
+    float2 f_rb = make_float2(0.f, 0.f);
+    if (RECIPE == Q4_RECIPE_FACTORED && fvec) {
+        const uint32_t cols = (uint32_t)d.cols;
+        uint32_t col = f_col + (uint32_t)(half * kBlock + j * 8), row = f_row;
+        if (col >= cols) { col -= cols; ++row; }
+        f_ri = __ldg(d.vrow + row);
+        f_c0 = __ldg(reinterpret_cast<const float4*>(d.vcol + col));
+        f_c1 = __ldg(reinterpret_cast<const float4*>(d.vcol + col + 4));
+        f_rb = *reinterpret_cast<const float2*>(d.rbar);
+    }
 
     // ---- loads from the stage ---------------------------------------------
     const float sm_old = st.ms[half];
@@ -773,7 +809,8 @@ __device__ __forceinline__ void compute_tile_full(const StepParams& P, const Dev
                                    lds_f32(__byte_perm(vhi, tb, 0x7650 + k)));
         } else {
             float vf[8];
-            factored_vhat(d, e0, 8, vf);
+            if (fvec) factored_vhat_pre(f_ri, f_c0, f_c1, f_rb, vf);
+            else factored_vhat(d, e0, 8, vf);
 #pragma unroll
             for (int k = 0; k < 4; ++k) {
                 v[k] = make_float2(0.f, 0.f);
@@ -1179,6 +1216,19 @@ __global__ void __launch_bounds__(kStepThreads, 1) step_kernel(const __grid_cons
     int64_t c_n = __ldg(P.pair_prefix + t0 + 1) - __ldg(P.pair_prefix + t0);
     reinterpret_cast<uint32_t*>(&ws.desc)[lane] = __ldg(reinterpret_cast<const uint32_t*>(P.tensors + c_t) + lane);
     __syncwarp();
+    // factored recipe: (row, column) of the current tile's first element, for
+    // tensors with DF_CVEC; set by one division per chunk or tensor, then
+    // advanced by 256 columns a tile (at most one wrap, as cols >= 256)
+    uint32_t f_row = 0, f_col = 0;
+    auto fpos = [&]() {
+        if (RECIPE == Q4_RECIPE_FACTORED && (ws.desc.flags & DF_CVEC)) {
+            const int64_t e = c_p * 2 * kBlock;
+            const int64_t r = e / ws.desc.cols;
+            f_row = (uint32_t)r;
+            f_col = (uint32_t)(e - r * ws.desc.cols);
+        }
+    };
+    fpos();
     for (int it = 0; it < n_it; ++it) {
         if (it + kStages - 1 < n_it) issue(it + kStages - 1);
         const int s = it & (kStages - 1);
@@ -1207,11 +1257,12 @@ __global__ void __launch_bounds__(kStepThreads, 1) step_kernel(const __grid_cons
             reinterpret_cast<uint32_t*>(&ws.desc)[lane] =
                 __ldg(reinterpret_cast<const uint32_t*>(P.tensors + c_t) + lane);
             __syncwarp();
+            fpos();
         }
         const bool full = c_p < c_n - 1 || ws.desc.numel - c_p * 2 * kBlock >= 2 * kBlock;
         if (full && !NEXTR) {
             compute_tile_full<RECIPE, URTN, MSR>(P, ws.desc, c_p, ws.st[s], lane, sm, ws.wt, my_nf4, my_nf4t,
-                                                 my_vl, my_vt, my_vl1, my_mag, clip);
+                                                 my_vl, my_vt, my_vl1, my_mag, clip, f_row, f_col);
         } else {
             const int64_t left = ws.desc.numel - c_p * 2 * kBlock;
             compute_tile<RECIPE, URTN, NEXTR>(P, ws.desc, c_p, (full || (left & 7) == 0) ? &ws.st[s] : nullptr,
@@ -1220,6 +1271,10 @@ __global__ void __launch_bounds__(kStepThreads, 1) step_kernel(const __grid_cons
         ++c_p;
         ++c_tile;
         ++c_k;
+        if (RECIPE == Q4_RECIPE_FACTORED) {
+            f_col += 2 * kBlock;
+            if (f_col >= (uint32_t)ws.desc.cols) { f_col -= (uint32_t)ws.desc.cols; ++f_row; }
+        }
         __syncwarp();
     }
 }

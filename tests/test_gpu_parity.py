@@ -115,6 +115,20 @@ def test_factored_small_list():
         assert r["rc"] == 0 and r["theta"] == 0 and r["bf16"] == 0, (t, r)
 
 
+def test_factored_wide_rows():
+    # rows of at least 256 columns take the vector path with the kernel's
+    # incremental (row, column) tracking: widths that are multiples of 256,
+    # and 1000 / 264 (multiples of 8 only), whose tiles straddle rows
+    shapes = [(5, 256), (3, 768), (70, 512), (41, 1000), (9, 264), (300,), (2, 2048), (1, 4096)]
+    w = W.custom("facwide", shapes, "factored", grad="normal", sigma=(1e-3, 1e-3))
+    p = Pair(w.tensors, "factored")
+    for t in range(1, 7):
+        p.step(t, grads_for(w, t))
+        r = p.compare(exact_theta=False)
+        assert r["codes"] == 0 and r["scales"] == 0, (t, r)
+        assert r["rc"] == 0 and r["theta"] == 0 and r["bf16"] == 0, (t, r)
+
+
 def test_sharded_tensor_matches_whole():
     # Two block-aligned shards with elem_offset produce the bits of the whole tensor.
     n, cut = 128 * 9 + 31, 128 * 4
