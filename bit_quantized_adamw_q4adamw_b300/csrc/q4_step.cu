@@ -593,19 +593,42 @@ __device__ __forceinline__ void moments_and_update(const StepParams& P, const fl
 }
 
 // vhat for 8 elements of one row from preloaded R_i, C_j (8 columns) and
-// {mean(R), RN(1/mean(R))}; the same operations and fallback as factored_vhat.
+// {mean(R), RN(1/mean(R))}: p = R_i C_j and q = p / mean(R) with the paired
+// quotient, the same operations and fallback as factored_vhat.  The quotient
+// is exact when every p and q is 0 or in [2^-100, 2^100]; as R_i, C_j >= 0 and
+// both roundings are monotone, that follows from the largest C_j and the
+// smallest nonzero one (the q bounds are taken with a factor-2 margin, as the
+// bounds themselves come from the fast quotient).
 __device__ __forceinline__ void factored_vhat_pre(const float Ri, const float4 c0, const float4 c1, const float2 rb,
                                                   float v1[8]) {
     const float C[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
-    bool q_fast = rb.x != 0.f && quot_range_ok(rb.x);
+    // on the bit patterns of the non-negative C_j: the largest (NaN and +inf
+    // above every finite value) and the smallest nonzero (minus 1; all ones: none)
+    uint32_t cmax_b = 0u, cmin_m1 = 0xffffffffu;
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
-        const float p = __fmul_rn(Ri, C[i]);
-        const float q = div_rn_by_rcp(p, rb.x, rb.y);
-        q_fast = q_fast && quot_range_ok(p) && quot_range_ok(q);
-        v1[i] = (rb.x == 0.f) ? 0.f : q;
+        cmax_b = max(cmax_b, __float_as_uint(C[i]));
+        cmin_m1 = min(cmin_m1, __float_as_uint(C[i]) - 1u);
     }
-    if (!q_fast) {
+    bool q_fast = rb.x != 0.f && quot_range_ok(rb.x);
+    if (Ri != 0.f && cmin_m1 != 0xffffffffu) {
+        const float pmax = __fmul_rn(Ri, __uint_as_float(cmax_b));
+        const float pmin = __fmul_rn(Ri, __uint_as_float(cmin_m1 + 1u));
+        q_fast = q_fast && quot_range_ok(pmax) && quot_range_ok(pmin);
+        if (q_fast) {
+            const float2 qb = div2_rn_by_rcp(make_float2(pmin, pmax), rb.x, rb.y);
+            q_fast = qb.x >= 0x1p-99f && qb.y <= 0x1p99f;
+        }
+    }
+    if (q_fast) {
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            const float2 p = mul2_rn(make_float2(Ri, Ri), make_float2(C[2 * k], C[2 * k + 1]));
+            const float2 q = div2_rn_by_rcp(p, rb.x, rb.y);
+            v1[2 * k] = q.x;
+            v1[2 * k + 1] = q.y;
+        }
+    } else {
 #pragma unroll
         for (int i = 0; i < 8; ++i) v1[i] = (rb.x == 0.f) ? 0.f : __fdiv_rn(__fmul_rn(Ri, C[i]), rb.x);
     }

@@ -87,6 +87,29 @@ __global__ void div_kernel(uint64_t n, uint64_t seed, unsigned long long* count,
     }
 }
 
+// The paired quotient (two dividends, one divisor) against __fdiv_rn, on the
+// same operand distribution as div_kernel; the second dividend is the first
+// scaled by a random power of two in [2^-8, 2^8] (both kept in range).
+__global__ void div2_kernel(uint64_t n, uint64_t seed, unsigned long long* count, unsigned* first) {
+    const uint64_t stride = (uint64_t)gridDim.x * blockDim.x;
+    for (uint64_t i = (uint64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += stride) {
+        const uint32_t u0 = mix(seed * 0x100000000ull + 2 * i), u1 = mix(seed * 0x100000000ull + 2 * i + 1);
+        const uint32_t ea = 35 + (u0 >> 24) % 185, eb = 27 + (u1 >> 24) % 201;
+        uint32_t mb = u1 & 0x7fffffu;
+        if ((i & 3) == 1) mb = 0x7fffffu;
+        const float b = __uint_as_float((eb << 23) | mb);
+        float a = __uint_as_float((ea << 23) | (u0 & 0x7fffffu));
+        if ((i & 3) == 2) a = __uint_as_float(__float_as_uint(__fmul_rn(b, (float)(1 + (u0 & 255)))) + (u0 >> 8 & 3) - 1);
+        const float a2 = __uint_as_float(__float_as_uint(a) + ((int)((u1 >> 8) % 17) - 8) * (1 << 23));
+        const float q1 = __fdiv_rn(a, b), q2 = __fdiv_rn(a2, b);
+        const bool in1 = fabsf(q1) >= 0x1p-100f && fabsf(q1) <= 0x1p100f && fabsf(a) >= 0x1p-100f && fabsf(a) <= 0x1p100f;
+        const bool in2 = fabsf(q2) >= 0x1p-100f && fabsf(q2) <= 0x1p100f && fabsf(a2) >= 0x1p-100f && fabsf(a2) <= 0x1p100f;
+        if (!in1 || !in2) continue;
+        const float2 q = q4::div2_rn_by_rcp(make_float2(a, a2), b, __frcp_rn(b));
+        if (!same(q.x, q1) || !same(q.y, q2)) record(count, first, (unsigned)(i & 0xffffffffu));
+    }
+}
+
 // The paired-arithmetic patterns the step kernel relies on, each against the
 // scalar operations: paired mul, add and fma alone; a single-use paired product
 // finished by a scalar add; a single-use paired product as the addend of a
@@ -127,6 +150,7 @@ extern "C" int fm_check(int which, int variant, uint64_t lo, uint64_t hi, unsign
         case 11: rcp_kernel<1><<<grid, block, 0, s>>>(lo, hi, count, first); break;
         case 12: rcp_kernel<2><<<grid, block, 0, s>>>(lo, hi, count, first); break;
         case 20: div_kernel<<<grid, block, 0, s>>>(hi, lo, count, first); break;
+        case 21: div2_kernel<<<grid, block, 0, s>>>(hi, lo, count, first); break;
         case 30: sqrt2_kernel<<<grid, block, 0, s>>>(lo, hi, count, first); break;
         case 31: rcp2_kernel<<<grid, block, 0, s>>>(lo, hi, count, first); break;
         case 40: pair_ops_kernel<<<grid, block, 0, s>>>(hi, lo, count, first); break;

@@ -84,3 +84,8 @@ def test_paired_patterns_round_like_scalar_ops():
 def test_quotient_random_and_adversarial_pairs():
     n, first = run_check(2, 0, 12345, 1 << 31)
     assert n == 0, f"{n} mismatches, first sample {first}"
+
+
+def test_paired_quotient_random_and_adversarial_pairs():
+    n, first = run_check(2, 1, 54321, 1 << 30)
+    assert n == 0, f"{n} mismatches, first sample {first}"
