@@ -78,6 +78,7 @@ int64_t round_up(int64_t x, int64_t a) { return (x + a - 1) / a * a; }
 // from a zeroed host image every step, which also clears the status word.
 struct Layout {
     int64_t status, desc, pairs, rows, tiles, cols, fids;  // uploaded part
+    int64_t desc2, pairs2;   // factored recipe: descriptors factored-first, and the two subsets' prefixes
     int64_t upload_bytes;
     int64_t rbar, colpart;                         // device-only part
     int64_t total;
@@ -98,6 +99,8 @@ Layout make_layout(const q4adamw_tensor_t* t, int n, int recipe) {
     L.tiles = off; off = round_up(off + (int64_t)(n + 1) * 8, 256);
     L.cols = off;  off = round_up(off + (int64_t)(n + 1) * 8, 256);
     L.fids = off;  off = round_up(off + (int64_t)(n > 0 ? n : 1) * 4, 256);
+    L.desc2 = off; off = round_up(off + (int64_t)n * (int64_t)sizeof(DevTensor), 256);
+    L.pairs2 = off; off = round_up(off + (int64_t)(n + 2) * 8, 256);
     L.upload_bytes = off;
     L.rbar = off;  off = round_up(off + (int64_t)(n > 0 ? n : 1) * 8, 256);   // {mean(R), 1/mean(R)}
     L.colpart = off;
@@ -364,6 +367,25 @@ int step_impl(const q4adamw_tensor_t* t, int n, float lr, float beta1, float bet
             fids[nf++] = i;
         }
     }
+    // Factored recipe with both kinds of tensor: the step runs as two launches,
+    // the factored tensors on an instantiation without the packed-v code, the
+    // others (1-D, packed v) on the general factored-recipe one.  desc2 holds
+    // the descriptors factored-first; pairs2 the two subsets' prefix sums.
+    int n_fact = 0;
+    if (recipe == Q4_RECIPE_FACTORED) {
+        DevTensor* desc2 = reinterpret_cast<DevTensor*>(img.data() + L.desc2);
+        int64_t* pa = reinterpret_cast<int64_t*>(img.data() + L.pairs2);
+        for (int i = 0; i < n; ++i)
+            if (desc[i].flags & q4::DF_FACTORED) desc2[n_fact++] = desc[i];
+        int k = n_fact;
+        for (int i = 0; i < n; ++i)
+            if (!(desc[i].flags & q4::DF_FACTORED)) desc2[k++] = desc[i];
+        pa[0] = 0;
+        for (int i = 0; i < n_fact; ++i) pa[i + 1] = pa[i] + (nblocks(desc2[i].numel) + 1) / 2;
+        int64_t* pb = pa + n_fact + 1;
+        pb[0] = 0;
+        for (int i = n_fact; i < n; ++i) pb[i - n_fact + 1] = pb[i - n_fact] + (nblocks(desc2[i].numel) + 1) / 2;
+    }
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     cudaError_t e = cudaMemcpyAsync(workspace, img.data(), (size_t)L.upload_bytes, cudaMemcpyHostToDevice, s);
     if (e != cudaSuccess) return cuda_fail(e);
@@ -434,6 +456,26 @@ int step_impl(const q4adamw_tensor_t* t, int n, float lr, float beta1, float bet
     if (p.total_pairs == 0) return Q4_OK;
     int dev = 0;
     if ((e = cudaGetDevice(&dev)) != cudaSuccess) return cuda_fail(e);
+    if (recipe == Q4_RECIPE_FACTORED && n_fact > 0) {
+        // factored tensors first (all factored: kRecipeFactoredOnly), then the rest
+        const DevTensor* d2 = reinterpret_cast<const DevTensor*>(ws + L.desc2);
+        const int64_t* pa = reinterpret_cast<const int64_t*>(ws + L.pairs2);
+        const int64_t* ha = reinterpret_cast<const int64_t*>(img.data() + L.pairs2);
+        const int sub_n[2] = {n_fact, n - n_fact};
+        const int64_t sub_pairs[2] = {ha[n_fact], ha[n_fact + 1 + (n - n_fact)]};
+        for (int k = 0; k < 2; ++k) {
+            if (sub_n[k] == 0 || sub_pairs[k] == 0) continue;
+            q4::StepParams ps = p;
+            ps.tensors = d2 + (k == 0 ? 0 : n_fact);
+            ps.pair_prefix = pa + (k == 0 ? 0 : n_fact + 1);
+            ps.n_tensors = sub_n[k];
+            ps.total_pairs = sub_pairs[k];
+            ps.recipe = k == 0 ? q4::kRecipeFactoredOnly : Q4_RECIPE_FACTORED;
+            if (int ce = q4::launch_step(ps, q4::step_grid_size(dev, ps.total_pairs), stream))
+                return cuda_fail((cudaError_t)ce);
+        }
+        return Q4_OK;
+    }
     const int grid = q4::step_grid_size(dev, p.total_pairs);
     if (int ce = q4::launch_step(p, grid, stream)) return cuda_fail((cudaError_t)ce);
     return Q4_OK;

@@ -132,6 +132,13 @@ struct NormParams {
     float* out;                   // the sum of squares
 };
 
+// Kernel-internal recipe value: the factored recipe on a launch whose tensors
+// are all factored (rank >= 2), which compiles without the packed-v code.
+constexpr int kRecipeFactoredOnly = 16;
+__host__ __device__ constexpr bool is_factored_recipe(int recipe) {
+    return recipe == Q4_RECIPE_FACTORED || recipe == kRecipeFactoredOnly;
+}
+
 constexpr int kSlabRows = 256;     // rows per column-partial slab (8 warps x 32 rows)
 constexpr int kSegCols = 256;      // columns per row-partial segment (32 lanes x 8)
 

@@ -650,7 +650,7 @@ __device__ __forceinline__ void compute_tile(const StepParams& P, const DevTenso
     const int64_t rem = numel - e0;
     const int nvalid = rem >= 8 ? 8 : (rem > 0 ? (int)rem : 0);
     const uint32_t flags = d.flags;
-    const bool fact = (RECIPE == Q4_RECIPE_FACTORED) && (flags & DF_FACTORED);
+    const bool fact = is_factored_recipe(RECIPE) && (RECIPE == kRecipeFactoredOnly || (flags & DF_FACTORED));
     const bool m_sr = (flags & DF_M_SR) != 0;
 
     // ---- loads -------------------------------------------------------
@@ -766,7 +766,7 @@ __device__ __forceinline__ void compute_tile_full(const StepParams& P, const Dev
     const int64_t blk = pair * 2 + half;
     const int64_t e0 = blk * kBlock + j * 8;
     const uint32_t flags = d.flags;
-    const bool fact = (RECIPE == Q4_RECIPE_FACTORED) && (flags & DF_FACTORED);
+    const bool fact = is_factored_recipe(RECIPE) && (RECIPE == kRecipeFactoredOnly || (flags & DF_FACTORED));
     const bool m_sr = (flags & DF_M_SR) != 0;
     const uint32_t tb = smem_addr(&wt);   // 256-byte aligned
 
@@ -778,7 +778,7 @@ __device__ __forceinline__ void compute_tile_full(const StepParams& P, const Dev
     float f_ri = 0.f;
     float4 f_c0 = make_float4(0.f, 0.f, 0.f, 0.f), f_c1 = f_c0;
     float2 f_rb = make_float2(0.f, 0.f);
-    if (RECIPE == Q4_RECIPE_FACTORED && fvec) {
+    if (is_factored_recipe(RECIPE) && fvec) {
         const uint32_t cols = (uint32_t)d.cols;
         uint32_t col = f_col + (uint32_t)(half * kBlock + j * 8), row = f_row;
         if (col >= cols) { col -= cols; ++row; }
@@ -1169,7 +1169,7 @@ __global__ void __launch_bounds__(kStepThreads, 1) step_kernel(const __grid_cons
     auto load_issue_tensor = [&]() {
         const DevTensor* dt = P.tensors + i_t;
         i_numel = dt->numel;
-        i_fact = (RECIPE == Q4_RECIPE_FACTORED) && (dt->flags & DF_FACTORED);
+        i_fact = is_factored_recipe(RECIPE) && (RECIPE == kRecipeFactoredOnly || (dt->flags & DF_FACTORED));
         const char* base = *reinterpret_cast<const char* const*>(reinterpret_cast<const char*>(dt) + cp_field);
         i_src = base + cp_first + i_p * cp_step;
         i_bytes = (i_fact && (lane == 3 || lane >= 6)) ? 0u : cp_full;
@@ -1244,7 +1244,7 @@ __global__ void __launch_bounds__(kStepThreads, 1) step_kernel(const __grid_cons
     // advanced by 256 columns a tile (at most one wrap, as cols >= 256)
     uint32_t f_row = 0, f_col = 0;
     auto fpos = [&]() {
-        if (RECIPE == Q4_RECIPE_FACTORED && (ws.desc.flags & DF_CVEC)) {
+        if (is_factored_recipe(RECIPE) && (ws.desc.flags & DF_CVEC)) {
             const int64_t e = c_p * 2 * kBlock;
             const int64_t r = e / ws.desc.cols;
             f_row = (uint32_t)r;
@@ -1294,7 +1294,7 @@ __global__ void __launch_bounds__(kStepThreads, 1) step_kernel(const __grid_cons
         ++c_p;
         ++c_tile;
         ++c_k;
-        if (RECIPE == Q4_RECIPE_FACTORED) {
+        if (is_factored_recipe(RECIPE)) {
             f_col += 2 * kBlock;
             if (f_col >= (uint32_t)ws.desc.cols) { f_col -= (uint32_t)ws.desc.cols; ++f_row; }
         }
@@ -1355,6 +1355,7 @@ int launch_step(const StepParams& p, int grid, void* stream) {
             else Q4_LAUNCH(Q4_RECIPE_ZE_EDEN, false, false, false);
             break;
         case Q4_RECIPE_TORCHAO: Q4_LAUNCH(Q4_RECIPE_TORCHAO, false, false, false); break;
+        case kRecipeFactoredOnly: Q4_LAUNCH(kRecipeFactoredOnly, false, false, false); break;
         default: Q4_LAUNCH(Q4_RECIPE_FACTORED, false, false, false); break;
     }
 #undef Q4_LAUNCH
