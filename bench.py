@@ -202,8 +202,11 @@ def algorithmic_bytes(st, recipe) -> float:
 
 
 def launches_per_step(st, clip: bool = False) -> int:
-    # step kernel; factored statistics (3 kernels); clipping's sum of squares (3 kernels)
-    return 1 + (3 if any(st.is_factored(s) for s in st.slots) else 0) + (3 if clip else 0)
+    # step kernel (two launches when a factored list also holds packed 1-D
+    # tensors); factored statistics (3 kernels); clipping's sum of squares (3)
+    fact = [st.is_factored(s) for s in st.slots if s.numel > 0]
+    step = 2 if (any(fact) and not all(fact)) else 1
+    return step + (3 if any(fact) else 0) + (3 if clip else 0)
 
 
 def time_sqnorm(st, stream, iters: int) -> float:
