@@ -23,7 +23,7 @@ from ._native import (BLOCK, Q4_LM_HEAD_SR_ACTIVE, Q4_M_SR_ALL, Q4_T_FACTORED, Q
 
 __all__ = ["q4adamw_version", "q4adamw_strerror", "q4adamw_state_bytes", "q4adamw_workspace_bytes",
            "q4adamw_state_init", "q4adamw_header_check", "q4adamw_step", "q4adamw_step_noalloc",
-           "q4adamw_dequant_state", "q4adamw_step_status", "q4adamw_grad_sqnorm", "q4adamw_step_clip",
+           "q4adamw_dequant_state", "q4adamw_step_status", "q4adamw_grad_sqnorm", "q4adamw_step_clip", "q4adamw_draws",
            "q4adamw_codebook", "Q4State", "Q4Tensor", "Q4Header", "Q4Error", "RECIPES", "Q4_T_LM_HEAD",
            "Q4_T_FACTORED", "Q4_LM_HEAD_SR_ACTIVE", "Q4_M_SR_ALL", "Q4_V_UPDATE_RTN", "Q4_V_NEXT_R", "BLOCK"]
 
@@ -116,6 +116,14 @@ def q4adamw_step_clip(tensors, lr, beta1, beta2, eps, weight_decay, step, seed, 
                                    ctypes.c_void_p(sqnorm.data_ptr()), ctypes.c_void_p(workspace.data_ptr()),
                                    workspace.numel() * workspace.element_size(), _stream(stream)),
            "q4adamw_step_clip")
+
+
+def q4adamw_draws(seed, step, tensor_id, idx0, purpose, out: torch.Tensor, stream=None) -> None:
+    """The step's Philox words for elements idx0 .. idx0+out.numel()-1 into a
+    device int32/uint32 tensor (purpose 0: m State-SR, 1: v Update-SR)."""
+    assert out.is_cuda and out.element_size() == 4
+    _check(lib().q4adamw_draws(int(seed) & (2 ** 64 - 1), int(step), int(tensor_id), int(idx0), int(purpose),
+                               out.numel(), ctypes.c_void_p(out.data_ptr()), _stream(stream)), "q4adamw_draws")
 
 
 def q4adamw_step_noalloc(tensors, lr, beta1, beta2, eps, weight_decay, step, seed, recipe, flags,

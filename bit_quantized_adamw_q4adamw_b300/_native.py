@@ -65,7 +65,7 @@ _lib = None
 EXPORTS = ("q4adamw_version", "q4adamw_strerror", "q4adamw_last_cuda_error", "q4adamw_state_bytes",
            "q4adamw_workspace_bytes", "q4adamw_state_init", "q4adamw_header_check", "q4adamw_step",
            "q4adamw_dequant_state", "q4adamw_codebook", "q4adamw_step_noalloc", "q4adamw_step_status",
-           "q4adamw_grad_sqnorm", "q4adamw_step_clip")
+           "q4adamw_grad_sqnorm", "q4adamw_step_clip", "q4adamw_draws")
 
 
 def lib():
@@ -95,9 +95,10 @@ def lib():
     L.q4adamw_step_status.argtypes = [P, ctypes.POINTER(U32), P]
     L.q4adamw_grad_sqnorm.argtypes = [TP, I, P, P, I64, P]
     L.q4adamw_step_clip.argtypes = [TP, I, F, F, F, F, F, I64, U64, I, U32, F, P, P, I64, P]
+    L.q4adamw_draws.argtypes = [U64, I64, U32, U64, U32, I64, P, P]
     for name in ("q4adamw_state_bytes", "q4adamw_workspace_bytes", "q4adamw_state_init", "q4adamw_header_check",
                  "q4adamw_step", "q4adamw_dequant_state", "q4adamw_codebook", "q4adamw_step_noalloc",
-                 "q4adamw_step_status", "q4adamw_grad_sqnorm", "q4adamw_step_clip"):
+                 "q4adamw_step_status", "q4adamw_grad_sqnorm", "q4adamw_step_clip", "q4adamw_draws"):
         getattr(L, name).restype = I
     _lib = L
     return L

@@ -447,11 +447,7 @@ int step_impl(const q4adamw_tensor_t* t, int n, float lr, float beta1, float bet
     p.x2_eps = make_float2(p.eps, p.eps);
     p.x2_decay = make_float2(p.decay, p.decay);
     p.x2_neg_step = make_float2(-p.step_size, -p.step_size);   // negation is exact
-    const uint32_t k0 = (uint32_t)seed, k1 = (uint32_t)(seed >> 32);
-    for (int r = 0; r < 10; ++r) {
-        p.round_keys[2 * r] = k0 + (uint32_t)r * 0x9E3779B9u;
-        p.round_keys[2 * r + 1] = k1 + (uint32_t)r * 0xBB67AE85u;
-    }
+    q4::philox_round_keys(seed, p.round_keys);
     p.tab = *tabs;
     if (p.total_pairs == 0) return Q4_OK;
     int dev = 0;
@@ -500,6 +496,16 @@ int q4adamw_step_clip(const q4adamw_tensor_t* t, int n, float lr, float beta1, f
     if (!(max_grad_norm > 0.f) || !std::isfinite(max_grad_norm)) return Q4_EINVAL;
     return step_impl(t, n, lr, beta1, beta2, eps, weight_decay, step, seed, recipe, flags, sqnorm, max_grad_norm,
                      workspace, workspace_bytes, stream);
+}
+
+int q4adamw_draws(uint64_t seed, int64_t step, uint32_t tensor_id, uint64_t idx0, uint32_t purpose, int64_t n,
+                  uint32_t* out, void* stream) {
+    if (n < 0 || (n > 0 && !out) || step < 1 || step > 0xFFFFFFFFll || purpose > 15u) return Q4_EINVAL;
+    if (out && !aligned(out, 4)) return Q4_EALIGN;
+    if (n == 0) return Q4_OK;
+    if (int ce = q4::launch_draws(seed, (uint32_t)step, tensor_id, idx0, purpose, n, out, stream))
+        return cuda_fail((cudaError_t)ce);
+    return Q4_OK;
 }
 
 int q4adamw_grad_sqnorm(const q4adamw_tensor_t* t, int n, float* sqnorm, void* workspace, int64_t workspace_bytes,

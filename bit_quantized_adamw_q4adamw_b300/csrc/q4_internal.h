@@ -142,6 +142,16 @@ __host__ __device__ constexpr bool is_factored_recipe(int recipe) {
 constexpr int kSlabRows = 256;     // rows per column-partial slab (8 warps x 32 rows)
 constexpr int kSegCols = 256;      // columns per row-partial segment (32 lanes x 8)
 
+// Philox4x32-10 key schedule of a 64-bit seed: (k0, k1) of rounds 0..9, the
+// Weyl increments 0x9E3779B9 and 0xBB67AE85 added once per round.
+inline void philox_round_keys(uint64_t seed, uint32_t rk[20]) {
+    const uint32_t k0 = (uint32_t)seed, k1 = (uint32_t)(seed >> 32);
+    for (int r = 0; r < 10; ++r) {
+        rk[2 * r] = k0 + (uint32_t)r * 0x9E3779B9u;
+        rk[2 * r + 1] = k1 + (uint32_t)r * 0xBB67AE85u;
+    }
+}
+
 // Records a cudaError_t for q4adamw_last_cuda_error() and returns Q4_ECUDA.
 int record_cuda_error(int cuda_error);
 
@@ -150,6 +160,8 @@ int launch_step(const StepParams& p, int grid, void* stream);
 int step_grid_size(int device, int64_t total_pairs);
 int launch_factored(const FactoredParams& p, void* stream);
 int launch_grad_sqnorm(const NormParams& p, int device, void* stream);
+int launch_draws(uint64_t seed, uint32_t step, uint32_t tensor_id, uint64_t idx0, uint32_t purpose, int64_t n,
+                 uint32_t* out, void* stream);
 int launch_dequant(const DevTensor& d, int recipe, const float* nf4, const float* vl, float* m_out, float* v_out,
                    void* stream);
 

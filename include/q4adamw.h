@@ -253,6 +253,19 @@ int q4adamw_step_clip(const q4adamw_tensor_t* t, int n, float lr, float beta1, f
                       void* stream);
 
 /*
+ * The stochastic-rounding draws of the step, for checking and reproducing its
+ * rounding: writes to out[0..n) (device, 4-B aligned) the 32-bit Philox4x32-10
+ * words that q4adamw_step draws for elements idx0 .. idx0+n-1 (global element
+ * index = elem_offset + index in the tensor) of tensor tensor_id at step
+ * `step` with `seed`; purpose 0 is the first moment's State-SR, 1 the second
+ * moment's Update-SR.  The uniform is u = (word >> 8) * 2^-24.  Asynchronous
+ * on stream.  Q4_EINVAL for n < 0, out NULL with n > 0, step outside
+ * [1, 2^32), purpose > 15; Q4_EALIGN for a misaligned out.
+ */
+int q4adamw_draws(uint64_t seed, int64_t step, uint32_t tensor_id, uint64_t idx0, uint32_t purpose, int64_t n,
+                  uint32_t* out, void* stream);
+
+/*
  * Status word of the most recent q4adamw_step that used `workspace`
  * (synchronises `stream`, then reads 4 bytes of the workspace).  0 means the
  * step ran to completion.  Bit 0 (Q4_STATUS_STAGE_TIMEOUT) means a warp of the

@@ -178,6 +178,18 @@ def test_clip_entry_points_validate_before_any_device_work():
     assert norm(arr=neg) == _native.Q4_ESHAPE
 
 
+def test_draws_validation_before_any_device_work():
+    L = _native.lib()
+    out = ctypes.c_void_p(1 << 41)
+    assert L.q4adamw_draws(0, 1, 0, 0, 0, -1, out, None) == _native.Q4_EINVAL
+    assert L.q4adamw_draws(0, 1, 0, 0, 0, 8, ctypes.c_void_p(0), None) == _native.Q4_EINVAL
+    assert L.q4adamw_draws(0, 0, 0, 0, 0, 8, out, None) == _native.Q4_EINVAL           # step < 1
+    assert L.q4adamw_draws(0, 2 ** 32, 0, 0, 0, 8, out, None) == _native.Q4_EINVAL     # step >= 2^32
+    assert L.q4adamw_draws(0, 1, 0, 0, 16, 8, out, None) == _native.Q4_EINVAL          # purpose > 15
+    assert L.q4adamw_draws(0, 1, 0, 0, 0, 8, ctypes.c_void_p((1 << 41) + 2), None) == _native.Q4_EALIGN
+    assert L.q4adamw_draws(0, 1, 0, 0, 0, 0, ctypes.c_void_p(0), None) == 0            # nothing to do
+
+
 def test_workspace_covers_the_norm_partials():
     # one huge tensor: few descriptors, many 2048-tile chunk partials
     L = _native.lib()
