@@ -150,14 +150,38 @@ class ClockSampler:
                 "reasons": sorted(reasons), "samples": len(sm)}
 
 
+def _strip_comments(src: str) -> str:
+    """C/C++ source without comments and with whitespace runs collapsed
+    (string and character literals kept as they are)."""
+    out, i, n = [], 0, len(src)
+    while i < n:
+        c = src[i]
+        if c in "\"'":
+            j = i + 1
+            while j < n and src[j] != c:
+                j += 2 if src[j] == "\\" else 1
+            out.append(src[i:j + 1])
+            i = j + 1
+        elif src.startswith("//", i):
+            j = src.find("\n", i)
+            i = n if j < 0 else j
+        elif src.startswith("/*", i):
+            j = src.find("*/", i + 2)
+            i = n if j < 0 else j + 2
+        else:
+            out.append(c)
+            i += 1
+    return " ".join("".join(out).split())
+
+
 def kernel_source_hash() -> str:
-    """Hash of every source of the CUDA library (a traffic record is valid
-    only for the kernel it was measured on)."""
+    """Hash of every source of the CUDA library, comments and layout ignored
+    (a traffic record is valid only for the code it was measured on)."""
     h = hashlib.sha256()
     d = os.path.join(ROOT, "bit_quantized_adamw_q4adamw_b300", "csrc")
     for name in sorted(os.listdir(d)):
-        with open(os.path.join(d, name), "rb") as f:
-            h.update(name.encode() + b"\0" + f.read())
+        with open(os.path.join(d, name), encoding="utf-8") as f:
+            h.update(name.encode() + b"\0" + _strip_comments(f.read()).encode())
     return h.hexdigest()[:16]
 
 

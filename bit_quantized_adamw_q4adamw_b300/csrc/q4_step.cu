@@ -31,13 +31,19 @@
 // root and reciprocal of r = 1/(sqrt(v') c2 + eps) and the factored quotient
 // use the correctly rounded sequences of q4_fastmath.cuh where a lane's
 // inputs are inside their verified domains, and the IEEE intrinsics
-// otherwise.  Block reductions (absmax, the EDEN sums) are half-warp
-// shuffles; per-block tables (dequantisation levels at the old scale,
-// thresholds, levels and ZIP-SR preconditioner levels at the new scale) are
-// built by the 16 lanes of a half in shared memory and read by table lookup.
-// Tiles whose two blocks are complete take a branch-free path (byte-permute
-// decoding, one table entry per code decision); ragged tiles, the LM-head
-// stochastic rounding and scales outside the fast range take the general one.
+// otherwise.  Block absmax is an integer warp reduction (redux.sync) on the
+// bit patterns, the EDEN sums a fixed shuffle tree; per-block tables
+// (dequantisation levels at the old scale, thresholds, levels and ZIP-SR
+// preconditioner levels at the new scale) are built by the 16 lanes of a half
+// in shared memory and read by table lookup.  Tiles whose two blocks are
+// complete take a branch-free path (byte-permute decoding, one table entry
+// per code decision; the LM-head State-SR, the TorchAO first moment and the
+// factored v included); ragged tiles, scales outside the fast range, the
+// Update-RTN and next-step rounding variants take the general one.
+//
+// Instantiations: step_kernel<recipe, Update-RTN, m State-SR present,
+// next-step r>, with the internal recipe kRecipeFactoredOnly for launches
+// whose tensors are all factored.
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
