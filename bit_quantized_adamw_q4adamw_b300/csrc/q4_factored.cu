@@ -5,8 +5,9 @@
 //
 // Three launches, all multi-tensor and deterministic (fixed summation order,
 // no atomics):
-//   stats_kernel    one CTA (8 warps) per tile of 256 rows x 256 columns of a
-//                   tensor: g is read once, 16 bytes (8 BF16) per lane and row.
+//   stats_kernel    persistent CTAs of 8 warps, four per SM, each taking tiles
+//                   of 256 rows x 256 columns of a tensor in turn: g is read
+//                   once, 16 bytes (8 BF16) per lane and row.
 //                   Each lane sums the 8 squares of its row chunk; a warp's 32
 //                   row chunks are reduced across lanes by a transpose tree
 //                   (lane l ends with row l's sum over the 256 columns), giving
@@ -18,7 +19,8 @@
 //                   average R_i <- beta2 R_i + (1-beta2) mean (C_j likewise).
 //   rbar_kernel     one CTA per factored tensor: mean(R) in a fixed tree order,
 //                   stored with its correctly rounded reciprocal.
-// The step kernel then reads vhat_ij = R_i * C_j / mean(R).
+// The step kernel then forms vhat_ij = R_i * C_j / mean(R) per element (with
+// the global-norm clip factor, when given, applied to g before squaring here).
 #include <cuda_runtime.h>
 
 #include <cstdint>
