@@ -225,12 +225,19 @@ def algorithmic_bytes(st, recipe) -> float:
     return total
 
 
-def launches_per_step(st, clip: bool = False) -> int:
-    # step kernel (two launches when a factored list also holds packed 1-D
-    # tensors); factored statistics (3 kernels); clipping's sum of squares (3)
-    fact = [st.is_factored(s) for s in st.slots if s.numel > 0]
-    step = 2 if (any(fact) and not all(fact)) else 1
-    return step + (3 if any(fact) else 0) + (3 if clip else 0)
+def launches_per_step(st, clip: bool = False, flags: int = 0) -> int:
+    # step kernel: two launches when one instantiation does not suit every
+    # tensor (a factored list with packed 1-D tensors; ZIP-SR / ZE-EDEN with
+    # stochastic m rounding on some tensors only); factored statistics (3
+    # kernels); clipping's sum of squares (3)
+    live = [s for s in st.slots if s.numel > 0]
+    fact = [st.is_factored(s) for s in live]
+    if st.recipe in ("zip_sr", "ze_eden"):
+        msr = [bool(flags & 0x2) or bool((s.flags & 0x1) and (flags & 0x1)) for s in live]
+    else:
+        msr = [False]
+    split = (any(fact) and not all(fact)) or (any(msr) and not all(msr))
+    return (2 if split else 1) + (3 if any(fact) else 0) + (3 if clip else 0)
 
 
 def time_sqnorm(st, stream, iters: int) -> float:
@@ -411,7 +418,7 @@ def run_ours(args, rank, world, local):
                      "traffic_source": tr["measured_on"] if tr else "no ncu record for this kernel source",
                      "algorithmic_bytes": alg, "kernel": "step_kernel (one launch per step)",
                      "frac_of_nominal_8tbs": achieved / NOMINAL_HBM_GBS},
-        "gpu_launches": launches_per_step(st, mgn is not None) * args.steps,
+        "gpu_launches": launches_per_step(st, mgn is not None, flags) * args.steps,
         "clocks": clocks,
     }
     if args.variant != "none":

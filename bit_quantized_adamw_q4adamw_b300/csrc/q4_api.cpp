@@ -367,24 +367,30 @@ int step_impl(const q4adamw_tensor_t* t, int n, float lr, float beta1, float bet
             fids[nf++] = i;
         }
     }
-    // Factored recipe with both kinds of tensor: the step runs as two launches,
-    // the factored tensors on an instantiation without the packed-v code, the
-    // others (1-D, packed v) on the general factored-recipe one.  desc2 holds
-    // the descriptors factored-first; pairs2 the two subsets' prefix sums.
-    int n_fact = 0;
-    if (recipe == Q4_RECIPE_FACTORED) {
+    // Two launches where one instantiation does not suit every tensor: under
+    // the factored recipe the factored tensors run on an instantiation without
+    // the packed-v code and the 1-D ones on the general factored one; under
+    // ZIP-SR / ZE-EDEN the tensors whose first moment is rounded
+    // stochastically (the LM head in the final phase) run on the m-SR
+    // instantiation and the rest on the plain one.  desc2 holds the
+    // descriptors of the first group first; pairs2 the two groups' prefix sums.
+    const uint32_t split_bit = recipe == Q4_RECIPE_FACTORED ? (uint32_t)q4::DF_FACTORED
+                               : (recipe == Q4_RECIPE_ZIP_SR || recipe == Q4_RECIPE_ZE_EDEN) ? (uint32_t)q4::DF_M_SR
+                                                                                          : 0u;
+    int n_first = 0;
+    if (split_bit) {
         DevTensor* desc2 = reinterpret_cast<DevTensor*>(img.data() + L.desc2);
         int64_t* pa = reinterpret_cast<int64_t*>(img.data() + L.pairs2);
         for (int i = 0; i < n; ++i)
-            if (desc[i].flags & q4::DF_FACTORED) desc2[n_fact++] = desc[i];
-        int k = n_fact;
+            if (desc[i].flags & split_bit) desc2[n_first++] = desc[i];
+        int k = n_first;
         for (int i = 0; i < n; ++i)
-            if (!(desc[i].flags & q4::DF_FACTORED)) desc2[k++] = desc[i];
+            if (!(desc[i].flags & split_bit)) desc2[k++] = desc[i];
         pa[0] = 0;
-        for (int i = 0; i < n_fact; ++i) pa[i + 1] = pa[i] + (nblocks(desc2[i].numel) + 1) / 2;
-        int64_t* pb = pa + n_fact + 1;
+        for (int i = 0; i < n_first; ++i) pa[i + 1] = pa[i] + (nblocks(desc2[i].numel) + 1) / 2;
+        int64_t* pb = pa + n_first + 1;
         pb[0] = 0;
-        for (int i = n_fact; i < n; ++i) pb[i - n_fact + 1] = pb[i - n_fact] + (nblocks(desc2[i].numel) + 1) / 2;
+        for (int i = n_first; i < n; ++i) pb[i - n_first + 1] = pb[i - n_first] + (nblocks(desc2[i].numel) + 1) / 2;
     }
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     cudaError_t e = cudaMemcpyAsync(workspace, img.data(), (size_t)L.upload_bytes, cudaMemcpyHostToDevice, s);
@@ -452,21 +458,25 @@ int step_impl(const q4adamw_tensor_t* t, int n, float lr, float beta1, float bet
     if (p.total_pairs == 0) return Q4_OK;
     int dev = 0;
     if ((e = cudaGetDevice(&dev)) != cudaSuccess) return cuda_fail(e);
-    if (recipe == Q4_RECIPE_FACTORED && n_fact > 0) {
-        // factored tensors first (all factored: kRecipeFactoredOnly), then the rest
+    // one group empty: the single launch below (the factored recipe with only
+    // factored tensors still takes the factored-only instantiation)
+    const bool split = split_bit != 0u && n_first > 0 && n_first < n;
+    if (recipe == Q4_RECIPE_FACTORED && n_first == n) p.recipe = q4::kRecipeFactoredOnly;
+    if (split) {
         const DevTensor* d2 = reinterpret_cast<const DevTensor*>(ws + L.desc2);
         const int64_t* pa = reinterpret_cast<const int64_t*>(ws + L.pairs2);
         const int64_t* ha = reinterpret_cast<const int64_t*>(img.data() + L.pairs2);
-        const int sub_n[2] = {n_fact, n - n_fact};
-        const int64_t sub_pairs[2] = {ha[n_fact], ha[n_fact + 1 + (n - n_fact)]};
+        const int sub_n[2] = {n_first, n - n_first};
+        const int64_t sub_pairs[2] = {ha[n_first], ha[n_first + 1 + (n - n_first)]};
         for (int k = 0; k < 2; ++k) {
-            if (sub_n[k] == 0 || sub_pairs[k] == 0) continue;
+            if (sub_pairs[k] == 0) continue;
             q4::StepParams ps = p;
-            ps.tensors = d2 + (k == 0 ? 0 : n_fact);
-            ps.pair_prefix = pa + (k == 0 ? 0 : n_fact + 1);
+            ps.tensors = d2 + (k == 0 ? 0 : n_first);
+            ps.pair_prefix = pa + (k == 0 ? 0 : n_first + 1);
             ps.n_tensors = sub_n[k];
             ps.total_pairs = sub_pairs[k];
-            ps.recipe = k == 0 ? q4::kRecipeFactoredOnly : Q4_RECIPE_FACTORED;
+            if (recipe == Q4_RECIPE_FACTORED) ps.recipe = k == 0 ? q4::kRecipeFactoredOnly : Q4_RECIPE_FACTORED;
+            else ps.has_m_sr = k == 0 ? 1 : 0;
             if (int ce = q4::launch_step(ps, q4::step_grid_size(dev, ps.total_pairs), stream))
                 return cuda_fail((cudaError_t)ce);
         }
