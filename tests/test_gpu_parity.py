@@ -104,6 +104,32 @@ def test_degenerate_values():
             _assert_exact(p.compare(), (recipe, t))
 
 
+@pytest.mark.parametrize("recipe,flags", [("zip_sr", 0), ("zip_sr", q4.Q4_LM_HEAD_SR_ACTIVE), ("ze_eden", 0),
+                                          ("torchao", 0), ("factored", 0)])
+def test_empty_tensors_in_the_list(recipe, flags):
+    # zero-size tensors first, in the middle and last (two flagged as the LM
+    # head), around ragged and full ones: the chunk walk skips them and the
+    # two-launch splits put them in either group
+    shapes = [(0,), (300,), (0,), (64, 130), (0,), (1000,), (0,)]
+    fl = [W.T_LM_HEAD, W.T_LM_HEAD, 0, W.T_FACTORED, 0, 0, W.T_LM_HEAD]
+    w = W.custom("empty", shapes, recipe, flags=fl, grad="normal", sigma=(1e-3, 1e-3))
+    p = Pair(w.tensors, recipe)
+    for t in range(1, 4):
+        p.step(t, grads_for(w, t), seed=6, flags=flags)
+        r = p.compare(exact_theta=recipe != "factored")
+        assert r["codes"] == 0 and r["scales"] == 0 and r["theta"] == 0 and r["bf16"] == 0 and r["rc"] == 0, (t, r)
+    assert p.gpu.status() == 0
+
+
+def test_all_empty_list_is_a_no_op():
+    w = W.custom("allempty", [(0,), (0,)], "zip_sr")
+    st = q4.Q4State(w.tensors, "zip_sr")
+    st.init()
+    st.step(1, 1e-3, 0.9, 0.999, 1e-8, 0.1, flags=q4.Q4_LM_HEAD_SR_ACTIVE, max_grad_norm=1.0)
+    torch.cuda.synchronize()
+    assert st.status() == 0 and float(st.sqnorm.cpu()[0]) == 0.0
+
+
 def test_factored_small_list():
     shapes = [(64, 96), (96,), (130, 128), (1, 256), (300, 40), (17,), (33, 64)]
     w = W.custom("fac", shapes, "factored", grad="normal", sigma=(1e-3, 1e-3))
