@@ -178,6 +178,28 @@ def test_clip_entry_points_validate_before_any_device_work():
     assert norm(arr=neg) == _native.Q4_ESHAPE
 
 
+def test_plain_c_client_compiles_links_and_runs(tmp_path):
+    # the ABI from plain C99 (no Python, no torch): header, linking, host calls
+    import os
+    import shutil
+    import subprocess
+    cc = shutil.which("gcc") or shutil.which("cc")
+    if cc is None:
+        pytest.skip("no C compiler")
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    lib = _native.LIB_PATH
+    exe = str(tmp_path / "abi_c_check")
+    subprocess.run([cc, "-std=c99", "-Wall", "-Wextra", "-pedantic", "-Werror",
+                    "-I", os.path.join(root, "include"), os.path.join(root, "tests", "csrc", "abi_c_check.c"),
+                    "-o", exe, lib, "-Wl,-rpath," + os.path.dirname(lib)], check=True)
+    env = dict(os.environ)
+    import torch as _t
+    env["LD_LIBRARY_PATH"] = os.pathsep.join([os.path.join(os.path.dirname(_t.__file__), "lib"),
+                                              env.get("LD_LIBRARY_PATH", "")])
+    out = subprocess.run([exe], capture_output=True, text=True, env=env)
+    assert out.returncode == 0 and out.stdout.strip() == "ok", out.stdout + out.stderr
+
+
 def test_draws_validation_before_any_device_work():
     L = _native.lib()
     out = ctypes.c_void_p(1 << 41)
