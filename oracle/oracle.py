@@ -107,7 +107,9 @@ _cbs = None
 def lib():
     global _lib
     if _lib is None:
-        L = ctypes.CDLL(build())
+        # Q4_ORACLE_LIB: a prebuilt oracle library to load instead (the mutation
+        # tests point it at copies of q4_oracle.c with a planted mistake)
+        L = ctypes.CDLL(os.environ.get("Q4_ORACLE_LIB") or build())
         P, U32, U64, I64, F = ctypes.c_void_p, ctypes.c_uint32, ctypes.c_uint64, ctypes.c_int64, ctypes.c_float
         L.oracle_philox4x32_10.argtypes = [P, P, P]
         L.oracle_draw.argtypes = [U64, U32, U32, U64, U32]

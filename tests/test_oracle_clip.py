@@ -184,3 +184,27 @@ def test_clip_one_is_the_plain_step():
         a.step(gb, h["lr"], h["beta1"], h["beta2"], h["eps"], h["weight_decay"], t, 0, "zip_sr", clip=1.0)
         b.step(gb, h["lr"], h["beta1"], h["beta2"], h["eps"], h["weight_decay"], t, 0, "zip_sr")
         assert np.array_equal(a.param.view(np.uint32), b.param.view(np.uint32))
+
+
+def test_sqnorm_pairing_on_equal_magnitude_tiles():
+    # with squares of one magnitude every pairing choice shows in the rounded
+    # bits: 200 single-tile tensors (and ragged ones) against textbook pairwise
+    rng = np.random.default_rng(77)
+    for k in range(200):
+        n = 256 if k % 4 else int(rng.integers(129, 256))
+        g = bf16_of(rng.normal(0, 1, n))
+        got = O.grad_sqnorm([g])
+        want = textbook_sqnorm([g])
+        assert got.view(np.uint32) == want.view(np.uint32), (k, got, want)
+
+
+def test_sqnorm_lane_pairing_hand_derived():
+    # BF16 squares carry at most 16 significant bits, so most lane sums are
+    # exact whatever the pairing; this case makes the pairing visible.  Lane 0
+    # holds 4096, 1, 2, 3 (squares 2^24, 1, 4, 9), everything else is 0.  The
+    # stated order: (2^24 + 1) rounds to 2^24 (tie to even), 4 + 9 = 13, and
+    # 2^24 + 13 rounds to 2^24 + 12 (tie to even).  Pairing (s0+s2), (s1+s3)
+    # would give 2^24 + 14 exactly; left to right, 2^24 + 12 as well.
+    g = np.zeros(256, np.float32)
+    g[:4] = [4096.0, 1.0, 2.0, 3.0]
+    assert float(O.grad_sqnorm([bf16_of(g)])) == 2.0 ** 24 + 12

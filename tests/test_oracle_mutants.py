@@ -1,0 +1,86 @@
+"""Mutation check of the oracle's pins.
+
+Each case plants one plausible mistake in a copy of oracle/q4_oracle.c (a
+swapped constant, a dropped term, a flipped sign or comparison, a wrong
+operand order), builds it, and runs the pin tests that should notice, with
+the oracle pointed at the mutant (Q4_ORACLE_LIB).  Every mutant must make
+those pins fail; the unmodified source, built the same way, must pass them.
+Nothing here touches a GPU.
+"""
+import os
+import subprocess
+import sys
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+SRC = os.path.join(ROOT, "oracle", "q4_oracle.c")
+
+STEP = "tests/test_oracle_step.py"
+ROUND = "tests/test_oracle_rounding.py"
+PRIM = "tests/test_oracle_primitives.py"
+CLIP = "tests/test_oracle_clip.py"
+
+MUTANTS = {
+    # AdamW recurrences and update
+    "m_uses_beta2": ("float mm = fmaf(s.beta1, m, s.omb1 * g);", "float mm = fmaf(s.beta2, m, s.omb1 * g);", [STEP]),
+    "v_drops_square": ("vv = fmaf(s.beta2, v, s.omb2 * (g * g));", "vv = fmaf(s.beta2, v, s.omb2 * g);", [STEP]),
+    "no_bias_correction": ("return 1.0f / (sqrtf(x) * s->c2 + s->eps);", "return 1.0f / (sqrtf(x) + s->eps);",
+                           [STEP]),
+    "decay_sign": ("float th = T->param[e] * s.decay - s.step_size * (mm * rr);",
+                   "float th = T->param[e] * s.decay + s.step_size * (mm * rr);", [STEP]),
+    # block scale and EDEN
+    "absmax_without_abs": ("float ax = fabsf(x[i]);", "float ax = x[i];", [STEP]),
+    "eden_inverted": ("return s * (A / B);", "return s * (B / A);", [STEP]),
+    # rounding rules
+    "state_sr_direction": ("return (u * (a[k + 1] - a[k]) < (x - a[k])) ? k + 1 : k;",
+                           "return (u * (a[k + 1] - a[k]) > (x - a[k])) ? k + 1 : k;", [ROUND]),
+    "update_sr_gap_sign": ("return (u * (rk - rk1) < (rk - r)) ? k + 1 : k;",
+                           "return (u * (rk - rk1) < (r - rk)) ? k + 1 : k;", [ROUND]),
+    "rtn_tie_up": ("if (x > T[k]) c++;", "if (x >= T[k]) c++;", [ROUND]),
+    # primitives
+    "philox_multiplier": ("(uint64_t)0xD2511F53u * (uint64_t)c0", "(uint64_t)0xD2511F55u * (uint64_t)c0", [PRIM]),
+    "bf16_truncates": ("return (uint16_t)((u + 0x7fffu + lsb) >> 16);", "return (uint16_t)(u >> 16);", [PRIM]),
+    # factored statistics
+    "row_mean_divisor": ("float mean = (float)(acc / (double)cols);", "float mean = (float)(acc / (double)rows);",
+                         [STEP]),
+    # gradient-norm clipping
+    "sqnorm_lane_order": ("q[l] = ((sq[0] + sq[1]) + (sq[2] + sq[3])) + ((sq[4] + sq[5]) + (sq[6] + sq[7]));",
+                          "q[l] = ((sq[0] + sq[2]) + (sq[1] + sq[3])) + ((sq[4] + sq[6]) + (sq[5] + sq[7]));",
+                          [CLIP]),
+    "clip_not_clamped": ("return (c >= 1.0f) ? 1.0f : c;", "return (c >= 1.0f) ? c : 1.0f;", [CLIP]),
+}
+
+
+def _build(src_text: str, out_dir) -> str:
+    c = os.path.join(out_dir, "q4_oracle_mut.c")
+    so = os.path.join(out_dir, "liboracle_mut.so")
+    with open(c, "w") as f:
+        f.write(src_text)
+    subprocess.run(["gcc", "-O2", "-std=c11", "-ffp-contract=off", "-fno-fast-math", "-fPIC", "-shared", "-o", so,
+                    c, "-lm"], check=True)
+    return so
+
+
+def _run_pins(so: str, files):
+    env = dict(os.environ, Q4_ORACLE_LIB=so)
+    return subprocess.run([sys.executable, "-m", "pytest", *files, "-x", "-q", "-m", "not gpu",
+                           "-p", "no:cacheprovider"], cwd=ROOT, env=env, capture_output=True, text=True)
+
+
+def test_unmodified_oracle_passes_the_pins_through_the_override(tmp_path):
+    with open(SRC) as f:
+        so = _build(f.read(), str(tmp_path))
+    r = _run_pins(so, [CLIP, PRIM])
+    assert r.returncode == 0, r.stdout[-2000:]
+
+
+@pytest.mark.parametrize("name", sorted(MUTANTS))
+def test_planted_mistake_fails_a_pin(name, tmp_path):
+    old, new, files = MUTANTS[name]
+    with open(SRC) as f:
+        src = f.read()
+    assert src.count(old) >= 1, f"mutation site for {name} not found"
+    so = _build(src.replace(old, new), str(tmp_path))
+    r = _run_pins(so, files)
+    assert r.returncode == 1, f"{name} survived the pins:\n{r.stdout[-1500:]}"

@@ -367,3 +367,57 @@ def test_v_next_r_rounds_in_the_next_steps_zero_gradient_preconditioner():
         assert np.all(chosen <= np.minimum(d_lo, d_hi) * (1 + 1e-5) + 1e-7 * r)
     # the two preconditioner spaces disagree on some elements
     assert (q != _codes(t_same.v_codes, n)).any()
+
+
+def _decode(packed: np.ndarray, scales: np.ndarray, levels: np.ndarray, n: int) -> np.ndarray:
+    """Stored state -> FP32 values: level[code] * block scale (plain lookup)."""
+    e = np.arange(n)
+    q = (packed[e >> 1] >> (4 * (e & 1))) & 15
+    return (levels[q].astype(np.float32) * scales[e // 128].astype(np.float32)).astype(np.float32)
+
+
+def _fma32(a, b, c):
+    # a*b is exact in float64 (two 24-bit significands); one more rounding
+    # to float32 after the float64 sum (a double rounding only matters at
+    # exact float32 ties, far below the tolerance used with it)
+    return (np.asarray(a, np.float64) * np.asarray(b, np.float64) + np.asarray(c, np.float64)).astype(np.float32)
+
+
+@pytest.mark.parametrize("recipe", ["zip_sr", "ze_eden", "torchao"])
+def test_later_step_is_adamw_on_the_decoded_state(recipe):
+    # From a nonzero quantised state (after steps 1 and 2), step 3 applies the
+    # AdamW recurrences to the decoded moments: m' = fma(b1, m~, (1-b1) g),
+    # v' = fma(b2, v~, (1-b2) g^2), r = 1/(sqrt(v') c2 + eps), and the update;
+    # the stored m is then the nearest level of m' at scale max|m'| (RTN).
+    # Everything is restated here in numpy from the definitions.
+    rng = np.random.default_rng(31)
+    n = 1000
+    gs = [_bf16(rng.normal(0, 1e-3, n) * np.exp(rng.uniform(-2, 2, n))) for _ in range(3)]
+    t = O.OracleTensor.zeros_state(rng.normal(0, 0.02, n).astype(np.float32), 5, recipe=recipe)
+    for k in (1, 2):
+        t.step(gs[k - 1], H["lr"], H["beta1"], H["beta2"], H["eps"], H["wd"], k, 0, recipe)
+    cb = O.codebooks()
+    Lm = cb["sdyn4" if recipe == "torchao" else "nf4"]
+    Lv = cb["dyn4" if recipe == "zip_sr" else "lin4nz" if recipe == "torchao" else "dyn4nz"]
+    m_dec = _decode(t.m_codes, t.m_scale, Lm, n)
+    v_dec = _decode(t.v_codes, t.v_scale, Lv, n)
+    theta = t.param.copy()
+    t.step(gs[2], H["lr"], H["beta1"], H["beta2"], H["eps"], H["wd"], 3, 0, recipe)
+    b1, b2 = np.float32(H["beta1"]), np.float32(H["beta2"])
+    d1, d2, lr, wd = float(b1), float(b2), float(np.float32(H["lr"])), float(np.float32(H["wd"]))
+    omb1, omb2 = np.float32(1.0 - d1), np.float32(1.0 - d2)
+    c2 = np.float32(1.0 / np.sqrt(1.0 - d2 ** 3))
+    step_size = np.float32(lr / (1.0 - d1 ** 3))
+    decay = np.float32(1.0 - lr * wd)
+    g = _from_bf16(gs[2]).astype(np.float32)
+    m1 = _fma32(b1, m_dec, (omb1 * g).astype(np.float32))
+    v1 = _fma32(b2, v_dec, (omb2 * (g * g).astype(np.float32)).astype(np.float32))
+    r = (np.float32(1) / ((np.sqrt(v1) * c2).astype(np.float32) + np.float32(H["eps"]))).astype(np.float32)
+    want = ((theta * decay).astype(np.float32) - (step_size * (m1 * r).astype(np.float32))).astype(np.float32)
+    assert np.all(np.abs(t.param.astype(np.float64) - want) <= 1e-6 * np.maximum(1, np.abs(want)))
+    for b in range(O.nblocks(n)):
+        sl = slice(128 * b, min(128 * b + 128, n))
+        sm = np.abs(m1[sl]).astype(np.float64).max()
+        qm = np.array([(t.m_codes[e >> 1] >> (4 * (e & 1))) & 15 for e in range(sl.start, sl.stop)])
+        dm = np.abs(m1[sl][:, None].astype(np.float64) - Lm[None, :].astype(np.float64) * sm)
+        assert np.all(dm[np.arange(qm.size), qm] <= dm.min(1) + 1e-6 * sm)
