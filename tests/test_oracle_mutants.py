@@ -52,6 +52,16 @@ MUTANTS = {
 }
 
 
+# Mistakes in the Python half of the oracle (the codebook constructions):
+# the pins run from a copy of oracle/ and tests/ with the mistake planted.
+PY_MUTANTS = {
+    "nf4_delta": ("delta = 1.0 - 0.5 * (1.0 / 30.0 + 1.0 / 32.0)", "delta = 1.0 - 0.5 * (1.0 / 30.0 + 1.0 / 31.0)"),
+    "dyn4_fraction_index": ("vals.append(10.0 ** (-e) * (0.1 + 0.9 * (j + 1) / 2 ** f))",
+                            "vals.append(10.0 ** (-e) * (0.1 + 0.9 * j / 2 ** f))"),
+    "sdyn4_left_endpoints": ("mags.append(10.0 ** (i - 2) * (lo + hi) / 2.0)", "mags.append(10.0 ** (i - 2) * lo)"),
+}
+
+
 def _build(src_text: str, out_dir) -> str:
     c = os.path.join(out_dir, "q4_oracle_mut.c")
     so = os.path.join(out_dir, "liboracle_mut.so")
@@ -84,3 +94,28 @@ def test_planted_mistake_fails_a_pin(name, tmp_path):
     so = _build(src.replace(old, new), str(tmp_path))
     r = _run_pins(so, files)
     assert r.returncode == 1, f"{name} survived the pins:\n{r.stdout[-1500:]}"
+
+
+@pytest.mark.parametrize("name", sorted(PY_MUTANTS) + ["unmodified"])
+def test_planted_codebook_mistake_fails_a_pin(name, tmp_path):
+    import shutil
+    old, new = PY_MUTANTS.get(name, ("delta = 1.0 - 0.5", "delta = 1.0 - 0.5"))
+    for d in ("oracle", "tests"):
+        shutil.copytree(os.path.join(ROOT, d), os.path.join(tmp_path, d),
+                        ignore=shutil.ignore_patterns("_build", "__pycache__", "*.so"))
+    cb = os.path.join(tmp_path, "oracle", "codebooks.py")
+    with open(cb) as f:
+        src = f.read()
+    assert src.count(old) == 1, f"mutation site for {name} not found"
+    with open(cb, "w") as f:
+        f.write(src.replace(old, new))
+    with open(SRC) as f:
+        so = _build(f.read(), str(tmp_path))      # the C half unchanged
+    env = dict(os.environ, Q4_ORACLE_LIB=so)
+    r = subprocess.run([sys.executable, "-m", "pytest", "tests/test_oracle_primitives.py", "-x", "-q",
+                        "-m", "not gpu", "-p", "no:cacheprovider", "--rootdir", str(tmp_path)],
+                       cwd=str(tmp_path), env=env, capture_output=True, text=True)
+    if name == "unmodified":                     # the copied tree itself passes
+        assert r.returncode == 0, r.stdout[-1500:]
+    else:
+        assert r.returncode == 1, f"{name} survived the pins:\n{r.stdout[-1500:]}"
