@@ -49,6 +49,19 @@ MUTANTS = {
                           "q[l] = ((sq[0] + sq[2]) + (sq[1] + sq[3])) + ((sq[4] + sq[6]) + (sq[5] + sq[7]));",
                           [CLIP]),
     "clip_not_clamped": ("return (c >= 1.0f) ? 1.0f : c;", "return (c >= 1.0f) ? c : 1.0f;", [CLIP]),
+    "factored_stats_ignore_clip": ("double g = clipped(grad[i * cols + j], clip);",
+                                   "double g = clipped(grad[i * cols + j], 1.0f);", [CLIP]),
+    # draws, phases and variants
+    "draw_purpose_bit": ("(uint32_t)(idx >> 34) | (purpose << 28)", "(uint32_t)(idx >> 34) | (purpose << 27)", [PRIM]),
+    "lm_head_sr_in_every_phase": ("(T->flags & OT_LM_HEAD) && (call_flags & OS_LM_HEAD_SR_ACTIVE) && recipe != OR_TORCHAO",
+                                  "(T->flags & OT_LM_HEAD) && recipe != OR_TORCHAO", [STEP]),
+    "torchao_head_sr": ("(call_flags & OS_LM_HEAD_SR_ACTIVE) && recipe != OR_TORCHAO)",
+                        "(call_flags & OS_LM_HEAD_SR_ACTIVE))", [STEP]),
+    "next_r_same_step_c2": ("s.rc = hn[1];", "s.rc = s.c2;", [STEP]),
+    "update_rtn_direction": ("return ((r - rk1) < (rk - r)) ? k + 1 : k;", "return ((r - rk1) > (rk - r)) ? k + 1 : k;",
+                             [ROUND, STEP]),
+    "column_mean_divisor": ("float mean = (float)(acc / (double)rows);", "float mean = (float)(acc / (double)cols);",
+                            [STEP]),
 }
 
 
