@@ -20,6 +20,7 @@ STEP = "tests/test_oracle_step.py"
 ROUND = "tests/test_oracle_rounding.py"
 PRIM = "tests/test_oracle_primitives.py"
 CLIP = "tests/test_oracle_clip.py"
+FACT = "tests/test_oracle_factored.py"
 
 MUTANTS = {
     # AdamW recurrences and update
@@ -62,6 +63,21 @@ MUTANTS = {
                              [ROUND, STEP]),
     "column_mean_divisor": ("float mean = (float)(acc / (double)rows);", "float mean = (float)(acc / (double)cols);",
                             [STEP]),
+    # factored second moment in the step
+    "factored_vhat_times_rbar": ("(T->v_row[ri] * T->v_col[cj]) / rbar;", "(T->v_row[ri] * T->v_col[cj]) * rbar;",
+                                 [FACT]),
+    "factored_row_column_swap": ("int64_t ri = e / cols, cj = e % cols;", "int64_t ri = e % cols, cj = e / cols;",
+                                 [FACT]),
+    "factored_zero_rbar_gives_one": ("vv = (rbar == 0.0f) ? 0.0f :", "vv = (rbar == 0.0f) ? 1.0f :", [FACT]),
+    "factored_rbar_from_columns": ("for (int64_t i = 0; i < rows; ++i) acc += R[i];",
+                                   "for (int64_t i = 0; i < rows; ++i) acc += C[i % cols];", [FACT]),
+    "factored_1d_v_in_dyn4": (
+        "const float* Lv = (recipe == OR_ZIP_SR) ? cb->dyn4 : (recipe == OR_TORCHAO) ? cb->lin4nz : cb->dyn4nz;\n"
+        "    const float* tv = (recipe == OR_ZIP_SR) ? cb->dyn4_t : (recipe == OR_TORCHAO) ? cb->lin4nz_t : cb->dyn4nz_t;",
+        "const float* Lv = (recipe == OR_ZIP_SR || recipe == OR_FACTORED) ? cb->dyn4 : (recipe == OR_TORCHAO) ? "
+        "cb->lin4nz : cb->dyn4nz;\n"
+        "    const float* tv = (recipe == OR_ZIP_SR || recipe == OR_FACTORED) ? cb->dyn4_t : (recipe == OR_TORCHAO) ? "
+        "cb->lin4nz_t : cb->dyn4nz_t;", [FACT]),
 }
 
 
@@ -94,7 +110,7 @@ def _run_pins(so: str, files):
 def test_unmodified_oracle_passes_the_pins_through_the_override(tmp_path):
     with open(SRC) as f:
         so = _build(f.read(), str(tmp_path))
-    r = _run_pins(so, [CLIP, PRIM])
+    r = _run_pins(so, [CLIP, PRIM, FACT])
     assert r.returncode == 0, r.stdout[-2000:]
 
 
