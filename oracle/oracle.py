@@ -27,7 +27,11 @@ What pins each function (tests under tests/test_oracle_*.py):
     and a float64 numpy closed form.
   * ZE-EDEN scale -- the closed form |y|^2 / <y, yhat> in float64; exactly
     1 on blocks that sit on codebook levels.
-  * Factored v -- brute-force float64 row/column means; rank-1 exactness.
+  * Factored v -- brute-force float64 row/column means; rank-1 exactness;
+    the weights against a float64 restatement of vhat = R_i C_j / mean(R);
+    data-parallel shards (partial sums added over the shards, then the
+    sums-based step) equal the whole-tensor step bit for bit when the sums
+    are exact, and the partial sums equal brute-force float64 sums.
   * Gradient-norm clipping -- the sum of squares against textbook recursive
     pairwise summation (numpy, level by level) and a float64 error bound;
     the factor against torch.nn.utils.clip_grad_norm_ on exact-norm cases;
@@ -130,6 +134,9 @@ def lib():
         L.oracle_step_tensor.restype = ctypes.c_int
         L.oracle_step_tensor_clip.argtypes = [P, P, F, F, F, F, F, I64, U64, ctypes.c_int, U32, F]
         L.oracle_step_tensor_clip.restype = ctypes.c_int
+        L.oracle_factored_partials.argtypes = [P, I64, F, P, P]
+        L.oracle_step_tensor_sums.argtypes = [P, P, I64, P, P, F, F, F, F, F, I64, U64, ctypes.c_int, U32, F]
+        L.oracle_step_tensor_sums.restype = ctypes.c_int
         L.oracle_grad_sqnorm.argtypes = [P, ctypes.c_int, P]
         L.oracle_grad_sqnorm.restype = F
         L.oracle_clip_factor.argtypes = [F, F]
@@ -275,33 +282,87 @@ class OracleTensor:
     v_scale: np.ndarray = None
     v_row: np.ndarray = None
     v_col: np.ndarray = None
+    cols: int = None                  # a shard's parameter column count (None: whole tensor)
     _keep: list = field(default_factory=list)
 
     @classmethod
     def zeros_state(cls, param: np.ndarray, tensor_id: int, rows: int = 1, flags: int = 0,
-                    elem_offset: int = 0, recipe: str = "zip_sr") -> "OracleTensor":
+                    elem_offset: int = 0, recipe: str = "zip_sr", cols: int | None = None) -> "OracleTensor":
+        """cols: for one data-parallel shard of a factored parameter, the
+        parameter's column count (its [rows, cols] matrix holds the shard's
+        elements from elem_offset on); None for a whole tensor."""
         p = np.ascontiguousarray(param, dtype=np.float32).copy()
         n = p.size
         nb = nblocks(n)
         factored = recipe == "factored" and bool(flags & T_FACTORED)
         t = cls(param=p, tensor_id=tensor_id, rows=rows, flags=flags, elem_offset=elem_offset,
                 factored=factored)
+        t.cols = cols
         t.param_bf16 = np.zeros(n, np.uint16)
         t.m_codes = np.zeros(nb * BLOCK // 2, np.uint8)
         t.m_scale = np.zeros(nb, np.float32)
         if factored:
             t.v_row = np.zeros(rows, np.float32)
-            t.v_col = np.zeros(n // rows, np.float32)
+            t.v_col = np.zeros(n // rows if cols is None else cols, np.float32)
         else:
             t.v_codes = np.zeros(nb * BLOCK // 2, np.uint8)
             t.v_scale = np.zeros(nb, np.float32)
         return t
+
+    def _desc(self, g) -> _Tensor:
+        d = _Tensor()
+        d.param = _ptr(self.param)
+        d.grad = _ptr(g)
+        d.param_bf16 = _ptr(self.param_bf16)
+        d.m_codes = _ptr(self.m_codes)
+        d.m_scale = _ptr(self.m_scale)
+        d.v_codes = _ptr(self.v_codes)
+        d.v_scale = _ptr(self.v_scale)
+        d.v_row = _ptr(self.v_row)
+        d.v_col = _ptr(self.v_col)
+        d.numel = self.param.size
+        d.rows = self.rows
+        d.elem_offset = self.elem_offset
+        d.tensor_id = self.tensor_id
+        d.flags = self.flags
+        return d
+
+    def factored_partials(self, grad_bf16: np.ndarray, clip: float | None = None):
+        """This shard's sums of (clip g)^2 per row and per column of the
+        parameter's matrix (float64 arrays of rows and cols entries)."""
+        assert self.factored
+        g = np.ascontiguousarray(grad_bf16, dtype=np.uint16)
+        cols = self.cols if self.cols is not None else self.param.size // self.rows
+        rs = np.zeros(self.rows, np.float64)
+        cs = np.zeros(cols, np.float64)
+        d = self._desc(g)
+        lib().oracle_factored_partials(ctypes.addressof(d), cols, 1.0 if clip is None else clip, _ptr(rs), _ptr(cs))
+        return rs, cs
+
+    def step_sums(self, grad_bf16: np.ndarray, row_sums, col_sums, lr, beta1, beta2, eps, wd, step, seed,
+                  recipe: str, call_flags: int = 0, clip: float | None = None) -> None:
+        """One step of this shard with the factored statistics taken from the
+        sums over all shards (a tensor that is not factored steps as step())."""
+        g = np.ascontiguousarray(grad_bf16, dtype=np.uint16)
+        assert g.size == self.param.size
+        cols = self.cols if self.cols is not None else self.param.size // self.rows
+        rs = np.ascontiguousarray(row_sums, np.float64)
+        cs = np.ascontiguousarray(col_sums, np.float64)
+        assert not self.factored or (rs.size == self.rows and cs.size == cols)
+        d = self._desc(g)
+        cbs = _cb_struct()            # kept alive across the call
+        rc = lib().oracle_step_tensor_sums(ctypes.addressof(cbs), ctypes.addressof(d), cols, _ptr(rs),
+                                           _ptr(cs), lr, beta1, beta2, eps, wd, step, seed, RECIPES[recipe],
+                                           call_flags, 1.0 if clip is None else clip)
+        if rc != 0:
+            raise ValueError(f"oracle_step_tensor_sums failed: {rc}")
 
     def step(self, grad_bf16: np.ndarray, lr, beta1, beta2, eps, wd, step, seed, recipe: str,
              call_flags: int = 0, clip: float | None = None) -> None:
         """One step; ``clip`` (a clip_factor() value) scales every gradient."""
         g = np.ascontiguousarray(grad_bf16, dtype=np.uint16)
         assert g.size == self.param.size
+        assert self.cols is None, "a shard of a factored parameter steps with step_sums()"
         d = _Tensor()
         d.param = _ptr(self.param)
         d.grad = _ptr(g)

@@ -30,6 +30,7 @@
  */
 #include <math.h>
 #include <stdint.h>
+#include <stdlib.h>
 #include <string.h>
 
 #define OB 128 /* block size: AReno docs "4-bit AdamW", State representation */
@@ -338,30 +339,41 @@ void oracle_adamw_fp32(float* theta, const float* grad, float* m, float* v, int6
 /* tensors viewed as [rows, cols] keep row means R and column means C of */
 /* g^2 as exponential averages; vhat_ij = R_i * C_j / mean_i(R_i).        */
 /* Sums run in double (exact per-term g^2 of BF16 inputs), rounded once. */
+/* For data-parallel training the same page has each rank's partial row  */
+/* and column sums combined across the group before the exponential      */
+/* update: factored_partials adds one shard's sums, factored_finalize    */
+/* applies the update from the sums over the whole parameter.            */
 /* ------------------------------------------------------------------ */
 static double clipped(uint16_t h, float clip) {
     float g = bf16_to_f32(h);
     return (double)(clip != 1.0f ? g * clip : g);
 }
 
-static void factored_update(const scal_t* s, const uint16_t* grad, int64_t rows, int64_t cols, float* R, float* C,
-                            float* rbar_out, float clip) {
+/* Adds the squares of the shard's (clipped) gradients to row_sums[rows] and
+ * col_sums[cols].  The shard holds the elements [fbase, fbase + numel) of
+ * the row-major [rows, cols] matrix; grad[e] is its element fbase + e.
+ * Elements are visited in row-major order, so each row's and each column's
+ * terms are added in order of increasing column and row index. */
+static void factored_partials(const uint16_t* grad, int64_t numel, int64_t fbase, int64_t cols, float clip,
+                              double* row_sums, double* col_sums) {
+    for (int64_t e = 0; e < numel; ++e) {
+        int64_t ge = fbase + e;
+        double g = clipped(grad[e], clip);
+        row_sums[ge / cols] += g * g;
+        col_sums[ge % cols] += g * g;
+    }
+}
+
+/* R_i <- fma(beta2, R_i, (1-beta2) * FP32(row_sums[i] / cols)), C_j likewise
+ * with rows; then mean(R) in double, rounded once. */
+static void factored_finalize(const scal_t* s, const double* row_sums, const double* col_sums, int64_t rows,
+                              int64_t cols, float* R, float* C, float* rbar_out) {
     for (int64_t i = 0; i < rows; ++i) {
-        double acc = 0.0;
-        for (int64_t j = 0; j < cols; ++j) {
-            double g = clipped(grad[i * cols + j], clip);
-            acc += g * g;
-        }
-        float mean = (float)(acc / (double)cols);
+        float mean = (float)(row_sums[i] / (double)cols);
         R[i] = fmaf(s->beta2, R[i], s->omb2 * mean);
     }
     for (int64_t j = 0; j < cols; ++j) {
-        double acc = 0.0;
-        for (int64_t i = 0; i < rows; ++i) {
-            double g = clipped(grad[i * cols + j], clip);
-            acc += g * g;
-        }
-        float mean = (float)(acc / (double)rows);
+        float mean = (float)(col_sums[j] / (double)rows);
         C[j] = fmaf(s->beta2, C[j], s->omb2 * mean);
     }
     double acc = 0.0;
@@ -461,25 +473,56 @@ float oracle_clip_factor(float sqnorm, float max_norm) {
     return (c >= 1.0f) ? 1.0f : c;
 }
 
+/* A factored parameter stepped as one shard: its [rows, cols] matrix, the
+ * shard's first element fbase in it, and the sums of squares over every
+ * shard (NULL: the shard is the whole tensor, fbase 0, cols = numel / rows,
+ * and the sums are its own). */
+typedef struct {
+    int64_t cols, fbase;
+    const double *row_sums, *col_sums;
+} shard_t;
+
 static int step_tensor(const oracle_codebooks* cb, const oracle_tensor* T, float lr, float beta1, float beta2,
                        float eps, float wd, int64_t step, uint64_t seed, int recipe, uint32_t call_flags,
-                       float clip);
+                       float clip, const shard_t* sh);
 
 int oracle_step_tensor(const oracle_codebooks* cb, const oracle_tensor* T, float lr, float beta1, float beta2,
                        float eps, float wd, int64_t step, uint64_t seed, int recipe, uint32_t call_flags) {
-    return step_tensor(cb, T, lr, beta1, beta2, eps, wd, step, seed, recipe, call_flags, 1.0f);
+    return step_tensor(cb, T, lr, beta1, beta2, eps, wd, step, seed, recipe, call_flags, 1.0f, NULL);
 }
 
 /* The step with gradients scaled by `clip` (oracle_clip_factor). */
 int oracle_step_tensor_clip(const oracle_codebooks* cb, const oracle_tensor* T, float lr, float beta1, float beta2,
                             float eps, float wd, int64_t step, uint64_t seed, int recipe, uint32_t call_flags,
                             float clip) {
-    return step_tensor(cb, T, lr, beta1, beta2, eps, wd, step, seed, recipe, call_flags, clip);
+    return step_tensor(cb, T, lr, beta1, beta2, eps, wd, step, seed, recipe, call_flags, clip, NULL);
+}
+
+/* Data-parallel factored statistics, one rank's part: adds the sums of
+ * (clip g)^2 of the shard T (elements [T->elem_offset, T->elem_offset +
+ * T->numel) of its parameter's row-major [T->rows, cols] matrix) into
+ * row_sums[T->rows] and col_sums[cols]. */
+void oracle_factored_partials(const oracle_tensor* T, int64_t cols, float clip, double* row_sums,
+                              double* col_sums) {
+    factored_partials(T->grad, T->numel, (int64_t)T->elem_offset, cols, clip, row_sums, col_sums);
+}
+
+/* The step of one shard T of a factored parameter (T->rows rows, `cols`
+ * columns; v_row and v_col hold the whole parameter's R and C), with R and C
+ * updated from the sums over all shards (the sums every rank's
+ * oracle_factored_partials added up); element e of the shard reads R and C
+ * at matrix position T->elem_offset + e.  A tensor that is not factored is
+ * stepped as by oracle_step_tensor_clip. */
+int oracle_step_tensor_sums(const oracle_codebooks* cb, const oracle_tensor* T, int64_t cols, const double* row_sums,
+                            const double* col_sums, float lr, float beta1, float beta2, float eps, float wd,
+                            int64_t step, uint64_t seed, int recipe, uint32_t call_flags, float clip) {
+    shard_t sh = {cols, (int64_t)T->elem_offset, row_sums, col_sums};
+    return step_tensor(cb, T, lr, beta1, beta2, eps, wd, step, seed, recipe, call_flags, clip, &sh);
 }
 
 static int step_tensor(const oracle_codebooks* cb, const oracle_tensor* T, float lr, float beta1, float beta2,
                        float eps, float wd, int64_t step, uint64_t seed, int recipe, uint32_t call_flags,
-                       float clip) {
+                       float clip, const shard_t* sh) {
     if (step < 1 || T->numel < 0) return -1;
     scal_t s = make_scalars(lr, beta1, beta2, eps, wd, step);
     const int factored = (recipe == OR_FACTORED) && (T->flags & OT_FACTORED);
@@ -495,12 +538,21 @@ static int step_tensor(const oracle_codebooks* cb, const oracle_tensor* T, float
         s.rb = beta2;
         s.rc = hn[1];
     }
-    int64_t cols = 0;
+    int64_t cols = 0, fbase = 0;
     float rbar = 0.0f;
-    if (factored) {
+    if (factored && sh == NULL) {
         if (T->rows < 1 || T->numel % T->rows) return -3;
         cols = T->numel / T->rows;
-        factored_update(&s, T->grad, T->rows, cols, T->v_row, T->v_col, &rbar, clip);
+        double* rs = (double*)calloc((size_t)(T->rows + cols + 1), sizeof(double));
+        if (!rs) return -2;
+        factored_partials(T->grad, T->numel, 0, cols, clip, rs, rs + T->rows);
+        factored_finalize(&s, rs, rs + T->rows, T->rows, cols, T->v_row, T->v_col, &rbar);
+        free(rs);
+    } else if (factored) {
+        if (T->rows < 1 || sh->cols < 1 || sh->fbase < 0 || sh->fbase + T->numel > T->rows * sh->cols) return -3;
+        cols = sh->cols;
+        fbase = sh->fbase;
+        factored_finalize(&s, sh->row_sums, sh->col_sums, T->rows, cols, T->v_row, T->v_col, &rbar);
     }
     /* Listing page Table 2: ZIP-SR v in Dyn4, ZE-EDEN v in Dyn4-NZ, TorchAO
      * v in Lin4-NZ and m in SDyn4; AReno docs: factored 1-D v excludes zero. */
@@ -525,7 +577,7 @@ static int step_tensor(const oracle_codebooks* cb, const oracle_tensor* T, float
             float mm = fmaf(s.beta1, m, s.omb1 * g);
             float vv;
             if (factored) {
-                int64_t ri = e / cols, cj = e % cols;
+                int64_t ri = (fbase + e) / cols, cj = (fbase + e) % cols;
                 vv = (rbar == 0.0f) ? 0.0f : (T->v_row[ri] * T->v_col[cj]) / rbar;
             } else {
                 float v = Lv[code_at(T->v_codes, e)] * sv_old;

@@ -231,3 +231,78 @@ def test_factored_1d_tensor_stores_nearest_zero_excluding_level():
     v2 = s["b2"] * v_dec + (1 - s["b2"]) * gf2 * gf2
     want = theta * s["decay"] - s["step_size"] * m1 / (np.sqrt(v2) * s["c2"] + H["eps"])
     assert np.all(np.abs(t.param - want) <= 1e-6 * np.maximum(1.0, np.abs(want)))
+
+
+# ------------------------------------------------- data-parallel shards
+# AReno docs "State representation": for data-parallel training the partial
+# row and column sums are combined across the group before the exponential
+# update.  A shard is a block-aligned run of the flattened parameter (it may
+# start and end inside a row); every rank keeps the whole R and C.
+
+def _exact_grad(n, rng, scale=2.0 ** -12):
+    # small integers times a power of two: the squares and every sum of them
+    # are exact in float64, so the order of the additions cannot matter
+    return _bf16(rng.integers(-200, 201, n).astype(np.float64) * scale)
+
+
+def test_shard_partials_equal_brute_force_sums():
+    rows, cols = 40, 200
+    n = rows * cols
+    rng = np.random.default_rng(16)
+    g = _bf16(rng.normal(0, 1e-3, n))
+    gf = _from_bf16(g).astype(np.float64)
+    for lo, hi in ((0, 128 * 7), (128 * 7, 128 * 33), (128 * 33, n)):
+        t = O.OracleTensor.zeros_state(np.zeros(hi - lo, np.float32), 0, rows=rows, flags=O.T_FACTORED,
+                                       elem_offset=lo, recipe="factored", cols=cols)
+        rs, cs = t.factored_partials(g[lo:hi])
+        e = np.arange(lo, hi)
+        want_r = np.bincount(e // cols, weights=gf[lo:hi] ** 2, minlength=rows)
+        want_c = np.bincount(e % cols, weights=gf[lo:hi] ** 2, minlength=cols)
+        assert np.allclose(rs, want_r, rtol=1e-14, atol=0) and np.allclose(cs, want_c, rtol=1e-14, atol=0)
+        assert np.all(rs[: lo // cols] == 0) and np.all(rs[(hi - 1) // cols + 1:] == 0)
+
+
+@pytest.mark.parametrize("flags,call_flags", [(O.T_FACTORED, 0), (O.T_FACTORED | O.T_LM_HEAD, O.LM_HEAD_SR_ACTIVE)])
+def test_sharded_factored_steps_equal_the_whole_tensor(flags, call_flags):
+    # three shards cut inside rows (cols = 200); each step: every shard's
+    # partial sums are added up, then each shard steps from the sums.  With
+    # exact sums the shards reproduce the whole-tensor step bit for bit.
+    rows, cols = 48, 200
+    n = rows * cols
+    cuts = [0, 128 * 23, 128 * 50, n]
+    rng = np.random.default_rng(17)
+    th0 = rng.normal(0, 0.02, n).astype(np.float32)
+    whole = O.OracleTensor.zeros_state(th0, 7, rows=rows, flags=flags, recipe="factored")
+    shards = [O.OracleTensor.zeros_state(th0[a:b], 7, rows=rows, flags=flags, elem_offset=a, recipe="factored",
+                                         cols=cols) for a, b in zip(cuts, cuts[1:])]
+    for step in range(1, 4):
+        g = _exact_grad(n, rng)
+        whole.step(g, H["lr"], H["beta1"], H["beta2"], H["eps"], H["wd"], step, 3, "factored", call_flags)
+        rs = np.zeros(rows)
+        cs = np.zeros(cols)
+        for sh, a, b in zip(shards, cuts, cuts[1:]):
+            r, c = sh.factored_partials(g[a:b])
+            rs += r
+            cs += c
+        for sh, a, b in zip(shards, cuts, cuts[1:]):
+            sh.step_sums(g[a:b], rs, cs, H["lr"], H["beta1"], H["beta2"], H["eps"], H["wd"], step, 3, "factored",
+                         call_flags)
+            assert np.array_equal(sh.param.view(np.uint32), whole.param[a:b].view(np.uint32)), (step, a)
+            assert np.array_equal(sh.param_bf16, whole.param_bf16[a:b]), (step, a)
+            assert np.array_equal(sh.m_codes, whole.m_codes[a // 2:b // 2 + (b - a) % 2]), (step, a)
+            assert np.array_equal(sh.m_scale, whole.m_scale[a // 128:(b + 127) // 128]), (step, a)
+            assert np.array_equal(sh.v_row, whole.v_row) and np.array_equal(sh.v_col, whole.v_col), (step, a)
+
+
+def test_shard_step_of_a_packed_tensor_is_the_plain_step():
+    n = 128 * 9
+    rng = np.random.default_rng(18)
+    th0 = rng.normal(0, 0.02, n).astype(np.float32)
+    a = O.OracleTensor.zeros_state(th0, 2, elem_offset=256, recipe="factored")
+    b = O.OracleTensor.zeros_state(th0, 2, elem_offset=256, recipe="factored")
+    for step in (1, 2):
+        g = _bf16(rng.normal(0, 1e-3, n))
+        a.step(g, H["lr"], H["beta1"], H["beta2"], H["eps"], H["wd"], step, 0, "factored")
+        b.step_sums(g, np.zeros(1), np.zeros(1), H["lr"], H["beta1"], H["beta2"], H["eps"], H["wd"], step, 0,
+                    "factored")
+        assert np.array_equal(a.param, b.param) and np.array_equal(a.v_codes, b.v_codes)

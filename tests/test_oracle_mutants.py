@@ -43,15 +43,16 @@ MUTANTS = {
     "philox_multiplier": ("(uint64_t)0xD2511F53u * (uint64_t)c0", "(uint64_t)0xD2511F55u * (uint64_t)c0", [PRIM]),
     "bf16_truncates": ("return (uint16_t)((u + 0x7fffu + lsb) >> 16);", "return (uint16_t)(u >> 16);", [PRIM]),
     # factored statistics
-    "row_mean_divisor": ("float mean = (float)(acc / (double)cols);", "float mean = (float)(acc / (double)rows);",
+    "row_mean_divisor": ("float mean = (float)(row_sums[i] / (double)cols);",
+                         "float mean = (float)(row_sums[i] / (double)rows);",
                          [STEP]),
     # gradient-norm clipping
     "sqnorm_lane_order": ("q[l] = ((sq[0] + sq[1]) + (sq[2] + sq[3])) + ((sq[4] + sq[5]) + (sq[6] + sq[7]));",
                           "q[l] = ((sq[0] + sq[2]) + (sq[1] + sq[3])) + ((sq[4] + sq[6]) + (sq[5] + sq[7]));",
                           [CLIP]),
     "clip_not_clamped": ("return (c >= 1.0f) ? 1.0f : c;", "return (c >= 1.0f) ? c : 1.0f;", [CLIP]),
-    "factored_stats_ignore_clip": ("double g = clipped(grad[i * cols + j], clip);",
-                                   "double g = clipped(grad[i * cols + j], 1.0f);", [CLIP]),
+    "factored_stats_ignore_clip": ("double g = clipped(grad[e], clip);", "double g = clipped(grad[e], 1.0f);",
+                                   [CLIP]),
     # draws, phases and variants
     "draw_purpose_bit": ("(uint32_t)(idx >> 34) | (purpose << 28)", "(uint32_t)(idx >> 34) | (purpose << 27)", [PRIM]),
     "lm_head_sr_in_every_phase": ("(T->flags & OT_LM_HEAD) && (call_flags & OS_LM_HEAD_SR_ACTIVE) && recipe != OR_TORCHAO",
@@ -61,13 +62,18 @@ MUTANTS = {
     "next_r_same_step_c2": ("s.rc = hn[1];", "s.rc = s.c2;", [STEP]),
     "update_rtn_direction": ("return ((r - rk1) < (rk - r)) ? k + 1 : k;", "return ((r - rk1) > (rk - r)) ? k + 1 : k;",
                              [ROUND, STEP]),
-    "column_mean_divisor": ("float mean = (float)(acc / (double)rows);", "float mean = (float)(acc / (double)cols);",
+    "column_mean_divisor": ("float mean = (float)(col_sums[j] / (double)rows);",
+                            "float mean = (float)(col_sums[j] / (double)cols);",
                             [STEP]),
     # factored second moment in the step
     "factored_vhat_times_rbar": ("(T->v_row[ri] * T->v_col[cj]) / rbar;", "(T->v_row[ri] * T->v_col[cj]) * rbar;",
                                  [FACT]),
-    "factored_row_column_swap": ("int64_t ri = e / cols, cj = e % cols;", "int64_t ri = e % cols, cj = e / cols;",
-                                 [FACT]),
+    "factored_row_column_swap": ("int64_t ri = (fbase + e) / cols, cj = (fbase + e) % cols;",
+                                 "int64_t ri = (fbase + e) % cols, cj = (fbase + e) / cols;", [FACT]),
+    # data-parallel shards of a factored parameter
+    "shard_step_ignores_offset": ("int64_t ri = (fbase + e) / cols, cj = (fbase + e) % cols;",
+                                  "int64_t ri = e / cols, cj = e % cols;", [FACT]),
+    "shard_partials_ignore_offset": ("int64_t ge = fbase + e;", "int64_t ge = e;", [FACT]),
     "factored_zero_rbar_gives_one": ("vv = (rbar == 0.0f) ? 0.0f :", "vv = (rbar == 0.0f) ? 1.0f :", [FACT]),
     "factored_rbar_from_columns": ("for (int64_t i = 0; i < rows; ++i) acc += R[i];",
                                    "for (int64_t i = 0; i < rows; ++i) acc += C[i % cols];", [FACT]),
