@@ -421,3 +421,49 @@ def test_later_step_is_adamw_on_the_decoded_state(recipe):
         qm = np.array([(t.m_codes[e >> 1] >> (4 * (e & 1))) & 15 for e in range(sl.start, sl.stop)])
         dm = np.abs(m1[sl][:, None].astype(np.float64) - Lm[None, :].astype(np.float64) * sm)
         assert np.all(dm[np.arange(qm.size), qm] <= dm.min(1) + 1e-6 * sm)
+
+
+@pytest.mark.parametrize("recipe", ["zip_sr", "ze_eden", "torchao", "factored"])
+def test_gradient_square_overflow_follows_ieee_fp32(recipe):
+    # The pages say nothing about overflow; the step is its definitions
+    # evaluated in IEEE FP32 with no special case.  Hand-derived consequences
+    # for a block whose gradients are ~1e25 (g*g overflows to +inf) next to a
+    # block of ordinary ones, first step from the zero state (1-D tensor, so
+    # the factored recipe keeps packed Dyn4-NZ v):
+    #   v' = fma(b2, 0, (1-b2) inf) = +inf  =>  r = 1 / (inf c2 + eps) = 0,
+    #   theta' = theta decay - step (m' 0) = theta decay exactly (m' finite);
+    #   block scale s_v = +inf; the scaled levels are L_k inf = +inf for
+    #   L_k > 0 and 0 inf = NaN for a zero level, the RTN thresholds all +inf.
+    #   ZIP-SR (Dyn4, L_0 = 0): an inf element's cell is 15 (code 15); a
+    #     finite one has no level <= it, cell 0, r_0 = r(NaN) = NaN, so the
+    #     SR comparison is false: code 0.  Stored s_v = +inf.
+    #   RTN recipes: x > +inf never holds: every code 0.  ZE-EDEN's EDEN sums
+    #     see y = inf * (1/inf) = NaN: stored s_v = NaN; TorchAO and factored
+    #     1-D v (no EDEN) store +inf.
+    #   The first moment stays finite: its codes and scale are ordinary.
+    n = 512
+    rng = np.random.default_rng(21)
+    g = rng.normal(0, 1e-3, n)
+    g[128:256] = rng.normal(0, 1, 128) * 1e25            # every square overflows
+    g[256:384] = np.where(np.arange(128) % 2 == 0, rng.normal(0, 1, 128) * 1e25, rng.normal(0, 1e-3, 128))
+    gb = _bf16(g)
+    gf = _from_bf16(gb).astype(np.float32)
+    with np.errstate(over="ignore"):
+        over = np.isinf((gf * gf).astype(np.float32))
+    assert over[128:256].all() and over[256:384].sum() == 64 and not over[:128].any() and not over[384:].any()
+    theta0, t = _one_tensor_steps(recipe, n, 1, lambda k: gb)
+    h = O.host_scalars(H["lr"], H["beta1"], H["beta2"], H["wd"], 1)
+    assert np.array_equal(t.param[over], (theta0[over] * np.float32(h["decay"])).astype(np.float32))
+    assert np.all(np.isfinite(t.param)) and np.all(np.isfinite(t.m_scale)) and np.all(t.m_scale[1:3] > 1e20)
+    q = np.array([(t.v_codes[e >> 1] >> (4 * (e & 1))) & 15 for e in range(n)])
+    for b in (1, 2):
+        sl = slice(128 * b, 128 * b + 128)
+        if recipe == "zip_sr":
+            assert np.array_equal(q[sl], np.where(over[sl], 15, 0))
+        else:
+            assert np.all(q[sl] == 0)
+        if recipe == "ze_eden":
+            assert np.isnan(t.v_scale[b])
+        else:
+            assert t.v_scale[b] == np.inf
+    assert np.all(np.isfinite(t.v_scale[[0, 3]]))
