@@ -51,7 +51,7 @@ def parse():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--workload", default="llama8b_zipsr")
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--e2e-steps", type=int, default=3)
+    ap.add_argument("--e2e-steps", type=int, default=10)
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0, help="target oracle time of the CPU sample")
@@ -323,26 +323,40 @@ def get_workload(args):
     return w
 
 
+def workload_config(w, world) -> dict:
+    """The workload as both arms name it in their JSON lines."""
+    alg = sum(s.numel * (BYTES_PER_PARAM_FACTORED if (w.recipe == "factored" and s.flags & 0x2) else BYTES_PER_PARAM)
+              for s in w.tensors)
+    return {"workload": w.name, "params": w.numel, "tensors": len(w.tensors), "recipe": w.recipe,
+            "lm_head_sr": w.lm_head_sr, "parallelism": f"replicas{world}",
+            "l2": f"inputs larger than L2 ({alg / 1e9:.1f} GB per step)"}
+
+
 def run_reference(args, rank, world):
+    """The oracle, single-threaded, each step a bounded sample of the workload.
+    Everything reported is measured on that sample: params/s is the sample's
+    parameters over the oracle's time, ms_per_step the oracle's time per step
+    (sample_params_per_step parameters, not the whole workload)."""
     if rank != 0:
         return
     w = get_workload(args)
     per_step = max(args.cpu_seconds / max(args.steps, 1), 0.5)
-    vals, secs_total, desc, n = [], 0.0, "", 0
+    secs_total, desc, n = 0.0, "", 0
     for k in range(args.warmup + args.steps):
         v, desc, n, secs = oracle_sample(w, per_step if k >= args.warmup else 0.2)
         if k >= args.warmup:
-            vals.append(v)
             secs_total += secs
-    value = len(vals) * n / secs_total if secs_total > 0 else 0.0
+    value = args.steps * n / secs_total if secs_total > 0 else 0.0
+    cpu = {"value": value, "unit": "params/s", "cores": 1, "host_cores": os.cpu_count(), "kind": "oracle",
+           "sample": f"each step: {desc}; {secs_total:.2f} s of oracle time over {args.steps} steps"}
     line = {
         "impl": "reference", "metric": "optimizer-step params/sec", "value": value, "unit": "params/s",
         "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
-        "ms_per_step": 1e3 * w.numel / value if value else None, "higher_is_better": True, "scaling": "weak",
+        "ms_per_step": 1e3 * secs_total / args.steps if args.steps else None,
+        "sample_params_per_step": n, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f32", "data": "synthetic",
-        "config": {"workload": w.name, "params": w.numel, "tensors": len(w.tensors), "recipe": w.recipe},
-        "cpu_baseline": {"value": value, "unit": "params/s", "cores": 1, "kind": "oracle",
-                         "sample": f"each step: {desc}"},
+        "config": workload_config(w, world),
+        "cpu_baseline": cpu,
         "e2e": {"value": value, "unit": "params/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
@@ -413,11 +427,9 @@ def run_ours(args, rank, world, local):
         "metric": "optimizer-step params/sec", "value": value, "unit": "params/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
-        "config": {"workload": w.name, "params": w.numel, "tensors": len(w.tensors), "recipe": w.recipe,
-                   "lm_head_sr": w.lm_head_sr, "parallelism": f"replicas{world}",
-                   "l2": f"inputs larger than L2 ({alg / 1e9:.1f} GB per step)",
-                   "step_ms_median": statistics.median(per), "step_ms_p10": sorted(per)[len(per) // 10],
-                   "step_ms_p90": sorted(per)[min(len(per) - 1, (9 * len(per)) // 10)]},
+        "config": workload_config(w, world),
+        "step_ms": {"median": statistics.median(per), "p10": sorted(per)[len(per) // 10],
+                    "p90": sorted(per)[min(len(per) - 1, (9 * len(per)) // 10)]},
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
                      "peak_kind": f"{peak_kind} copy bandwidth (MEASURED_PEAKS.json hbm_gbs)"
                      if peak_kind == "measured" else "fallback 6.4 TB/s",
@@ -446,8 +458,8 @@ def run_ours(args, rank, world, local):
         line["e2e"] = e2e
     if not args.no_cpu_baseline:
         v, desc, n, secs = oracle_sample(w, args.cpu_seconds)
-        line["cpu_baseline"] = {"value": v, "unit": "params/s", "cores": 1, "kind": "oracle",
-                                "sample": f"{desc}; {secs:.1f} s single-threaded"}
+        line["cpu_baseline"] = {"value": v, "unit": "params/s", "cores": 1, "host_cores": os.cpu_count(),
+                                "kind": "oracle", "sample": f"{desc}; {secs:.1f} s single-threaded"}
     print(json.dumps(line), flush=True)
 
 
