@@ -15,6 +15,7 @@ namespace {
 using q4::DevTensor;
 
 thread_local int g_last_cuda = 0;
+thread_local long long g_wait_cycles = q4::kDefaultWaitCycles;   // q4adamw_set_stage_wait_limit
 
 int cuda_fail(cudaError_t e) {
     g_last_cuda = (int)e;
@@ -42,19 +43,21 @@ int v_book(int recipe) {
     return recipe == Q4_RECIPE_ZIP_SR ? 1 : recipe == Q4_RECIPE_TORCHAO ? 4 : 2;
 }
 
-// Shape-only checks (host-only entry points).
-int check_shape(const q4adamw_tensor_t& t, int recipe) {
+// Shape-only checks (host-only entry points).  A data-parallel shard of a
+// factored parameter (dp) need not hold whole rows: check_dp checks its
+// parameter's shape instead.
+int check_shape(const q4adamw_tensor_t& t, int recipe, bool dp = false) {
     if (t.numel < 0) return Q4_ESHAPE;
     if (t.elem_offset % q4::kBlock) return Q4_ESHAPE;
-    if (is_factored(t, recipe)) {
+    if (is_factored(t, recipe) && !dp) {
         if (t.rows < 1 || (t.numel > 0 && t.numel % t.rows)) return Q4_ESHAPE;
     }
     return Q4_OK;
 }
 
 // Full pointer checks for calls that touch device memory.
-int check_tensor(const q4adamw_tensor_t& t, int recipe, bool need_grad) {
-    int rc = check_shape(t, recipe);
+int check_tensor(const q4adamw_tensor_t& t, int recipe, bool need_grad, bool dp = false) {
+    int rc = check_shape(t, recipe, dp);
     if (rc) return rc;
     if (t.numel == 0) return Q4_OK;
     if (!t.param || !t.m_codes || !t.m_scale) return Q4_EINVAL;
@@ -74,6 +77,55 @@ int check_tensor(const q4adamw_tensor_t& t, int recipe, bool need_grad) {
 
 int64_t round_up(int64_t x, int64_t a) { return (x + a - 1) / a * a; }
 
+int64_t n_slabs(int64_t rows) { return (rows + q4::kSlabRows - 1) / q4::kSlabRows; }
+int64_t n_segs(int64_t cols) { return (cols + q4::kSegCols - 1) / q4::kSegCols; }
+
+// Where a factored tensor's elements sit in its parameter's [rows, cols]
+// matrix.  A whole tensor (full_numel NULL) is the matrix [rows, numel/rows]
+// from element 0; a data-parallel shard holds the elements [elem_offset,
+// elem_offset + numel) of the matrix [rows, full_numel[i] / rows].  `fact`:
+// the tensor keeps factored statistics in this call (a shard does even when
+// it holds no element, as every rank updates the replicated R and C).
+struct Geo {
+    bool fact = false;
+    int64_t rows = 0, cols = 0, fbase = 0;
+    int64_t tiles = 0, partials = 0;   // statistics-pass tiles and partial-sum floats
+};
+
+Geo geometry(const q4adamw_tensor_t& t, int recipe, const int64_t* full_numel, int i) {
+    Geo g;
+    const int64_t full = full_numel ? full_numel[i] : t.numel;
+    if (!is_factored(t, recipe) || full <= 0 || t.rows < 1) return g;
+    g.fact = true;
+    g.rows = t.rows;
+    g.cols = full / t.rows;
+    g.fbase = full_numel ? (int64_t)t.elem_offset : 0;
+    int64_t r_first = 0, cov = 0;
+    if (t.numel > 0) q4::covered_rows(g.fbase, t.numel, g.cols, &r_first, &cov);
+    g.tiles = n_slabs(cov) * n_segs(g.cols);
+    g.partials = n_slabs(cov) * g.cols + cov * n_segs(g.cols);
+    return g;
+}
+
+// Data-parallel calls: the shape checks of a shard of a factored parameter
+// (its matrix [rows, full_numel[i] / rows] holds the shard's elements
+// [elem_offset, elem_offset + numel)), and R and C present even in a shard
+// that holds no element.
+int check_dp(const q4adamw_tensor_t* t, int n, int recipe, const int64_t* full_numel) {
+    if (!full_numel) return Q4_OK;
+    for (int i = 0; i < n; ++i) {
+        if (!is_factored(t[i], recipe)) continue;
+        const int64_t full = full_numel[i];
+        if (full < 0 || t[i].rows < 1 || (full > 0 && full % t[i].rows)) return Q4_ESHAPE;
+        if ((int64_t)t[i].elem_offset > full || t[i].numel > full - (int64_t)t[i].elem_offset) return Q4_ESHAPE;
+        if (full > 0) {
+            if (!t[i].v_row || !t[i].v_col) return Q4_EINVAL;
+            if (!aligned(t[i].v_row, 4) || !aligned(t[i].v_col, 4)) return Q4_EALIGN;
+        }
+    }
+    return Q4_OK;
+}
+
 // Workspace layout, all offsets 256-B aligned.  The uploaded part is rewritten
 // from a zeroed host image every step, which also clears the status word.
 struct Layout {
@@ -86,10 +138,7 @@ struct Layout {
     int64_t colpart_floats;
 };
 
-int64_t n_slabs(int64_t rows) { return (rows + q4::kSlabRows - 1) / q4::kSlabRows; }
-int64_t n_segs(int64_t cols) { return (cols + q4::kSegCols - 1) / q4::kSegCols; }
-
-Layout make_layout(const q4adamw_tensor_t* t, int n, int recipe) {
+Layout make_layout(const q4adamw_tensor_t* t, int n, int recipe, const int64_t* full_numel = nullptr) {
     Layout L{};
     int64_t off = 0;
     L.status = off; off = round_up(off + 4, 256);
@@ -106,9 +155,10 @@ Layout make_layout(const q4adamw_tensor_t* t, int n, int recipe) {
     L.colpart = off;
     int64_t cp = 0;
     for (int i = 0; i < n; ++i) {
-        if (is_factored(t[i], recipe) && t[i].numel > 0) {
+        const Geo g = geometry(t[i], recipe, full_numel, i);
+        if (g.fact) {
             L.n_factored++;
-            cp += n_slabs(t[i].rows) * (t[i].numel / t[i].rows) + t[i].rows * n_segs(t[i].numel / t[i].rows);
+            cp += g.partials;
         }
     }
     L.colpart_floats = cp;
@@ -179,7 +229,7 @@ q4::Tables* tables_for(int recipe) {
     return g_tabs[recipe];
 }
 
-DevTensor make_dev(const q4adamw_tensor_t& t, int recipe, uint32_t call_flags) {
+DevTensor make_dev(const q4adamw_tensor_t& t, int recipe, uint32_t call_flags, const Geo& g) {
     DevTensor d{};
     d.param = t.param;
     d.grad = t.grad;
@@ -203,6 +253,10 @@ DevTensor make_dev(const q4adamw_tensor_t& t, int recipe, uint32_t call_flags) {
         d.flags |= q4::DF_M_SR;
     if (is_factored(t, recipe)) {
         d.flags |= q4::DF_FACTORED;
+        if (g.fact) {
+            d.cols = g.cols;
+            d.fbase = g.fbase;   // in place of the (absent) packed-v scales
+        }
         // vector column loads and incremental (row, column) tracking in the step
         // kernel: columns a multiple of 8 (16-B aligned float4 runs) and at
         // least one tile (256) wide, rows within 32 bits
@@ -280,25 +334,35 @@ int q4adamw_header_check(const q4adamw_header_t* h, int recipe) {
     return Q4_OK;
 }
 
-int q4adamw_state_init(const q4adamw_tensor_t* t, int n, int recipe, q4adamw_header_t* header_out, void* stream) {
+}  // extern "C"
+
+namespace {
+
+// q4adamw_state_init and q4adamw_dp_state_init (full_numel: the shard
+// geometry, NULL for whole tensors).
+int state_init_impl(const q4adamw_tensor_t* t, int n, int recipe, const int64_t* full_numel,
+                    q4adamw_header_t* header_out, void* stream) {
     if (n < 0 || (n > 0 && !t)) return Q4_EINVAL;
     if (int rc = check_recipe(recipe)) return rc;
     for (int i = 0; i < n; ++i)
-        if (int rc = check_tensor(t[i], recipe, false)) return rc;
+        if (int rc = check_tensor(t[i], recipe, false, full_numel != nullptr)) return rc;
+    if (int rc = check_dp(t, n, recipe, full_numel)) return rc;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     int64_t total = 0;
     for (int i = 0; i < n; ++i) {
         const q4adamw_tensor_t& x = t[i];
         total += x.numel;
-        if (x.numel == 0) continue;
-        const int64_t nb = nblocks(x.numel);
-        cudaError_t e = cudaMemsetAsync(x.m_codes, 0, (size_t)(nb * 64), s);
-        if (e == cudaSuccess) e = cudaMemsetAsync(x.m_scale, 0, (size_t)(nb * 4), s);
-        if (e == cudaSuccess) {
-            if (is_factored(x, recipe)) {
-                e = cudaMemsetAsync(x.v_row, 0, (size_t)(x.rows * 4), s);
-                if (e == cudaSuccess) e = cudaMemsetAsync(x.v_col, 0, (size_t)(x.numel / x.rows * 4), s);
-            } else {
+        const Geo g = geometry(x, recipe, full_numel, i);
+        cudaError_t e = cudaSuccess;
+        if (g.fact) {   // R and C of the whole parameter (an empty shard's too)
+            e = cudaMemsetAsync(x.v_row, 0, (size_t)(g.rows * 4), s);
+            if (e == cudaSuccess) e = cudaMemsetAsync(x.v_col, 0, (size_t)(g.cols * 4), s);
+        }
+        if (e == cudaSuccess && x.numel > 0) {
+            const int64_t nb = nblocks(x.numel);
+            e = cudaMemsetAsync(x.m_codes, 0, (size_t)(nb * 64), s);
+            if (e == cudaSuccess) e = cudaMemsetAsync(x.m_scale, 0, (size_t)(nb * 4), s);
+            if (e == cudaSuccess && !is_factored(x, recipe)) {
                 e = cudaMemsetAsync(x.v_codes, 0, (size_t)(nb * 64), s);
                 if (e == cudaSuccess) e = cudaMemsetAsync(x.v_scale, 0, (size_t)(nb * 4), s);
             }
@@ -316,31 +380,35 @@ int q4adamw_state_init(const q4adamw_tensor_t* t, int n, int recipe, q4adamw_hea
     return Q4_OK;
 }
 
+}  // namespace
+
+extern "C" {
+
+int q4adamw_state_init(const q4adamw_tensor_t* t, int n, int recipe, q4adamw_header_t* header_out, void* stream) {
+    return state_init_impl(t, n, recipe, nullptr, header_out, stream);
+}
+
+int q4adamw_dp_state_init(const q4adamw_tensor_t* t, int n, int recipe, const int64_t* full_numel,
+                          q4adamw_header_t* header_out, void* stream) {
+    return state_init_impl(t, n, recipe, full_numel, header_out, stream);
+}
+
 }  // extern "C"
 
 namespace {
 
-// q4adamw_step and q4adamw_step_clip: sqnorm NULL means no clipping.
-int step_impl(const q4adamw_tensor_t* t, int n, float lr, float beta1, float beta2, float eps, float weight_decay,
-              int64_t step, uint64_t seed, int recipe, uint32_t flags, const float* sqnorm, float max_norm,
-              void* workspace, int64_t workspace_bytes, void* stream) {
-    if (n < 0 || (n > 0 && !t)) return Q4_EINVAL;
-    if (int rc = check_recipe(recipe)) return rc;
-    if (step < 1 || step > 0xFFFFFFFFll) return Q4_EINVAL;
-    if (flags & ~(Q4_LM_HEAD_SR_ACTIVE | Q4_M_SR_ALL | Q4_V_UPDATE_RTN | Q4_V_NEXT_R)) return Q4_EINVAL;
-    if ((flags & (Q4_V_UPDATE_RTN | Q4_V_NEXT_R)) && recipe != Q4_RECIPE_ZIP_SR) return Q4_EINVAL;
-    if (!(beta1 >= 0.f && beta1 < 1.f) || !(beta2 >= 0.f && beta2 < 1.f)) return Q4_EINVAL;
-    if (!(eps > 0.f) || !std::isfinite(eps) || !std::isfinite(lr) || !std::isfinite(weight_decay)) return Q4_EINVAL;
-    for (int i = 0; i < n; ++i)
-        if (int rc = check_tensor(t[i], recipe, true)) return rc;
-    const Layout L = make_layout(t, n, recipe);
-    if (!workspace || !aligned(workspace, 256) || workspace_bytes < L.total) return Q4_EWORKSPACE;
-    q4::Tables* tabs = tables_for(recipe);
-    if (!tabs) return Q4_EINVAL;
-    if (n == 0) return Q4_OK;
+// Host image of the uploaded part of the workspace: descriptors, tile prefix
+// sums, factored row/tile/column prefixes and ids, and the grouped copy for
+// the two-launch split.  Returns the number of factored tensors.
+struct Image {
+    int nf = 0;
+    int n_first = 0;           // tensors of the first group of the split (0: no split)
+    uint32_t split_bit = 0;
+};
 
-    // Host image of the uploaded part of the workspace.
-    thread_local std::vector<unsigned char> img;
+Image build_image(const q4adamw_tensor_t* t, int n, int recipe, uint32_t flags, const int64_t* full_numel,
+                  const Layout& L, std::vector<unsigned char>& img, char* ws) {
+    Image im;
     img.assign((size_t)L.upload_bytes, 0);
     DevTensor* desc = reinterpret_cast<DevTensor*>(img.data() + L.desc);
     int64_t* pairs = reinterpret_cast<int64_t*>(img.data() + L.pairs);
@@ -348,23 +416,21 @@ int step_impl(const q4adamw_tensor_t* t, int n, float lr, float beta1, float bet
     int64_t* tiles = reinterpret_cast<int64_t*>(img.data() + L.tiles);
     int64_t* cols = reinterpret_cast<int64_t*>(img.data() + L.cols);
     int32_t* fids = reinterpret_cast<int32_t*>(img.data() + L.fids);
-    char* ws = static_cast<char*>(workspace);
     int64_t colpart_off = L.colpart;
-    int nf = 0;
     pairs[0] = rows[0] = tiles[0] = cols[0] = 0;
     for (int i = 0; i < n; ++i) {
-        desc[i] = make_dev(t[i], recipe, flags);
+        const Geo g = geometry(t[i], recipe, full_numel, i);
+        desc[i] = make_dev(t[i], recipe, flags, g);
         const int64_t nb = nblocks(t[i].numel);
         pairs[i + 1] = pairs[i] + (nb + 1) / 2;
-        const bool f = (desc[i].flags & q4::DF_FACTORED) && t[i].numel > 0;
-        rows[i + 1] = rows[i] + (f ? desc[i].rows : 0);
-        cols[i + 1] = cols[i] + (f ? desc[i].cols : 0);
-        tiles[i + 1] = tiles[i] + (f ? n_slabs(desc[i].rows) * n_segs(desc[i].cols) : 0);
-        if (f) {
-            desc[i].rbar = reinterpret_cast<float*>(ws + L.rbar) + 2 * nf;
+        rows[i + 1] = rows[i] + (g.fact ? g.rows : 0);
+        cols[i + 1] = cols[i] + (g.fact ? g.cols : 0);
+        tiles[i + 1] = tiles[i] + (g.fact ? g.tiles : 0);
+        if (g.fact) {
+            desc[i].rbar = reinterpret_cast<float*>(ws + L.rbar) + 2 * im.nf;
             desc[i].colpart = reinterpret_cast<float*>(ws + colpart_off);
-            colpart_off += (n_slabs(desc[i].rows) * desc[i].cols + desc[i].rows * n_segs(desc[i].cols)) * 4;
-            fids[nf++] = i;
+            colpart_off += g.partials * 4;
+            fids[im.nf++] = i;
         }
     }
     // Two launches where one instantiation does not suit every tensor: under
@@ -374,24 +440,83 @@ int step_impl(const q4adamw_tensor_t* t, int n, float lr, float beta1, float bet
     // stochastically (the LM head in the final phase) run on the m-SR
     // instantiation and the rest on the plain one.  desc2 holds the
     // descriptors of the first group first; pairs2 the two groups' prefix sums.
-    const uint32_t split_bit = recipe == Q4_RECIPE_FACTORED ? (uint32_t)q4::DF_FACTORED
-                               : (recipe == Q4_RECIPE_ZIP_SR || recipe == Q4_RECIPE_ZE_EDEN) ? (uint32_t)q4::DF_M_SR
-                                                                                          : 0u;
-    int n_first = 0;
-    if (split_bit) {
+    im.split_bit = recipe == Q4_RECIPE_FACTORED ? (uint32_t)q4::DF_FACTORED
+                   : (recipe == Q4_RECIPE_ZIP_SR || recipe == Q4_RECIPE_ZE_EDEN) ? (uint32_t)q4::DF_M_SR
+                                                                                : 0u;
+    if (im.split_bit) {
         DevTensor* desc2 = reinterpret_cast<DevTensor*>(img.data() + L.desc2);
         int64_t* pa = reinterpret_cast<int64_t*>(img.data() + L.pairs2);
         for (int i = 0; i < n; ++i)
-            if (desc[i].flags & split_bit) desc2[n_first++] = desc[i];
-        int k = n_first;
+            if (desc[i].flags & im.split_bit) desc2[im.n_first++] = desc[i];
+        int k = im.n_first;
         for (int i = 0; i < n; ++i)
-            if (!(desc[i].flags & split_bit)) desc2[k++] = desc[i];
+            if (!(desc[i].flags & im.split_bit)) desc2[k++] = desc[i];
         pa[0] = 0;
-        for (int i = 0; i < n_first; ++i) pa[i + 1] = pa[i] + (nblocks(desc2[i].numel) + 1) / 2;
-        int64_t* pb = pa + n_first + 1;
+        for (int i = 0; i < im.n_first; ++i) pa[i + 1] = pa[i] + (nblocks(desc2[i].numel) + 1) / 2;
+        int64_t* pb = pa + im.n_first + 1;
         pb[0] = 0;
-        for (int i = n_first; i < n; ++i) pb[i - n_first + 1] = pb[i - n_first] + (nblocks(desc2[i].numel) + 1) / 2;
+        for (int i = im.n_first; i < n; ++i)
+            pb[i - im.n_first + 1] = pb[i - im.n_first] + (nblocks(desc2[i].numel) + 1) / 2;
     }
+    return im;
+}
+
+q4::FactoredParams factored_params(const Layout& L, const std::vector<unsigned char>& img, char* ws, int n, int nf,
+                                   float beta2, float omb2, const float* sqnorm, float max_norm) {
+    const int64_t* rows = reinterpret_cast<const int64_t*>(img.data() + L.rows);
+    const int64_t* tiles = reinterpret_cast<const int64_t*>(img.data() + L.tiles);
+    const int64_t* cols = reinterpret_cast<const int64_t*>(img.data() + L.cols);
+    q4::FactoredParams fp{};
+    fp.tensors = reinterpret_cast<const DevTensor*>(ws + L.desc);
+    fp.row_prefix = reinterpret_cast<const int64_t*>(ws + L.rows);
+    fp.tile_prefix = reinterpret_cast<const int64_t*>(ws + L.tiles);
+    fp.col_prefix = reinterpret_cast<const int64_t*>(ws + L.cols);
+    fp.factored_ids = reinterpret_cast<const int32_t*>(ws + L.fids);
+    fp.n_tensors = n;
+    fp.n_factored = nf;
+    fp.total_rows = rows[n];
+    fp.total_tiles = tiles[n];
+    fp.total_cols = cols[n];
+    fp.beta2 = beta2;
+    fp.omb2 = omb2;
+    fp.sqnorm = sqnorm;
+    fp.max_norm = max_norm;
+    return fp;
+}
+
+// q4adamw_step, q4adamw_step_clip and q4adamw_dp_step: sqnorm NULL means no
+// clipping; full_numel: the data-parallel shard geometry (NULL: whole
+// tensors); from_sums: the factored statistics come from `sums`, the sums
+// over all shards, instead of this call's own gradients.
+int step_impl(const q4adamw_tensor_t* t, int n, float lr, float beta1, float beta2, float eps, float weight_decay,
+              int64_t step, uint64_t seed, int recipe, uint32_t flags, const float* sqnorm, float max_norm,
+              const int64_t* full_numel, bool from_sums, const float* sums, void* workspace, int64_t workspace_bytes,
+              void* stream) {
+    if (n < 0 || (n > 0 && !t)) return Q4_EINVAL;
+    if (int rc = check_recipe(recipe)) return rc;
+    if (step < 1 || step > 0xFFFFFFFFll) return Q4_EINVAL;
+    if (flags & ~(Q4_LM_HEAD_SR_ACTIVE | Q4_M_SR_ALL | Q4_V_UPDATE_RTN | Q4_V_NEXT_R)) return Q4_EINVAL;
+    if ((flags & (Q4_V_UPDATE_RTN | Q4_V_NEXT_R)) && recipe != Q4_RECIPE_ZIP_SR) return Q4_EINVAL;
+    if (!(beta1 >= 0.f && beta1 < 1.f) || !(beta2 >= 0.f && beta2 < 1.f)) return Q4_EINVAL;
+    if (!(eps > 0.f) || !std::isfinite(eps) || !std::isfinite(lr) || !std::isfinite(weight_decay)) return Q4_EINVAL;
+    for (int i = 0; i < n; ++i)
+        if (int rc = check_tensor(t[i], recipe, true, full_numel != nullptr)) return rc;
+    if (int rc = check_dp(t, n, recipe, full_numel)) return rc;
+    const Layout L = make_layout(t, n, recipe, full_numel);
+    if (!workspace || !aligned(workspace, 256) || workspace_bytes < L.total) return Q4_EWORKSPACE;
+    if (from_sums && L.n_factored > 0) {
+        if (!sums) return Q4_EINVAL;
+        if (!aligned(sums, 4)) return Q4_EALIGN;
+    }
+    q4::Tables* tabs = tables_for(recipe);
+    if (!tabs) return Q4_EINVAL;
+    if (n == 0) return Q4_OK;
+
+    thread_local std::vector<unsigned char> img;
+    char* ws = static_cast<char*>(workspace);
+    const Image im = build_image(t, n, recipe, flags, full_numel, L, img, ws);
+    const DevTensor* desc = reinterpret_cast<const DevTensor*>(img.data() + L.desc);
+    const int64_t* pairs = reinterpret_cast<const int64_t*>(img.data() + L.pairs);
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     cudaError_t e = cudaMemcpyAsync(workspace, img.data(), (size_t)L.upload_bytes, cudaMemcpyHostToDevice, s);
     if (e != cudaSuccess) return cuda_fail(e);
@@ -399,23 +524,16 @@ int step_impl(const q4adamw_tensor_t* t, int n, float lr, float beta1, float bet
     const Scalars hs = host_scalars(lr, beta1, beta2, weight_decay, step);
     const DevTensor* d_desc = reinterpret_cast<const DevTensor*>(ws + L.desc);
 
-    if (nf > 0) {
-        q4::FactoredParams fp{};
-        fp.tensors = d_desc;
-        fp.row_prefix = reinterpret_cast<const int64_t*>(ws + L.rows);
-        fp.tile_prefix = reinterpret_cast<const int64_t*>(ws + L.tiles);
-        fp.col_prefix = reinterpret_cast<const int64_t*>(ws + L.cols);
-        fp.factored_ids = reinterpret_cast<const int32_t*>(ws + L.fids);
-        fp.n_tensors = n;
-        fp.n_factored = nf;
-        fp.total_rows = rows[n];
-        fp.total_tiles = tiles[n];
-        fp.total_cols = cols[n];
-        fp.beta2 = beta2;
-        fp.omb2 = hs.omb2;
-        fp.sqnorm = sqnorm;
-        fp.max_norm = max_norm;
-        if (int ce = q4::launch_factored(fp, stream)) return cuda_fail((cudaError_t)ce);
+    if (im.nf > 0) {
+        q4::FactoredParams fp = factored_params(L, img, ws, n, im.nf, beta2, hs.omb2, sqnorm, max_norm);
+        int ce;
+        if (from_sums) {
+            fp.sums = const_cast<float*>(sums);
+            ce = q4::launch_factored_from_sums(fp, stream);
+        } else {
+            ce = q4::launch_factored(fp, stream);
+        }
+        if (ce) return cuda_fail((cudaError_t)ce);
     }
 
     q4::StepParams p{};
@@ -444,6 +562,7 @@ int step_impl(const q4adamw_tensor_t* t, int n, float lr, float beta1, float bet
     p.has_m_sr = 0;
     p.sqnorm = sqnorm;
     p.max_norm = max_norm;
+    p.wait_cycles = g_wait_cycles;
     for (int i = 0; i < n; ++i) p.has_m_sr |= (desc[i].flags & q4::DF_M_SR) ? 1 : 0;
     p.x2_beta1 = make_float2(p.beta1, p.beta1);
     p.x2_beta2 = make_float2(p.beta2, p.beta2);
@@ -460,7 +579,8 @@ int step_impl(const q4adamw_tensor_t* t, int n, float lr, float beta1, float bet
     if ((e = cudaGetDevice(&dev)) != cudaSuccess) return cuda_fail(e);
     // one group empty: the single launch below (the factored recipe with only
     // factored tensors still takes the factored-only instantiation)
-    const bool split = split_bit != 0u && n_first > 0 && n_first < n;
+    const int n_first = im.n_first;
+    const bool split = im.split_bit != 0u && n_first > 0 && n_first < n;
     if (recipe == Q4_RECIPE_FACTORED && n_first == n) p.recipe = q4::kRecipeFactoredOnly;
     if (split) {
         const DevTensor* d2 = reinterpret_cast<const DevTensor*>(ws + L.desc2);
@@ -494,8 +614,8 @@ extern "C" {
 int q4adamw_step(const q4adamw_tensor_t* t, int n, float lr, float beta1, float beta2, float eps, float weight_decay,
                  int64_t step, uint64_t seed, int recipe, uint32_t flags, void* workspace, int64_t workspace_bytes,
                  void* stream) {
-    return step_impl(t, n, lr, beta1, beta2, eps, weight_decay, step, seed, recipe, flags, nullptr, 1.f, workspace,
-                     workspace_bytes, stream);
+    return step_impl(t, n, lr, beta1, beta2, eps, weight_decay, step, seed, recipe, flags, nullptr, 1.f, nullptr,
+                     false, nullptr, workspace, workspace_bytes, stream);
 }
 
 int q4adamw_step_clip(const q4adamw_tensor_t* t, int n, float lr, float beta1, float beta2, float eps,
@@ -505,7 +625,79 @@ int q4adamw_step_clip(const q4adamw_tensor_t* t, int n, float lr, float beta1, f
     if (!sqnorm || !aligned(sqnorm, 4)) return sqnorm ? Q4_EALIGN : Q4_EINVAL;
     if (!(max_grad_norm > 0.f) || !std::isfinite(max_grad_norm)) return Q4_EINVAL;
     return step_impl(t, n, lr, beta1, beta2, eps, weight_decay, step, seed, recipe, flags, sqnorm, max_grad_norm,
-                     workspace, workspace_bytes, stream);
+                     nullptr, false, nullptr, workspace, workspace_bytes, stream);
+}
+
+int q4adamw_dp_workspace_bytes(const q4adamw_tensor_t* t, int n, int recipe, const int64_t* full_numel,
+                               int64_t* bytes) {
+    if (n < 0 || (n > 0 && !t) || !bytes) return Q4_EINVAL;
+    if (int rc = check_recipe(recipe)) return rc;
+    for (int i = 0; i < n; ++i)
+        if (int rc = check_shape(t[i], recipe, full_numel != nullptr)) return rc;
+    if (int rc = check_dp(t, n, recipe, full_numel)) return rc;
+    const int64_t a = make_layout(t, n, recipe, full_numel).total, b = make_norm_layout(t, n).total;
+    *bytes = a > b ? a : b;
+    return Q4_OK;
+}
+
+int q4adamw_dp_sums_floats(const q4adamw_tensor_t* t, int n, int recipe, const int64_t* full_numel,
+                           int64_t* floats) {
+    if (n < 0 || (n > 0 && !t) || !floats) return Q4_EINVAL;
+    if (int rc = check_recipe(recipe)) return rc;
+    for (int i = 0; i < n; ++i)
+        if (int rc = check_shape(t[i], recipe, full_numel != nullptr)) return rc;
+    if (int rc = check_dp(t, n, recipe, full_numel)) return rc;
+    int64_t f = 0;
+    for (int i = 0; i < n; ++i) {
+        const Geo g = geometry(t[i], recipe, full_numel, i);
+        if (g.fact) f += g.rows + g.cols;
+    }
+    *floats = f;
+    return Q4_OK;
+}
+
+int q4adamw_dp_factored_sums(const q4adamw_tensor_t* t, int n, int recipe, const int64_t* full_numel,
+                             float max_grad_norm, const float* sqnorm, float* sums, void* workspace,
+                             int64_t workspace_bytes, void* stream) {
+    if (n < 0 || (n > 0 && !t)) return Q4_EINVAL;
+    if (int rc = check_recipe(recipe)) return rc;
+    if (sqnorm && (!(max_grad_norm > 0.f) || !std::isfinite(max_grad_norm))) return Q4_EINVAL;
+    if (sqnorm && !aligned(sqnorm, 4)) return Q4_EALIGN;
+    for (int i = 0; i < n; ++i) {
+        if (int rc = check_shape(t[i], recipe, full_numel != nullptr)) return rc;
+        if (is_factored(t[i], recipe) && t[i].numel > 0) {
+            if (!t[i].grad) return Q4_EINVAL;
+            if (!aligned(t[i].grad, 16)) return Q4_EALIGN;
+        }
+    }
+    if (int rc = check_dp(t, n, recipe, full_numel)) return rc;
+    const Layout L = make_layout(t, n, recipe, full_numel);
+    if (L.n_factored == 0 || n == 0) return Q4_OK;
+    if (!sums) return Q4_EINVAL;
+    if (!aligned(sums, 4)) return Q4_EALIGN;
+    if (!workspace || !aligned(workspace, 256) || workspace_bytes < L.total) return Q4_EWORKSPACE;
+    thread_local std::vector<unsigned char> img;
+    char* ws = static_cast<char*>(workspace);
+    const Image im = build_image(t, n, recipe, 0u, full_numel, L, img, ws);
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    cudaError_t e = cudaMemcpyAsync(workspace, img.data(), (size_t)L.upload_bytes, cudaMemcpyHostToDevice, s);
+    if (e != cudaSuccess) return cuda_fail(e);
+    q4::FactoredParams fp = factored_params(L, img, ws, n, im.nf, 0.f, 0.f, sqnorm, sqnorm ? max_grad_norm : 1.f);
+    fp.sums = sums;
+    if (int ce = q4::launch_factored_sums(fp, stream)) return cuda_fail((cudaError_t)ce);
+    return Q4_OK;
+}
+
+int q4adamw_dp_step(const q4adamw_tensor_t* t, int n, float lr, float beta1, float beta2, float eps,
+                    float weight_decay, int64_t step, uint64_t seed, int recipe, uint32_t flags,
+                    const int64_t* full_numel, const float* sums, float max_grad_norm, const float* sqnorm,
+                    void* workspace, int64_t workspace_bytes, void* stream) {
+    if (sqnorm && (!(max_grad_norm > 0.f) || !std::isfinite(max_grad_norm))) return Q4_EINVAL;
+    if (sqnorm && !aligned(sqnorm, 4)) return Q4_EALIGN;
+    // full_numel NULL: every tensor whole (matrix offset 0); its statistics
+    // still come from sums
+    return step_impl(t, n, lr, beta1, beta2, eps, weight_decay, step, seed, recipe, flags, sqnorm,
+                     sqnorm ? max_grad_norm : 1.f, full_numel, true, sums, workspace, workspace_bytes, stream);
 }
 
 int q4adamw_draws(uint64_t seed, int64_t step, uint32_t tensor_id, uint64_t idx0, uint32_t purpose, int64_t n,
@@ -557,6 +749,12 @@ int q4adamw_grad_sqnorm(const q4adamw_tensor_t* t, int n, float* sqnorm, void* w
     return Q4_OK;
 }
 
+int q4adamw_set_stage_wait_limit(int64_t cycles) {
+    if (cycles < 0) return Q4_EINVAL;
+    g_wait_cycles = cycles == 0 ? q4::kDefaultWaitCycles : (long long)cycles;
+    return Q4_OK;
+}
+
 int q4adamw_step_status(const void* workspace, uint32_t* status, void* stream) {
     if (!workspace || !status) return Q4_EINVAL;
     if (!aligned(workspace, 256)) return Q4_EWORKSPACE;
@@ -574,7 +772,7 @@ int q4adamw_dequant_state(const q4adamw_tensor_t* t, int recipe, float* m_out, f
     if (int rc = check_recipe(recipe)) return rc;
     if (int rc = check_tensor(*t, recipe, false)) return rc;
     if (t->numel == 0 || (!m_out && !v_out)) return Q4_OK;
-    const DevTensor d = make_dev(*t, recipe, 0);
+    const DevTensor d = make_dev(*t, recipe, 0, geometry(*t, recipe, nullptr, 0));
     const q4::Codebook& nf4 = q4::codebook(m_book(recipe));
     const q4::Codebook& vb = q4::codebook(v_book(recipe));
     if (int ce = q4::launch_dequant(d, recipe, nf4.levels, vb.levels, m_out, v_out, stream))

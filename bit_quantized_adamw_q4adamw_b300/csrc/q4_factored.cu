@@ -4,7 +4,12 @@
 // averages; 1-D tensors keep packed 4-bit v).
 //
 // Three launches, all multi-tensor and deterministic (fixed summation order,
-// no atomics):
+// no atomics).  A tensor may be one data-parallel shard of its parameter (the
+// same page: partial row and column sums are combined across the group before
+// their exponential update): its elements are [fbase, fbase + numel) of the
+// whole [rows, cols] matrix, the pass covers the rows they touch, and the
+// rows/cols kernels either write the shard's row and column sums for the
+// caller to add over the ranks, or update R and C from the added sums.
 //   stats_kernel    persistent CTAs of 8 warps, four per SM, each taking tiles
 //                   of 256 rows x 256 columns of a tensor in turn: g is read
 //                   once, 16 bytes (8 BF16) per lane and row.
@@ -14,9 +19,11 @@
 //                   row partials per 256-column segment.  Column sums over the
 //                   warp's 32 rows are combined over the 8 warps in warp order,
 //                   giving column partials per 256-row slab.
-//   finalize_kernel one thread per factored row or column: sums its partials in
-//                   segment (slab) order, mean = sum / cols (rows), and the
-//                   average R_i <- beta2 R_i + (1-beta2) mean (C_j likewise).
+//   rows_kernel,    a row's partials summed in segment order by one thread, a
+//   cols_kernel     column's over its slabs by one CTA of 8 warps (contiguous
+//                   slab ranges per warp, then the warps in order); mean = sum /
+//                   cols (rows), and the average R_i <- beta2 R_i + (1-beta2)
+//                   mean (C_j likewise).
 //   rbar_kernel     one CTA per factored tensor: mean(R) in a fixed tree order,
 //                   stored with its correctly rounded reciprocal.
 // The step kernel then forms vhat_ij = R_i * C_j / mean(R) per element (with
@@ -48,7 +55,11 @@ __global__ void __launch_bounds__(kStatsWarps * 32, kStatsCtasPerSm) stats_kerne
         const int t = find_tensor(P.tile_prefix, P.n_tensors, tile);
         const DevTensor& d = P.tensors[t];
         const int64_t local = tile - __ldg(P.tile_prefix + t);
-        const int64_t rows = d.rows, cols = d.cols;
+        const int64_t cols = d.cols, fbase = d.fbase, fend = d.fbase + d.numel;
+        // the rows of the matrix this tensor's elements [fbase, fend) touch
+        // (all of them for a whole tensor); slabs count from the first
+        int64_t r_first, cov;
+        covered_rows(fbase, d.numel, cols, &r_first, &cov);
         const int64_t nseg = (cols + kSegCols - 1) / kSegCols;
         const int64_t slab = local / nseg, seg = local - slab * nseg;
         const int64_t r0 = slab * kSlabRows + warp * 32;
@@ -61,22 +72,26 @@ __global__ void __launch_bounds__(kStatsWarps * 32, kStatsCtasPerSm) stats_kerne
         for (int i = 0; i < 32; ++i) {
             const int64_t r = r0 + i;
             float sq[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-            if (r < rows && nc > 0) {
-                const uint16_t* g = d.grad + r * cols + c0;
+            if (r < cov && nc > 0) {
+                const int64_t ge = (r_first + r) * cols + c0;   // matrix index of the lane's first column
+                const uint16_t* g = d.grad + (ge - fbase);
                 if (vec) {
-                    const uint4 w = __ldcs(reinterpret_cast<const uint4*>(g));
-                    const uint32_t h[4] = {w.x, w.y, w.z, w.w};
+                    // fbase and cols are multiples of 8: a run of 8 lies wholly inside or outside
+                    if (ge >= fbase && ge < fend) {
+                        const uint4 w = __ldcs(reinterpret_cast<const uint4*>(g));
+                        const uint32_t h[4] = {w.x, w.y, w.z, w.w};
 #pragma unroll
-                    for (int k = 0; k < 4; ++k) {
-                        const float lo = __fmul_rn(bf16f(h[k] & 0xffffu), clip);
-                        const float hi = __fmul_rn(bf16f(h[k] >> 16), clip);
-                        sq[2 * k] = __fmul_rn(lo, lo);
-                        sq[2 * k + 1] = __fmul_rn(hi, hi);
+                        for (int k = 0; k < 4; ++k) {
+                            const float lo = __fmul_rn(bf16f(h[k] & 0xffffu), clip);
+                            const float hi = __fmul_rn(bf16f(h[k] >> 16), clip);
+                            sq[2 * k] = __fmul_rn(lo, lo);
+                            sq[2 * k + 1] = __fmul_rn(hi, hi);
+                        }
                     }
                 } else {
 #pragma unroll
                     for (int k = 0; k < 8; ++k) {
-                        if (k < nc) {
+                        if (k < nc && ge + k >= fbase && ge + k < fend) {
                             const float x = __fmul_rn(bf16f(g[k]), clip);
                             sq[k] = __fmul_rn(x, x);
                         }
@@ -100,8 +115,8 @@ __global__ void __launch_bounds__(kStatsWarps * 32, kStatsCtasPerSm) stats_kerne
                 rowp[i] = __fadd_rn(keep, __shfl_xor_sync(0xffffffffu, send, o));
             }
         }
-        const int64_t nslab = (rows + kSlabRows - 1) / kSlabRows;
-        if (r0 + lane < rows) d.colpart[nslab * cols + (r0 + lane) * nseg + seg] = rowp[0];
+        const int64_t nslab = (cov + kSlabRows - 1) / kSlabRows;
+        if (r0 + lane < cov) d.colpart[nslab * cols + (r0 + lane) * nseg + seg] = rowp[0];
 #pragma unroll
         for (int k = 0; k < 8; ++k) colsum[warp][lane * 8 + k] = col[k];
         __syncthreads();
@@ -117,30 +132,86 @@ __global__ void __launch_bounds__(kStatsWarps * 32, kStatsCtasPerSm) stats_kerne
     }
 }
 
-__global__ void __launch_bounds__(256) finalize_kernel(const __grid_constant__ FactoredParams P) {
-    const int64_t total = P.total_rows + P.total_cols;
-    for (int64_t idx = (int64_t)blockIdx.x * 256 + threadIdx.x; idx < total; idx += (int64_t)gridDim.x * 256) {
-        if (idx < P.total_rows) {
-            const int t = find_tensor(P.row_prefix, P.n_tensors, idx);
-            const DevTensor& d = P.tensors[t];
-            const int64_t i = idx - __ldg(P.row_prefix + t);
-            const int64_t nseg = (d.cols + kSegCols - 1) / kSegCols;
-            const int64_t nslab = (d.rows + kSlabRows - 1) / kSlabRows;
-            const float* p = d.colpart + nslab * d.cols + i * nseg;
-            float acc = __ldg(p);
-            for (int64_t q = 1; q < nseg; ++q) acc = __fadd_rn(acc, __ldg(p + q));
-            const float mean = __fdiv_rn(acc, (float)d.cols);
-            d.vrow[i] = __fmaf_rn(P.beta2, d.vrow[i], __fmul_rn(P.omb2, mean));
+// Sum of a row's partials over its segments and of a column's over its
+// slabs, in segment (slab) order; rows the tensor does not touch sum to 0.
+__device__ __forceinline__ float row_sum(const DevTensor& d, int64_t i) {
+    int64_t r_first, cov;
+    covered_rows(d.fbase, d.numel, d.cols, &r_first, &cov);
+    if (i < r_first || i >= r_first + cov) return 0.f;
+    const int64_t nseg = (d.cols + kSegCols - 1) / kSegCols;
+    const int64_t nslab = (cov + kSlabRows - 1) / kSlabRows;
+    const float* p = d.colpart + nslab * d.cols + (i - r_first) * nseg;
+    float acc = __ldg(p);
+    for (int64_t q = 1; q < nseg; ++q) acc = __fadd_rn(acc, __ldg(p + q));
+    return acc;
+}
+// Column j's sum over its slab partials by one CTA of kColWarps warps, each
+// lane one column: warp w adds the slabs [w q, (w+1) q) left to right (q =
+// ceil(nslab / kColWarps)), then the warp results are added in warp order.
+// Empty ranges contribute +0, which leaves a sum of squares unchanged, so with
+// at most kColWarps slabs this is the sequential sum.  Every thread of the
+// CTA must call it (it synchronises); lanes without a column pass valid =
+// false and get 0.
+constexpr int kColWarps = 8;
+__device__ __forceinline__ float col_sum_cta(const DevTensor& d, int64_t j, bool valid, float (*red)[32]) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    float acc = 0.f;
+    if (valid) {
+        int64_t r_first, cov;
+        covered_rows(d.fbase, d.numel, d.cols, &r_first, &cov);
+        const int64_t nslab = (cov + kSlabRows - 1) / kSlabRows;
+        const int64_t q = (nslab + kColWarps - 1) / kColWarps;
+        const int64_t s0 = warp * q, s1 = s0 + q < nslab ? s0 + q : nslab;
+        for (int64_t s = s0; s < s1; ++s) acc = __fadd_rn(acc, __ldg(d.colpart + s * d.cols + j));
+    }
+    red[warp][lane] = acc;
+    __syncthreads();
+    float tot = red[0][lane];
+#pragma unroll
+    for (int w = 1; w < kColWarps; ++w) tot = __fadd_rn(tot, red[w][lane]);
+    __syncthreads();
+    return tot;
+}
+
+// One thread per factored row: R_i from its segment partials (finalize) or
+// from the summed sums (data-parallel); or this shard's row sum into P.sums.
+enum { ROWS_FINALIZE = 0, ROWS_SUMS = 1, ROWS_FROM_SUMS = 2 };
+template <int MODE>
+__global__ void __launch_bounds__(256) rows_kernel(const __grid_constant__ FactoredParams P) {
+    for (int64_t idx = (int64_t)blockIdx.x * 256 + threadIdx.x; idx < P.total_rows; idx += (int64_t)gridDim.x * 256) {
+        const int t = find_tensor(P.row_prefix, P.n_tensors, idx);
+        const DevTensor& d = P.tensors[t];
+        const int64_t i = idx - __ldg(P.row_prefix + t);
+        float* sums = P.sums + __ldg(P.row_prefix + t) + __ldg(P.col_prefix + t);
+        if (MODE == ROWS_SUMS) {
+            sums[i] = row_sum(d, i);
         } else {
-            const int64_t cidx = idx - P.total_rows;
-            const int t = find_tensor(P.col_prefix, P.n_tensors, cidx);
-            const DevTensor& d = P.tensors[t];
-            const int64_t j = cidx - __ldg(P.col_prefix + t);
-            const int64_t nslab = (d.rows + kSlabRows - 1) / kSlabRows;
-            float acc = __ldg(d.colpart + j);
-            for (int64_t s = 1; s < nslab; ++s) acc = __fadd_rn(acc, __ldg(d.colpart + s * d.cols + j));
-            const float mean = __fdiv_rn(acc, (float)d.rows);
-            d.vcol[j] = __fmaf_rn(P.beta2, d.vcol[j], __fmul_rn(P.omb2, mean));
+            const float acc = MODE == ROWS_FINALIZE ? row_sum(d, i) : __ldg(sums + i);
+            d.vrow[i] = __fmaf_rn(P.beta2, d.vrow[i], __fmul_rn(P.omb2, __fdiv_rn(acc, (float)d.cols)));
+        }
+    }
+}
+
+// Factored columns, kColWarps warps per CTA over 32 columns of the global
+// column list (a tensor boundary may fall inside a CTA's columns): C_j from
+// its slab partials (finalize), this shard's column sum into P.sums, or C_j
+// from the summed sums (data-parallel).
+template <int MODE>
+__global__ void __launch_bounds__(kColWarps * 32) cols_kernel(const __grid_constant__ FactoredParams P) {
+    __shared__ float red[kColWarps][32];
+    const int lane = threadIdx.x & 31;
+    for (int64_t base = (int64_t)blockIdx.x * 32; base < P.total_cols; base += (int64_t)gridDim.x * 32) {
+        const int64_t g = base + lane;
+        const bool valid = g < P.total_cols;
+        const int64_t gc = valid ? g : P.total_cols - 1;
+        const int t = find_tensor(P.col_prefix, P.n_tensors, gc);
+        const DevTensor& d = P.tensors[t];
+        const int64_t j = gc - __ldg(P.col_prefix + t);
+        float* sums = P.sums + __ldg(P.row_prefix + t) + __ldg(P.col_prefix + t) + d.rows;
+        const float acc = MODE == ROWS_FROM_SUMS ? (valid ? __ldg(sums + j) : 0.f) : col_sum_cta(d, j, valid, red);
+        if (valid && (threadIdx.x >> 5) == 0) {
+            if (MODE == ROWS_SUMS) sums[j] = acc;
+            else d.vcol[j] = __fmaf_rn(P.beta2, d.vcol[j], __fmul_rn(P.omb2, __fdiv_rn(acc, (float)d.rows)));
         }
     }
 }
@@ -161,17 +232,49 @@ int grid_for(int64_t work, int per_cta, int64_t cap) {
     return (int)g;
 }
 
+int sm_count() {
+    int dev = 0, sms = 148;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+        sms = 148;
+    return sms;
+}
+
+void launch_stats(const FactoredParams& p, cudaStream_t s) {
+    if (p.total_tiles > 0)
+        stats_kernel<<<grid_for(p.total_tiles, 1, (int64_t)sm_count() * kStatsCtasPerSm), kStatsWarps * 32, 0, s>>>(
+            p);
+}
+
+template <int MODE>
+void launch_rows_cols(const FactoredParams& p, cudaStream_t s) {
+    if (p.total_rows > 0) rows_kernel<MODE><<<grid_for(p.total_rows, 256, 148 * 16), 256, 0, s>>>(p);
+    if (p.total_cols > 0) cols_kernel<MODE><<<grid_for(p.total_cols, 32, 148 * 64), kColWarps * 32, 0, s>>>(p);
+}
+
 }  // namespace
 
 int launch_factored(const FactoredParams& p, void* stream) {
     if (p.n_factored == 0) return 0;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    int dev = 0, sms = 148;
-    if (cudaGetDevice(&dev) != cudaSuccess ||
-        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
-        sms = 148;
-    stats_kernel<<<grid_for(p.total_tiles, 1, (int64_t)sms * kStatsCtasPerSm), kStatsWarps * 32, 0, s>>>(p);
-    finalize_kernel<<<grid_for(p.total_rows + p.total_cols, 256, 148 * 16), 256, 0, s>>>(p);
+    launch_stats(p, s);
+    launch_rows_cols<ROWS_FINALIZE>(p, s);
+    rbar_kernel<<<p.n_factored < 1024 ? p.n_factored : 1024, 256, 0, s>>>(p);
+    return (int)cudaGetLastError();
+}
+
+int launch_factored_sums(const FactoredParams& p, void* stream) {
+    if (p.n_factored == 0) return 0;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    launch_stats(p, s);
+    launch_rows_cols<ROWS_SUMS>(p, s);
+    return (int)cudaGetLastError();
+}
+
+int launch_factored_from_sums(const FactoredParams& p, void* stream) {
+    if (p.n_factored == 0) return 0;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    launch_rows_cols<ROWS_FROM_SUMS>(p, s);
     rbar_kernel<<<p.n_factored < 1024 ? p.n_factored : 1024, 256, 0, s>>>(p);
     return (int)cudaGetLastError();
 }

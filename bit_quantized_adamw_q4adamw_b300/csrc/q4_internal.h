@@ -26,18 +26,23 @@ struct DevTensor {
     uint8_t* mc;
     float* ms;
     uint8_t* vc;
-    float* vs;
+    union {
+        float* vs;         // packed v: block scales
+        int64_t fbase;     // factored: matrix index of element 0 (a data-parallel
+                           // shard's elem_offset; 0 for a whole tensor)
+    };
     float* vrow;
     float* vcol;
     int64_t numel;
-    int64_t rows;
-    int64_t cols;
+    int64_t rows;          // factored: rows of the whole parameter's matrix
+    int64_t cols;          // factored: its columns (numel / rows for a whole tensor)
     uint64_t elem_offset;
     uint32_t tensor_id;
     uint32_t flags;        // DF_* bits
     float* rbar;           // factored: {mean(R), RN(1/mean(R))} of this step
     float* colpart;        // factored: column partial sums [n_slabs][cols], then
-                           // row partial sums [rows][n_segs]
+                           // row partial sums [cov_rows][n_segs] (the rows the
+                           // tensor's elements touch, 256-row slabs from the first)
 };
 static_assert(sizeof(DevTensor) == 128, "descriptor must stay 128 bytes");
 
@@ -50,6 +55,10 @@ enum : uint32_t {
 
 // Bits of the step's device status word (first word of the workspace).
 enum : uint32_t { ST_STAGE_TIMEOUT = 1u };
+
+// Default limit of the step kernel's wait for a staged tile: about one second
+// at the SM clock.  The drain after a timed-out wait always uses it.
+constexpr long long kDefaultWaitCycles = 2000000000ll;
 
 // Codebooks and candidate tables (built on the host by q4_tables.cpp).
 struct Tables {
@@ -93,6 +102,8 @@ struct StepParams {
     int has_m_sr;                 // some tensor rounds its first moment stochastically
     const float* sqnorm;          // global-norm clipping: device sum of squares, or NULL
     float max_norm;               //   and the clipping threshold
+    long long wait_cycles;        // limit of a warp's wait for a staged tile (SM clock cycles)
+    int chunk;                    // consecutive tiles a warp takes at a time (set by launch_step)
     // the step scalars broadcast to pairs, for the paired FP32 instructions
     float2 x2_beta1, x2_beta2, x2_omb1, x2_omb2, x2_c2, x2_eps, x2_decay, x2_neg_step;
     uint32_t round_keys[20];      // Philox key schedule: (k0, k1) for rounds 0..9
@@ -101,7 +112,7 @@ struct StepParams {
 
 struct FactoredParams {
     const DevTensor* tensors;
-    const int64_t* row_prefix;    // n+1: factored rows of each tensor
+    const int64_t* row_prefix;    // n+1: factored rows of each tensor (its whole matrix)
     const int64_t* tile_prefix;   // n+1: column tiles (slab x segment) of each tensor
     const int64_t* col_prefix;    // n+1: factored columns of each tensor
     const int32_t* factored_ids;  // tensor index of the k-th factored tensor
@@ -111,7 +122,17 @@ struct FactoredParams {
     float beta2, omb2;
     const float* sqnorm;          // as StepParams
     float max_norm;
+    float* sums;                  // data-parallel: per factored tensor, row sums [rows] then
+                                  // column sums [cols], at row_prefix[t] + col_prefix[t]
 };
+
+// Rows of a factored tensor's matrix that its elements [fbase, fbase + numel)
+// touch: the first, and how many.
+__host__ __device__ inline void covered_rows(int64_t fbase, int64_t numel, int64_t cols, int64_t* first,
+                                             int64_t* count) {
+    *first = fbase / cols;
+    *count = numel > 0 ? (fbase + numel - 1) / cols - *first + 1 : 0;
+}
 
 // Gradient sum of squares (global-norm clipping).  Chunks are aligned runs of
 // kNormChunkTiles 256-element tiles of one tensor.
@@ -159,6 +180,11 @@ int record_cuda_error(int cuda_error);
 int launch_step(const StepParams& p, int grid, void* stream);
 int step_grid_size(int device, int64_t total_pairs);
 int launch_factored(const FactoredParams& p, void* stream);
+// Data-parallel factored statistics: this shard's row/column sums into p.sums
+// (statistics pass, then the sums), and the update of R and C from sums over
+// all shards followed by mean(R).
+int launch_factored_sums(const FactoredParams& p, void* stream);
+int launch_factored_from_sums(const FactoredParams& p, void* stream);
 int launch_grad_sqnorm(const NormParams& p, int device, void* stream);
 int launch_draws(uint64_t seed, uint32_t step, uint32_t tensor_id, uint64_t idx0, uint32_t purpose, int64_t n,
                  uint32_t* out, void* stream);

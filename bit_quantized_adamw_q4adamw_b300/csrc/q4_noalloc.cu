@@ -58,3 +58,10 @@ extern "C" int q4adamw_step_noalloc(const q4adamw_tensor_t* t, int n, float lr, 
     return q4adamw_step(t, n, lr, beta1, beta2, eps, weight_decay, step, seed, recipe, flags, ws, kScratchBytes,
                         stream);
 }
+
+extern "C" int q4adamw_step_noalloc_status(uint32_t* status, void* stream) {
+    if (!status) return Q4_EINVAL;
+    void* ws = nullptr;
+    if (int ce = scratch_address(&ws)) return q4::record_cuda_error(ce);
+    return q4adamw_step_status(ws, status, stream);
+}

@@ -7,7 +7,7 @@
 //
 // Data movement.  The grid is persistent (one 16-warp CTA per SM).  The global
 // list of tiles of all tensors (the tensor-chunk table is the prefix sum of
-// tiles per tensor) is cut into chunks of kChunk consecutive tiles, dealt
+// tiles per tensor) is cut into chunks of P.chunk consecutive tiles, dealt
 // round-robin to the warps of the grid; within a chunk and a tensor each copy
 // source advances by a constant per tile.  Each warp keeps
 // a ring of kStages shared-memory staging buffers: while it computes tile k,
@@ -19,9 +19,10 @@
 // not a multiple of 8 elements (a tensor's ragged tail) is read directly from
 // global memory instead.  Results (FP32 and BF16 weights, codes, scales) are
 // written straight from registers with coalesced streaming stores.  Every
-// wait on an mbarrier is bounded by a clock limit; on expiry the warp sets
-// ST_STAGE_TIMEOUT in the step's status word, drains its own copies (again
-// with a limit) and exits.
+// wait on an mbarrier is bounded by a clock limit (StepParams::wait_cycles,
+// about one second by default); on expiry the warp sets ST_STAGE_TIMEOUT in
+// the step's status word, drains its own copies, the late one included (each
+// with the default limit), and exits.
 //
 // Arithmetic.  The method's per-element and per-block definitions (listing
 // page "Rounding in Preconditioner Space", Abstract and Tables 1-2; news page
@@ -60,8 +61,7 @@ namespace {
 
 constexpr float kMagic = 12582912.0f;                // 1.5 * 2^23: rounds to an integer in the low mantissa bits
 constexpr float kTwoM24 = 5.9604644775390625e-08f;   // 2^-24
-constexpr long long kWaitCycles = 2000000000ll;      // about one second at the SM clock
-constexpr int kChunk = 16;                           // consecutive tiles a warp takes at a time
+constexpr int kMaxChunk = 16;                        // most consecutive tiles a warp takes at a time
 
 struct __align__(16) Stage {
     uint4 grad[32];     // 256 BF16 gradients
@@ -99,6 +99,8 @@ struct __align__(256) WarpSmem {
 struct __align__(256) SmemAll {
     WarpSmem w[kStepWarps];
     float2 nf4_bucket[64];  // NF4 RTN by linear bucket: {unscaled threshold of the candidate, candidate}
+    float4 v_rtn[16];       // v RTN by candidate c: {unscaled threshold t_c, level L_c, level L_{c+1}, 0}
+    float v_next[16];       // ZIP-SR cell search by candidate c: unscaled level L_{c+1}
     float vl[16];     // unscaled v levels (EDEN reconstruction)
     uint8_t lut_nf4_t[64];
     uint8_t lut_nf4_l[64];
@@ -124,15 +126,30 @@ __device__ __forceinline__ bool mbar_try_wait(unsigned long long* bar, uint32_t 
         : "memory");
     return ok != 0;
 }
+__device__ __forceinline__ bool mbar_test_wait(unsigned long long* bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_addr(bar)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
 // Waits for the phase with the given parity; false if it has not completed
-// within kWaitCycles.
-__device__ __forceinline__ bool mbar_wait_bounded(unsigned long long* bar, uint32_t parity) {
-    if (mbar_try_wait(bar, parity)) return true;
+// within `limit` SM clock cycles.  A limit below kPollBelow polls with the
+// non-blocking test_wait, so that it expires even when the data would arrive
+// during a try_wait suspension; longer limits suspend in try_wait between
+// clock checks.  (The limit is uniform over the launch.)
+constexpr long long kPollBelow = 1000000;
+__device__ __forceinline__ bool mbar_wait_bounded(unsigned long long* bar, uint32_t parity, long long limit) {
+    if (mbar_test_wait(bar, parity)) return true;
     const long long t0 = clock64();
-    while (!mbar_try_wait(bar, parity)) {
-        if (clock64() - t0 > kWaitCycles) return false;
+    for (;;) {
+        if (limit < kPollBelow ? mbar_test_wait(bar, parity) : mbar_try_wait(bar, parity)) return true;
+        if (clock64() - t0 > limit) return false;
     }
-    return true;
 }
 // Predicated forms (no branch): the operation runs on lanes whose flag is set.
 __device__ __forceinline__ void mbar_arrive_expect_tx_if(uint32_t flag, uint32_t bar, uint32_t bytes) {
@@ -509,9 +526,10 @@ __device__ __forceinline__ void factored_vhat(const DevTensor& d, int64_t e0, in
     const float2 rb = *reinterpret_cast<const float2*>(d.rbar);
     const bool rb_ok = rb.x != 0.f && quot_range_ok(rb.x);
     float R[8], C[8];
+    const int64_t me0 = d.fbase + e0;   // matrix index of the lane's first element
     if (nvalid == 8 && (d.flags & DF_CVEC)) {
-        const int64_t frow = e0 / d.cols;
-        const int64_t fcol = e0 - frow * d.cols;
+        const int64_t frow = me0 / d.cols;
+        const int64_t fcol = me0 - frow * d.cols;
         const float Ri = __ldg(d.vrow + frow);
         const float4 c0 = __ldg(reinterpret_cast<const float4*>(d.vcol + fcol));
         const float4 c1 = __ldg(reinterpret_cast<const float4*>(d.vcol + fcol + 4));
@@ -522,8 +540,8 @@ __device__ __forceinline__ void factored_vhat(const DevTensor& d, int64_t e0, in
     } else {
         int64_t frow = 0, fcol = 0;
         if (nvalid > 0) {
-            frow = e0 / d.cols;
-            fcol = e0 - frow * d.cols;
+            frow = me0 / d.cols;
+            fcol = me0 - frow * d.cols;
         }
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
@@ -857,9 +875,32 @@ __device__ __forceinline__ void compute_tile_full(const StepParams& P, const Dev
         return;
     }
 
+    // ---- m codes, NF4 RTN: no per-block table ------------------------------
+    // The linear bucket b of m' (buckets 0..32 occur for |m'| <= s_m) reads
+    // the CTA's constant entry {t_c, c} (c the candidate code, t_c its
+    // unscaled threshold); the threshold at the new scale is t_c * s_m, the
+    // same product a per-block table would hold.  Computed ahead of the table
+    // stores below so that it overlaps their dependency chain.
+    const bool nf4_rtn = RECIPE != Q4_RECIPE_TORCHAO && !(MSR && m_sr);
+    uint32_t cm = 0;
+    if (nf4_rtn) {
+        const float rho16 = __fmul_rn(16.f, rcp_rn_normal<1>(s_m));
+        const uint32_t nb_base = smem_addr(sm.nf4_bucket);
+        const float2 sm2 = make_float2(s_m, s_m);
+        uint32_t c[8];
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            const float2 z = fma2_rn(m1[k], make_float2(rho16, rho16), make_float2(kMagic + 16.f, kMagic + 16.f));
+            const float2 e0v = lds_f32x2(nb_base + (__float_as_uint(z.x) & 63u) * 8u);
+            const float2 e1v = lds_f32x2(nb_base + (__float_as_uint(z.y) & 63u) * 8u);
+            const float2 thr = mul2_rn(make_float2(e0v.x, e1v.x), sm2);
+            c[2 * k] = __float_as_uint(e0v.y) + (m1[k].x > thr.x ? 1u : 0u);
+            c[2 * k + 1] = __float_as_uint(e1v.y) + (m1[k].y > thr.y ? 1u : 0u);
+        }
+        cm = pack8(c);
+    }
+
     // ---- fast tables at the new scales ------------------------------------
-    // RTN: mt[half][b] = {t_c * s_m, c} for the linear bucket b (c its
-    // candidate); buckets 0..32 occur for |m'| <= s_m.
     // State-SR (LM head in the final phase): a_k = level k at the new scale;
     // the cell search reads a_{c+1} (floats 0..15 of mt[half]), then
     // (a_k, d_k) with d_k = (a_{k+1} - a_k) 2^-24 (float2 8..23).
@@ -871,36 +912,22 @@ __device__ __forceinline__ void compute_tile_full(const StepParams& P, const Dev
         float* mb = reinterpret_cast<float*>(&wt.mt[half][0]);
         mb[j] = a1;
         reinterpret_cast<float2*>(mb + 16)[j] = make_float2(a, j < 15 ? __fmul_rn(__fsub_rn(a1, a), kTwoM24) : 0.f);
-    } else {
-        const float2 e1 = sm.nf4_bucket[j];
-        const float2 e2 = sm.nf4_bucket[j + 16];
-        wt.mt[half][j] = make_float2(__fmul_rn(e1.x, s_m), e1.y);
-        wt.mt[half][j + 16] = make_float2(__fmul_rn(e2.x, s_m), e2.y);
-        if (j == 0) {
-            const float2 e3 = sm.nf4_bucket[32];
-            wt.mt[half][32] = make_float2(__fmul_rn(e3.x, s_m), e3.y);
-        }
     }
-    if (!fact) {
-        if (RECIPE == Q4_RECIPE_ZIP_SR) {
-            // a_k = level k at the new scale, r_k its preconditioner, d_k =
-            // (r_k - r_{k+1}) 2^-24: the cell search reads a_{c+1}, then (r_k, d_k).
-            const float a = __fmul_rn(my_vl, s_v);
-            const float rk = P.fast_math ? precond<true>(P, a) : precond<false>(P, a);
-            const float rk1 = __shfl_down_sync(0xffffffffu, rk, 1);
-            const float dk = j < 15 ? __fmul_rn(__fsub_rn(rk, rk1), kTwoM24) : 0.f;
-            const float a1 = __shfl_down_sync(0xffffffffu, a, 1);
-            reinterpret_cast<float*>(&wt.ve[half][0])[j] = a1;                  // a_{c+1} by cell
-            reinterpret_cast<float2*>(&wt.ve[half][4])[j] = make_float2(rk, dk);  // (r_k, d_k) by cell
-        } else {
-            // ve[half][c] = {t_c * s_v, L_c, L_{c+1}} (unscaled levels for EDEN)
-            wt.ve[half][j] = make_float4(__fmul_rn(my_vt, s_v), my_vl, my_vl1, 0.f);
-        }
+    if (RECIPE == Q4_RECIPE_ZIP_SR && !fact) {
+        // a_k = level k at the new scale, r_k its preconditioner, d_k =
+        // (r_k - r_{k+1}) 2^-24: after the cell search (from the constant
+        // levels) the SR decision reads (r_k, d_k) by cell.
+        const float a = __fmul_rn(my_vl, s_v);
+        const float rk = P.fast_math ? precond<true>(P, a) : precond<false>(P, a);
+        const float rk1 = __shfl_down_sync(0xffffffffu, rk, 1);
+        const float dk = j < 15 ? __fmul_rn(__fsub_rn(rk, rk1), kTwoM24) : 0.f;
+        reinterpret_cast<float2*>(&wt.ve[half][4])[j] = make_float2(rk, dk);  // (r_k, d_k) by cell
     }
-    __syncwarp();
+    // the v RTN codes (ZE-EDEN, TorchAO, factored 1-D) and the NF4 RTN m codes
+    // read constant tables only: no per-block table to wait for
+    if (RECIPE == Q4_RECIPE_ZIP_SR || RECIPE == Q4_RECIPE_TORCHAO || (MSR && m_sr)) __syncwarp();
 
-    // ---- m codes: NF4 RTN, or NF4 State-SR; TorchAO SDyn4 RTN by magnitude ----
-    uint32_t cm;
+    // ---- m codes: NF4 State-SR; TorchAO SDyn4 RTN by magnitude ----------------
     if (RECIPE == Q4_RECIPE_TORCHAO) {
         // count n = #{i : A_i s_m below |m'|} from the log-bucket lower bound c
         // and one comparison with A_c s_m (strict for m' >= 0, non-strict for
@@ -946,19 +973,6 @@ __device__ __forceinline__ void compute_tile_full(const StepParams& P, const Dev
             c[2 * k + 1] = k1 + (t.y < gap.y ? 1u : 0u);
         }
         cm = pack8(c);
-    } else {
-        const float rho16 = __fmul_rn(16.f, rcp_rn_normal<1>(s_m));
-        const uint32_t mt_base = tb + (uint32_t)((char*)&wt.mt[half][0] - (char*)&wt);
-        uint32_t c[8];
-#pragma unroll
-        for (int k = 0; k < 4; ++k) {
-            const float2 z = fma2_rn(m1[k], make_float2(rho16, rho16), make_float2(kMagic + 16.f, kMagic + 16.f));
-            const float2 e0v = lds_f32x2(mt_base + (__float_as_uint(z.x) & 63u) * 8u);
-            const float2 e1v = lds_f32x2(mt_base + (__float_as_uint(z.y) & 63u) * 8u);
-            c[2 * k] = __float_as_uint(e0v.y) + (m1[k].x > e0v.x ? 1u : 0u);
-            c[2 * k + 1] = __float_as_uint(e1v.y) + (m1[k].y > e1v.x ? 1u : 0u);
-        }
-        cm = pack8(c);
     }
 
     // ---- v codes ----------------------------------------------------------
@@ -968,8 +982,10 @@ __device__ __forceinline__ void compute_tile_full(const StepParams& P, const Dev
         const float rho = rcp_rn_normal<1>(s_v);
         const uint32_t ve_base = tb + (uint32_t)((char*)&wt.ve[half][0] - (char*)&wt);
         uint32_t c[8];
+        const float2 sv2 = make_float2(s_v, s_v);
         if (RECIPE == Q4_RECIPE_ZIP_SR) {
             const uint32_t lut = smem_addr(sm.lut_v_l);
+            const uint32_t vn_base = smem_addr(sm.v_next);
             uint32_t w[8];
             draws8(d.elem_offset + (uint64_t)e0, 1u, d.tensor_id, P.step, P.round_keys, w);
 #pragma unroll
@@ -977,8 +993,10 @@ __device__ __forceinline__ void compute_tile_full(const StepParams& P, const Dev
                 const float2 y = mul2_rn(v1[k], make_float2(rho, rho));
                 const uint32_t c0 = lds_u8(lut + (__float_as_uint(y.x) >> 19));
                 const uint32_t c1 = lds_u8(lut + (__float_as_uint(y.y) >> 19));
-                const bool up0 = lds_f32(ve_base + c0 * 4u) <= v1[k].x;
-                const bool up1 = lds_f32(ve_base + c1 * 4u) <= v1[k].y;
+                // a_{c+1} = L_{c+1} * s_v, the level at the new scale
+                const float2 a1 = mul2_rn(make_float2(lds_f32(vn_base + c0 * 4u), lds_f32(vn_base + c1 * 4u)), sv2);
+                const bool up0 = a1.x <= v1[k].x;
+                const bool up1 = a1.y <= v1[k].y;
                 const uint32_t k0 = c0 + (up0 ? 1u : 0u), k1 = c1 + (up1 ? 1u : 0u);
                 const float2 e0v = lds_f32x2(ve_base + 64u + k0 * 8u);
                 const float2 e1v = lds_f32x2(ve_base + 64u + k1 * 8u);
@@ -992,15 +1010,18 @@ __device__ __forceinline__ void compute_tile_full(const StepParams& P, const Dev
             }
         } else {
             const uint32_t lut = smem_addr(sm.lut_v_t);
+            const uint32_t vr_base = smem_addr(sm.v_rtn);
             float ta[8], tb2[8];
 #pragma unroll
             for (int k = 0; k < 4; ++k) {
                 const float2 y = mul2_rn(v1[k], make_float2(rho, rho));
                 const uint32_t c0 = lds_u8(lut + (__float_as_uint(y.x) >> 19));
                 const uint32_t c1 = lds_u8(lut + (__float_as_uint(y.y) >> 19));
-                const float4 e0v = lds_f32x4(ve_base + c0 * 16u);
-                const float4 e1v = lds_f32x4(ve_base + c1 * 16u);
-                const bool up0 = v1[k].x > e0v.x, up1 = v1[k].y > e1v.x;
+                // {t_c, L_c, L_{c+1}}; the threshold at the new scale is t_c * s_v
+                const float4 e0v = lds_f32x4(vr_base + c0 * 16u);
+                const float4 e1v = lds_f32x4(vr_base + c1 * 16u);
+                const float2 thr = mul2_rn(make_float2(e0v.x, e1v.x), sv2);
+                const bool up0 = v1[k].x > thr.x, up1 = v1[k].y > thr.y;
                 c[2 * k] = c0 + (up0 ? 1u : 0u);
                 c[2 * k + 1] = c1 + (up1 ? 1u : 0u);
                 if (RECIPE == Q4_RECIPE_ZE_EDEN) {
@@ -1056,7 +1077,12 @@ __global__ void __launch_bounds__(kStepThreads, 1) step_kernel(const __grid_cons
     const int warp = threadIdx.x >> 5;
     WarpSmem& ws = sm.w[warp];
 
-    if (threadIdx.x < 16) sm.vl[threadIdx.x] = P.tab.vl[threadIdx.x];
+    if (threadIdx.x < 16) {
+        const int c = threadIdx.x, c1 = c < 15 ? c + 1 : 15;
+        sm.vl[c] = P.tab.vl[c];
+        sm.v_rtn[c] = make_float4(P.tab.vt[c], P.tab.vl[c], P.tab.vl[c1], 0.f);
+        sm.v_next[c] = P.tab.vl[c1];
+    }
     for (int i = threadIdx.x; i < 64; i += blockDim.x) {
         sm.lut_nf4_t[i] = P.tab.lut_nf4_t[i];
         sm.lut_nf4_l[i] = P.tab.lut_nf4_l[i];
@@ -1086,7 +1112,7 @@ __global__ void __launch_bounds__(kStepThreads, 1) step_kernel(const __grid_cons
     const float clip = clip_factor(P.sqnorm, P.max_norm);
     const uint64_t policy = evict_first_policy();
 
-    // Work split: the global tile list is cut into chunks of kChunk consecutive
+    // Work split: the global tile list is cut into chunks of `chunk` consecutive
     // tiles, dealt round-robin to the W warps of the grid (warp w takes chunks
     // w, w+W, ...).  Inside a chunk a warp's tiles are consecutive, so within a
     // tensor every copy source advances by a constant; dealing chunks
@@ -1094,6 +1120,7 @@ __global__ void __launch_bounds__(kStepThreads, 1) step_kernel(const __grid_cons
     const int64_t gw = (int64_t)blockIdx.x * kStepWarps + warp;
     const int64_t W = (int64_t)gridDim.x * kStepWarps;
     const int64_t total = P.total_pairs;
+    const int kChunk = P.chunk;
     const int64_t n_chunks = (total + kChunk - 1) / kChunk;
     if (gw >= n_chunks) return;
     const int64_t my_chunks = (n_chunks - 1 - gw) / W + 1;
@@ -1219,13 +1246,14 @@ __global__ void __launch_bounds__(kStepThreads, 1) step_kernel(const __grid_cons
     int64_t c_n = __ldg(P.pair_prefix + t0 + 1) - __ldg(P.pair_prefix + t0);
     reinterpret_cast<uint32_t*>(&ws.desc)[lane] = __ldg(reinterpret_cast<const uint32_t*>(P.tensors + c_t) + lane);
     __syncwarp();
-    // factored recipe: (row, column) of the current tile's first element, for
-    // tensors with DF_CVEC; set by one division per chunk or tensor, then
-    // advanced by 256 columns a tile (at most one wrap, as cols >= 256)
+    // factored recipe: (row, column) of the current tile's first element in
+    // the parameter's matrix (a shard starts at fbase), for tensors with
+    // DF_CVEC; set by one division per chunk or tensor, then advanced by 256
+    // columns a tile (at most one wrap, as cols >= 256)
     uint32_t f_row = 0, f_col = 0;
     auto fpos = [&]() {
         if (is_factored_recipe(RECIPE) && (ws.desc.flags & DF_CVEC)) {
-            const int64_t e = c_p * 2 * kBlock;
+            const int64_t e = ws.desc.fbase + c_p * 2 * kBlock;
             const int64_t r = e / ws.desc.cols;
             f_row = (uint32_t)r;
             f_col = (uint32_t)(e - r * ws.desc.cols);
@@ -1235,13 +1263,16 @@ __global__ void __launch_bounds__(kStepThreads, 1) step_kernel(const __grid_cons
     for (int it = 0; it < n_it; ++it) {
         if (it + kStages - 1 < n_it) issue(it + kStages - 1);
         const int s = it & (kStages - 1);
-        const bool ok = __all_sync(0xffffffffu, mbar_wait_bounded(&ws.bar[s], (uint32_t)((it / kStages) & 1)));
+        const bool ok =
+            __all_sync(0xffffffffu, mbar_wait_bounded(&ws.bar[s], (uint32_t)((it / kStages) & 1), P.wait_cycles));
         if (!ok) {
             if (lane == 0) atomicOr(P.status, ST_STAGE_TIMEOUT);
-            // drain the copies this warp still has in flight, then leave
+            // drain the copies this warp still has in flight (the late stage
+            // included), each with the default bound, then leave
             const int last = (it + kStages - 1 < n_it) ? it + kStages - 1 : n_it - 1;
-            for (int k = it + 1; k <= last; ++k)
-                (void)mbar_wait_bounded(&ws.bar[k & (kStages - 1)], (uint32_t)((k / kStages) & 1));
+            for (int k = it; k <= last; ++k)
+                (void)mbar_wait_bounded(&ws.bar[k & (kStages - 1)], (uint32_t)((k / kStages) & 1),
+                                        kDefaultWaitCycles);
             return;
         }
         if (c_k == kChunk || c_p == c_n) {
@@ -1310,8 +1341,16 @@ int step_grid_size(int device, int64_t total_pairs) {
     return (int)(need < full ? (need > 0 ? need : 1) : full);
 }
 
-int launch_step(const StepParams& p, int grid, void* stream) {
+int launch_step(const StepParams& p_in, int grid, void* stream) {
     cudaStream_t s = static_cast<cudaStream_t>(stream);
+    // Chunk size: kMaxChunk tiles when every warp gets many chunks (a chunk
+    // switch costs a tensor search; within a chunk copy sources advance by
+    // constants), fewer when the launch is small, so that its tiles spread
+    // over the warps instead of a few warps taking 16 each.
+    StepParams p = p_in;
+    const int64_t warps = (int64_t)grid * kStepWarps;
+    const int64_t per = p.total_pairs / (4 * warps);
+    p.chunk = (int)(per >= kMaxChunk ? kMaxChunk : per < 1 ? 1 : per);
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return (int)e;

@@ -6,6 +6,16 @@ a tensor steps it exactly as the whole tensor would be stepped, given the
 shard's ``elem_offset``.  This module only computes the ranges (ZeRO-style:
 the flattened parameter list cut into ``world`` nearly equal, block-aligned
 pieces); it moves no data.
+
+Factored parameters (rank >= 2 under the factored recipe) are the exception:
+their row and column statistics span the whole parameter, so a shard of one
+cannot be stepped on its own.  AReno docs "4-bit AdamW", section "State
+representation": the partial row and column sums are combined across the
+data-parallel group before their exponential update.  With the library that
+is q4adamw_dp_factored_sums on every rank, a SUM all-reduce of the sums
+buffers, then q4adamw_dp_step (include/q4adamw.h).  The buffers line up only
+if every rank passes every factored parameter, in the same order, even where
+it holds none of its elements: partition_all() gives that list.
 """
 from __future__ import annotations
 
@@ -44,3 +54,11 @@ def partition(numels, world: int, rank: int):
             out.append(Shard(t, s, e - s))
         base += nb
     return out
+
+
+def partition_all(numels, world: int, rank: int):
+    """One shard per tensor, in list order: rank `rank`'s part as partition()
+    gives it, or an empty shard (start 0, numel 0) where the rank holds none of
+    the tensor -- the list a data-parallel factored step passes on every rank."""
+    mine = {s.tensor: s for s in partition(numels, world, rank)}
+    return [mine.get(t, Shard(t, 0, 0)) for t in range(len(numels))]

@@ -213,6 +213,9 @@ int q4adamw_header_check(const q4adamw_header_t* h, int recipe);
  * workspace: device memory of at least q4adamw_workspace_bytes() bytes,
  * 256-B aligned, not used concurrently by another call.  The host tensor
  * array t is read during the call only.  Tensors must not overlap.
+ * Each call uploads its descriptor table to the workspace with one
+ * cudaMemcpyAsync from a pageable host buffer that the next call on the same
+ * thread reuses; the call is not designed for CUDA graph capture.
  */
 int q4adamw_step(const q4adamw_tensor_t* t, int n, float lr, float beta1, float beta2, float eps, float weight_decay,
                  int64_t step, uint64_t seed, int recipe, uint32_t flags, void* workspace, int64_t workspace_bytes,
@@ -253,6 +256,61 @@ int q4adamw_step_clip(const q4adamw_tensor_t* t, int n, float lr, float beta1, f
                       void* stream);
 
 /*
+ * Data-parallel shards of factored parameters (AReno docs "4-bit AdamW",
+ * section "State representation": for data-parallel training the partial
+ * row and column sums are combined across the group before their
+ * exponential update).  Each rank passes its own shards; a shard of a
+ * factored parameter i is the elements [elem_offset, elem_offset + numel)
+ * of the parameter's row-major matrix [rows, full_numel[i] / rows]
+ * (elem_offset a multiple of 128, as for every tensor; numel may be 0).
+ * v_row and v_col hold the whole parameter's R (rows floats) and C
+ * (full_numel[i] / rows floats): every rank keeps its own copy and updates
+ * it identically.  full_numel NULL means every tensor is whole (matrix
+ * offset 0, full_numel = numel).  Tensors that are not factored in the
+ * recipe ignore full_numel and step as in q4adamw_step.
+ *
+ * One step is three calls per rank:
+ *   1. q4adamw_dp_factored_sums writes this rank's FP32 sums of g^2 (g
+ *      multiplied first by the clip factor when sqnorm is not NULL, as in
+ *      q4adamw_step_clip) into sums: for each factored tensor in list order,
+ *      its rows' sums (rows floats; 0 for rows the shard does not touch),
+ *      then its columns' sums (cols floats).  Within a shard the order of
+ *      the additions is fixed (as in the single-call step).
+ *   2. The caller adds the sums buffers of all ranks (an all-reduce, SUM).
+ *      Every rank must pass the same factored tensors in the same order, a
+ *      shard with no element included, so that the buffers line up.
+ *   3. q4adamw_dp_step updates R_i <- beta2 R_i + (1-beta2) (S_i / cols) and
+ *      C_j likewise (S_j / rows) from the added sums, forms mean(R) and runs
+ *      the step of this rank's shards with vhat = R_i C_j / mean(R) at each
+ *      element's matrix position.
+ * With one rank (each parameter one shard) the result equals q4adamw_step
+ * (q4adamw_step_clip) bit for bit.
+ *
+ * q4adamw_dp_state_init: q4adamw_state_init for such a shard list (codes and
+ * scales of the shard, the whole R and C of each factored parameter, also for
+ * an empty shard).
+ * q4adamw_dp_sums_floats: floats of the sums buffer (host-only).
+ * q4adamw_dp_workspace_bytes: the workspace both device calls need
+ * (host-only; 256-B aligned, not shared with a concurrent call).
+ * Errors: as q4adamw_step; Q4_ESHAPE when full_numel[i] is negative or not a
+ * multiple of rows, or the shard does not fit in the matrix; Q4_EINVAL for a
+ * NULL sums (with factored tensors present) or NULL v_row / v_col of a
+ * factored shard, also an empty one; Q4_EALIGN for a misaligned sums.
+ */
+int q4adamw_dp_state_init(const q4adamw_tensor_t* t, int n, int recipe, const int64_t* full_numel,
+                          q4adamw_header_t* header_out, void* stream);
+int q4adamw_dp_sums_floats(const q4adamw_tensor_t* t, int n, int recipe, const int64_t* full_numel, int64_t* floats);
+int q4adamw_dp_workspace_bytes(const q4adamw_tensor_t* t, int n, int recipe, const int64_t* full_numel,
+                               int64_t* bytes);
+int q4adamw_dp_factored_sums(const q4adamw_tensor_t* t, int n, int recipe, const int64_t* full_numel,
+                             float max_grad_norm, const float* sqnorm, float* sums, void* workspace,
+                             int64_t workspace_bytes, void* stream);
+int q4adamw_dp_step(const q4adamw_tensor_t* t, int n, float lr, float beta1, float beta2, float eps,
+                    float weight_decay, int64_t step, uint64_t seed, int recipe, uint32_t flags,
+                    const int64_t* full_numel, const float* sums, float max_grad_norm, const float* sqnorm,
+                    void* workspace, int64_t workspace_bytes, void* stream);
+
+/*
  * The stochastic-rounding draws of the step, for checking and reproducing its
  * rounding: writes to out[0..n) (device, 4-B aligned) the 32-bit Philox4x32-10
  * words that q4adamw_step draws for elements idx0 .. idx0+n-1 (global element
@@ -276,6 +334,21 @@ int q4adamw_draws(uint64_t seed, int64_t step, uint32_t tensor_id, uint64_t idx0
  */
 #define Q4_STATUS_STAGE_TIMEOUT 0x1u
 int q4adamw_step_status(const void* workspace, uint32_t* status, void* stream);
+
+/*
+ * Limit, in SM clock cycles, of the step kernel's bounded wait for a staged
+ * tile, for the calling thread's subsequent q4adamw_step, q4adamw_step_clip
+ * and q4adamw_step_noalloc calls (a per-thread setting; host-only).  0
+ * restores the default of 2,000,000,000 cycles (about one second at the
+ * B300's 2.03 GHz).  A warp whose wait exceeds the limit sets
+ * Q4_STATUS_STAGE_TIMEOUT in the step's status word, then waits, with the
+ * default limit, for the copies it still has in flight and stops; the tiles
+ * it had not computed keep their previous values.  A short limit exists to
+ * exercise that path: the data always arrives, only later.  The pages have
+ * no counterpart (the staging and its bounded wait are this library's
+ * design).  Returns Q4_EINVAL for a negative value.
+ */
+int q4adamw_set_stage_wait_limit(int64_t cycles);
 
 /*
  * Decode the state of one tensor into FP32 device buffers of numel floats
@@ -309,6 +382,17 @@ int q4adamw_dequant_state(const q4adamw_tensor_t* t, int recipe, float* m_out, f
 #define Q4ADAMW_NOALLOC_SCRATCH_BYTES (4 * 1024 * 1024)
 int q4adamw_step_noalloc(const q4adamw_tensor_t* t, int n, float lr, float beta1, float beta2, float eps,
                          float weight_decay, int64_t step, uint64_t seed, int recipe, uint32_t flags, void* stream);
+
+/*
+ * Status word of the most recent q4adamw_step_noalloc on the current device
+ * (the counterpart of q4adamw_step_status for the static scratch, whose
+ * device address callers never see): synchronises `stream`, then reads the
+ * word; 0 means the step ran to completion, Q4_STATUS_STAGE_TIMEOUT as for
+ * q4adamw_step_status.  Like the step, it shares the one array: read it on
+ * the stream of the call it reports on, before the next noalloc call.  Q4_EINVAL
+ * for a NULL status, Q4_ECUDA if the address lookup or the copy fails.
+ */
+int q4adamw_step_noalloc_status(uint32_t* status, void* stream);
 
 /*
  * The library's own codebook tables (host-only).  which: 0 = NF4, 1 = Dyn4

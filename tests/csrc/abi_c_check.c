@@ -50,6 +50,9 @@ int main(void) {
     CHECK(q4adamw_step_clip(NULL, 0, 1e-3f, 0.9f, 0.999f, 1e-8f, 0.1f, 1, 0, 0, 0, 0.0f, NULL, NULL, 0, NULL) ==
           Q4_EINVAL);
     CHECK(q4adamw_draws(0, 0, 0, 0, 0, 4, NULL, NULL) == Q4_EINVAL);
+    CHECK(q4adamw_set_stage_wait_limit(-1) == Q4_EINVAL);
+    CHECK(q4adamw_set_stage_wait_limit(1000) == Q4_OK && q4adamw_set_stage_wait_limit(0) == Q4_OK);
+    CHECK(q4adamw_step_noalloc_status(NULL, NULL) == Q4_EINVAL);
     printf("ok\n");
     return 0;
 }

@@ -240,3 +240,43 @@ def test_header_check():
     h.format = 0
     with pytest.raises(q4.Q4Error):
         q4.q4adamw_header_check(h, "zip_sr")
+
+
+def _dp_list(shards, full, rows, flags):
+    arr = (q4.Q4Tensor * len(shards))()
+    fake = 1 << 40                        # host-only calls never touch the pointers
+    for k, ((start, n), r, f) in enumerate(zip(shards, rows, flags)):
+        d = arr[k]
+        d.param = d.grad = d.m_codes = d.m_scale = d.v_codes = d.v_scale = d.v_row = d.v_col = fake
+        d.numel, d.rows, d.elem_offset, d.flags = n, r, start, f
+    return arr, (ctypes.c_int64 * len(full))(*full)
+
+
+def test_dp_host_calls_size_and_validate_shards():
+    L = _native.lib()
+    F = _native.Q4_T_FACTORED
+    # a 100 x 200 parameter cut inside a row, an empty shard of a 48 x 256 one,
+    # and a 1-D tensor (no statistics)
+    arr, full = _dp_list([(8960, 11040), (0, 0), (128, 172)], [20000, 12288, 300], [100, 48, 1], [F, F, 0])
+    n = ctypes.c_int64()
+    assert L.q4adamw_dp_sums_floats(arr, 3, 2, full, ctypes.byref(n)) == 0
+    assert n.value == (100 + 200) + (48 + 256)
+    ws = ctypes.c_int64()
+    assert L.q4adamw_dp_workspace_bytes(arr, 3, 2, full, ctypes.byref(ws)) == 0 and ws.value % 256 == 0
+    # other recipes keep no statistics
+    assert L.q4adamw_dp_sums_floats(arr, 3, 0, full, ctypes.byref(n)) == 0 and n.value == 0
+    # NULL full_numel: whole tensors; the cut shard is then not a whole matrix
+    assert L.q4adamw_dp_sums_floats(arr, 3, 2, None, ctypes.byref(n)) == _native.Q4_ESHAPE
+    # the parameter's element count must be a multiple of rows, the shard inside it
+    bad, full_bad = _dp_list([(0, 256)], [20001], [100], [F])
+    assert L.q4adamw_dp_sums_floats(bad, 1, 2, full_bad, ctypes.byref(n)) == _native.Q4_ESHAPE
+    out, full_out = _dp_list([(19968, 128)], [20000], [100], [F])
+    assert L.q4adamw_dp_sums_floats(out, 1, 2, full_out, ctypes.byref(n)) == _native.Q4_ESHAPE
+    # an empty factored shard still needs R and C (every rank updates them)
+    empty, full_e = _dp_list([(0, 0)], [12288], [48], [F])
+    empty[0].v_row = 0
+    assert L.q4adamw_dp_sums_floats(empty, 1, 2, full_e, ctypes.byref(n)) == _native.Q4_EINVAL
+    # device calls validate before any device work
+    assert L.q4adamw_dp_step(arr, 3, 1e-3, 0.9, 0.999, 1e-8, 0.1, 1, 0, 2, 0, full, None, 1.0, None, None, 0,
+                             None) == _native.Q4_EWORKSPACE
+    assert L.q4adamw_dp_factored_sums(arr, 3, 2, full, 1.0, None, None, None, 0, None) == _native.Q4_EINVAL

@@ -6,7 +6,9 @@ implicit synchronisation is not acceptable.  q4adamw_step_noalloc serves them
 from a fixed static device array.  These tests call it through the C ABI and
 check, over two calls in a row, that it produces the same bits as
 q4adamw_step with a caller workspace (the parity bar of every GPU test here is
-bit-exact), and that a tensor list too large for the static array is refused.
+bit-exact), that the status word in the static array reads 0 after each call
+(q4adamw_step_noalloc_status), and that a tensor list too large for the static
+array is refused.
 This file is collected last on purpose.
 """
 
@@ -52,6 +54,8 @@ def test_noalloc_matches_workspace_step_two_calls(recipe):
         q4.q4adamw_step_noalloc(na.descs, h["lr"], h["beta1"], h["beta2"], h["eps"], h["weight_decay"], t, 5,
                                 recipe, q4.Q4_LM_HEAD_SR_ACTIVE)
         torch.cuda.synchronize()
+        # the static scratch's status word: the noalloc step ran to completion
+        assert q4.q4adamw_step_noalloc_status() == 0, (recipe, t)
         a, b = _buffers(ref), _buffers(na)
         for name in a:
             assert torch.equal(a[name].view(torch.uint8), b[name].view(torch.uint8)), (recipe, t, name)
