@@ -13,8 +13,6 @@ namespace q4 {
 constexpr int kBlock = 128;        // elements per quantisation block
 constexpr int kStepWarps = 16;     // warps per CTA of the step kernel
 constexpr int kStepThreads = kStepWarps * 32;
-constexpr int kStages = 4;         // staging buffers per warp (tiles in flight)
-static_assert((kStages & (kStages - 1)) == 0 && kStages >= 2, "the staging ring is indexed with a mask");
 constexpr int kVLut = 4096;        // entries of the log-bucket candidate tables
                                    // (one per bits(x)>>19 of a non-negative float)
 
@@ -103,7 +101,6 @@ struct StepParams {
     const float* sqnorm;          // global-norm clipping: device sum of squares, or NULL
     float max_norm;               //   and the clipping threshold
     long long wait_cycles;        // limit of a warp's wait for a staged tile (SM clock cycles)
-    int chunk;                    // consecutive tiles a warp takes at a time (set by launch_step)
     // the step scalars broadcast to pairs, for the paired FP32 instructions
     float2 x2_beta1, x2_beta2, x2_omb1, x2_omb2, x2_c2, x2_eps, x2_decay, x2_neg_step;
     uint32_t round_keys[20];      // Philox key schedule: (k0, k1) for rounds 0..9

@@ -7,15 +7,16 @@
 //
 // Data movement.  The grid is persistent (one 16-warp CTA per SM).  The global
 // list of tiles of all tensors (the tensor-chunk table is the prefix sum of
-// tiles per tensor) is cut into chunks of P.chunk consecutive tiles, dealt
-// round-robin to the warps of the grid; within a chunk and a tensor each copy
-// source advances by a constant per tile.  Each warp keeps
-// a ring of kStages shared-memory staging buffers: while it computes tile k,
-// tiles k+1 .. k+kStages-1 are in flight.  Lanes 0-7 fill a buffer in one
-// pass: four cp.async.bulk copies (BF16 gradient, FP32 master weight, packed m
+// tiles per tensor) is cut into one contiguous range per warp; within a tensor
+// each copy source advances by a constant per tile.  Each warp keeps two
+// shared-memory stage buffers of three tiles each: while it computes the tiles
+// of one, the next three are in flight.  A stage is filled by one pass of 24
+// lanes, lanes 8g..8g+7 for its tile g, each group with its own cursor: per
+// tile four cp.async.bulk copies (BF16 gradient, FP32 master weight, packed m
 // and v code words; the tensor memory access unit moves whole 16-byte
 // granules) and four 4-byte cp.async copies (the block scales, which are only
-// 4-byte aligned), all completing on the buffer's mbarrier.  A tile whose length is
+// 4-byte aligned), all completing on the stage's mbarrier, so a stage costs
+// one wait and one issue pass for three tiles.  A tile whose length is
 // not a multiple of 8 elements (a tensor's ragged tail) is read directly from
 // global memory instead.  Results (FP32 and BF16 weights, codes, scales) are
 // written straight from registers with coalesced streaming stores.  Every
@@ -61,7 +62,6 @@ namespace {
 
 constexpr float kMagic = 12582912.0f;                // 1.5 * 2^23: rounds to an integer in the low mantissa bits
 constexpr float kTwoM24 = 5.9604644775390625e-08f;   // 2^-24
-constexpr int kMaxChunk = 16;                        // most consecutive tiles a warp takes at a time
 
 struct __align__(16) Stage {
     uint4 grad[32];     // 256 BF16 gradients
@@ -79,21 +79,25 @@ static_assert(sizeof(Stage) % 16 == 0, "stage buffers must keep 16-byte alignmen
 struct __align__(256) WarpTables {
     float deqm[32];        // [half][16] NF4 level * old s_m
     float deqv[32];        // [half][16] v level * old s_v
-    float2 mt[2][64];      // fast path: [half][linear bucket] {NF4 threshold of the candidate * new s_m, candidate};
-                           // TorchAO: floats 0..8 of [half] = SDyn4 magnitudes A_0..A_7 * new s_m, +inf
-    float4 ve[2][16];      // fast path, per half: ZIP-SR a_{c+1} by cell (floats 0..15) and (r_k, d_k)
-                           // by cell (float2 8..23); RTN {t_c s_v, L_c, L_{c+1}} by cell
+    float mt[2][48];       // fast path, per half: m State-SR a_{c+1} by cell (floats 0..15) and (a_k, d_k)
+                           // by cell (float2 8..23); TorchAO: floats 0..8 = SDyn4 magnitudes A_0..A_7 * new
+                           // s_m, +inf
+    float2 rdv[2][16];     // fast path, per half: ZIP-SR (r_k, d_k) by cell
     float tm[32];          // general path: [half][16] NF4 threshold * new s_m
     float am[32];          // [half][16] NF4 level * new s_m (LM-head SR)
     float av[32];          // [half][16] v level * new s_v (ZIP-SR) or v threshold * new s_v (RTN)
     float2 rd[32];         // [half][16] (r_k, (r_k - r_{k+1}) * 2^-24) for ZIP-SR
 };
 
+constexpr int kTilesPerStage = 3;   // tiles a stage buffer holds (8 issuing lanes each)
+constexpr int kStageBufs = 2;       // stage buffers per warp
+static_assert(kTilesPerStage * 8 <= 32 && kStageBufs >= 2, "stage geometry");
+
 struct __align__(256) WarpSmem {
     WarpTables wt;
-    Stage st[kStages];
-    DevTensor desc;                      // descriptor of the tensor being computed
-    unsigned long long bar[kStages];     // one mbarrier per staging buffer
+    Stage st[kStageBufs][kTilesPerStage];   // stage buffers of kTilesPerStage tiles each
+    DevTensor desc;                         // descriptor of the tensor being computed
+    unsigned long long bar[kStageBufs];     // one mbarrier per stage buffer
 };
 
 struct __align__(256) SmemAll {
@@ -921,7 +925,7 @@ __device__ __forceinline__ void compute_tile_full(const StepParams& P, const Dev
         const float rk = P.fast_math ? precond<true>(P, a) : precond<false>(P, a);
         const float rk1 = __shfl_down_sync(0xffffffffu, rk, 1);
         const float dk = j < 15 ? __fmul_rn(__fsub_rn(rk, rk1), kTwoM24) : 0.f;
-        reinterpret_cast<float2*>(&wt.ve[half][4])[j] = make_float2(rk, dk);  // (r_k, d_k) by cell
+        wt.rdv[half][j] = make_float2(rk, dk);  // (r_k, d_k) by cell
     }
     // the v RTN codes (ZE-EDEN, TorchAO, factored 1-D) and the NF4 RTN m codes
     // read constant tables only: no per-block table to wait for
@@ -980,7 +984,7 @@ __device__ __forceinline__ void compute_tile_full(const StepParams& P, const Dev
     float sv_store = s_v;
     if (!fact) {
         const float rho = rcp_rn_normal<1>(s_v);
-        const uint32_t ve_base = tb + (uint32_t)((char*)&wt.ve[half][0] - (char*)&wt);
+        const uint32_t rd_base = tb + (uint32_t)((char*)&wt.rdv[half][0] - (char*)&wt);
         uint32_t c[8];
         const float2 sv2 = make_float2(s_v, s_v);
         if (RECIPE == Q4_RECIPE_ZIP_SR) {
@@ -998,8 +1002,8 @@ __device__ __forceinline__ void compute_tile_full(const StepParams& P, const Dev
                 const bool up0 = a1.x <= v1[k].x;
                 const bool up1 = a1.y <= v1[k].y;
                 const uint32_t k0 = c0 + (up0 ? 1u : 0u), k1 = c1 + (up1 ? 1u : 0u);
-                const float2 e0v = lds_f32x2(ve_base + 64u + k0 * 8u);
-                const float2 e1v = lds_f32x2(ve_base + 64u + k1 * 8u);
+                const float2 e0v = lds_f32x2(rd_base + k0 * 8u);
+                const float2 e1v = lds_f32x2(rd_base + k1 * 8u);
                 const float2 rk = make_float2(e0v.x, e1v.x);
                 const float2 dk = make_float2(e0v.y, e1v.y);
                 // u (r_k - r_{k+1}) with u = (w >> 8) 2^-24, as (w >> 8) ((r_k - r_{k+1}) 2^-24)
@@ -1095,10 +1099,10 @@ __global__ void __launch_bounds__(kStepThreads, 1) step_kernel(const __grid_cons
             reinterpret_cast<uint32_t*>(sm.lut_m_log)[i] = reinterpret_cast<const uint32_t*>(P.tab.lut_m_log)[i];
     }
     if (lane == 0) {
-        // count 5: the arrive.expect_tx of lane 0 and the arrives that
-        // cp.async.mbarrier.arrive.noinc of lanes 4..7 trigger once their
-        // scale copies have landed
-        for (int s = 0; s < kStages; ++s) mbar_init(&ws.bar[s], 5);
+        // count 5 per tile of a stage: the arrive (with expect_tx) of its
+        // group's lead lane and the arrives that cp.async.mbarrier.arrive.noinc
+        // of the group's four scale lanes trigger once their copies have landed
+        for (int s = 0; s < kStageBufs; ++s) mbar_init(&ws.bar[s], 5 * kTilesPerStage);
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
     __syncthreads();
@@ -1112,63 +1116,66 @@ __global__ void __launch_bounds__(kStepThreads, 1) step_kernel(const __grid_cons
     const float clip = clip_factor(P.sqnorm, P.max_norm);
     const uint64_t policy = evict_first_policy();
 
-    // Work split: the global tile list is cut into chunks of `chunk` consecutive
-    // tiles, dealt round-robin to the W warps of the grid (warp w takes chunks
-    // w, w+W, ...).  Inside a chunk a warp's tiles are consecutive, so within a
-    // tensor every copy source advances by a constant; dealing chunks
-    // round-robin spreads tensors of unequal cost over all warps.
+    // Work split: warp gw of W takes the contiguous tiles [T gw / W, T (gw+1) / W)
+    // of the global tile list (within a tensor every copy source advances by a
+    // constant).  A launch holds tiles of one instantiation's cost, so the
+    // ranges need no finer interleaving.  Its tiles are staged kTilesPerStage
+    // at a time: stage iteration i fills buffer i % kStageBufs with tiles
+    // kTilesPerStage i + g of the warp's range; while the warp computes one
+    // stage the next kStageBufs - 1 are in flight.
     const int64_t gw = (int64_t)blockIdx.x * kStepWarps + warp;
     const int64_t W = (int64_t)gridDim.x * kStepWarps;
     const int64_t total = P.total_pairs;
-    const int kChunk = P.chunk;
-    const int64_t n_chunks = (total + kChunk - 1) / kChunk;
-    if (gw >= n_chunks) return;
-    const int64_t my_chunks = (n_chunks - 1 - gw) / W + 1;
-    const bool owns_last = (n_chunks - 1) % W == gw;
-    const int n_it = (int)(my_chunks * kChunk - (owns_last ? n_chunks * kChunk - total : 0));
-    const int64_t t_begin = gw * kChunk;
-    const int64_t chunk_jump = (W - 1) * kChunk;   // tiles skipped between two of this warp's chunks
+    const int64_t t_begin = total * gw / W, t_end = total * (gw + 1) / W;
+    const int n_tiles = (int)(t_end - t_begin);
+    if (n_tiles <= 0) return;
+    const int n_st = (n_tiles + kTilesPerStage - 1) / kTilesPerStage;   // stage iterations
 
-    // Tensor holding t_begin: the last t with prefix[t] <= t_begin.
-    int t0 = 0;
+    // Issue cursors.  Lanes 8g..8g+7 stage tile g of every stage (g <
+    // kTilesPerStage); within a group lane 0 copies the gradient, 1 the master
+    // weight, 2 the m codes, 3 the v codes (bulk copies), 4, 5 the m scales and
+    // 6, 7 the v scales of the tile's two blocks (4-byte copies).  Each group
+    // walks its own tiles (every kTilesPerStage-th tile of the range); the
+    // remaining lanes issue nothing.
+    const int sl = lane & 7;
+    const bool copier = lane < 8 * kTilesPerStage;
+    const int grp = copier ? lane >> 3 : 0;
+    const uint32_t cp_field = sl == 0 ? (uint32_t)offsetof(DevTensor, grad)
+                              : sl == 1 ? (uint32_t)offsetof(DevTensor, param)
+                              : sl == 2 ? (uint32_t)offsetof(DevTensor, mc)
+                              : sl == 3 ? (uint32_t)offsetof(DevTensor, vc)
+                              : sl < 6  ? (uint32_t)offsetof(DevTensor, ms)
+                                        : (uint32_t)offsetof(DevTensor, vs);
+    const uint32_t cp_dst = (uint32_t)grp * (uint32_t)sizeof(Stage) +
+                            (sl == 0 ? (uint32_t)offsetof(Stage, grad)
+                             : sl == 1 ? (uint32_t)offsetof(Stage, param)
+                             : sl == 2 ? (uint32_t)offsetof(Stage, mc)
+                             : sl == 3 ? (uint32_t)offsetof(Stage, vc)
+                             : sl < 6  ? (uint32_t)offsetof(Stage, ms) + 4u * (sl & 1)
+                                       : (uint32_t)offsetof(Stage, vs) + 4u * (sl & 1));
+    // bytes of this lane's copy for a complete tile, and the source advance per tile
+    const uint32_t cp_full = sl == 0 ? 512u : sl == 1 ? 1024u : sl < 4 ? 128u : 4u;
+    const int64_t cp_step = sl == 0 ? 512 : sl == 1 ? 1024 : sl < 4 ? 128 : 8;
+    const uint32_t cp_first = (sl >= 4 && (sl & 1)) ? 4u : 0u;    // second block's scale
+    const uint32_t is_bulk = (copier && sl < 4) ? 1u : 0u;
+    const uint32_t is_scale = (copier && sl >= 4) ? 1u : 0u;
+    const uint32_t is_lead = (copier && sl == 0) ? 1u : 0u;
+    const uint32_t stage0 = smem_addr(&ws.st[0][0]);
+    const uint32_t bar0 = smem_addr(&ws.bar[0]);
+
+    // this lane's group: tiles t_begin + grp, t_begin + grp + kTilesPerStage, ...
+    int i_t = 0;
     {
+        const int64_t t0i = t_begin + grp < t_end ? t_begin + grp : t_begin;
         int lo = 0, hi = P.n_tensors - 1;
         while (lo < hi) {
             const int mid = (lo + hi + 1) >> 1;
-            if (__ldg(P.pair_prefix + mid) <= t_begin) lo = mid; else hi = mid - 1;
+            if (__ldg(P.pair_prefix + mid) <= t0i) lo = mid; else hi = mid - 1;
         }
-        t0 = lo;
+        i_t = lo;
     }
-
-    // Issue cursor.  Lanes 0..7 each own one copy of every tile: 0 gradient,
-    // 1 master weight, 2 m codes, 3 v codes (bulk copies); 4, 5 the m scales and
-    // 6, 7 the v scales of the tile's two blocks (4-byte copies).
-    const uint32_t cp_field = lane == 0 ? (uint32_t)offsetof(DevTensor, grad)
-                              : lane == 1 ? (uint32_t)offsetof(DevTensor, param)
-                              : lane == 2 ? (uint32_t)offsetof(DevTensor, mc)
-                              : lane == 3 ? (uint32_t)offsetof(DevTensor, vc)
-                              : lane < 6  ? (uint32_t)offsetof(DevTensor, ms)
-                                          : (uint32_t)offsetof(DevTensor, vs);
-    const uint32_t cp_dst = lane == 0 ? (uint32_t)offsetof(Stage, grad)
-                            : lane == 1 ? (uint32_t)offsetof(Stage, param)
-                            : lane == 2 ? (uint32_t)offsetof(Stage, mc)
-                            : lane == 3 ? (uint32_t)offsetof(Stage, vc)
-                            : lane < 6  ? (uint32_t)offsetof(Stage, ms) + 4u * (lane & 1)
-                                        : (uint32_t)offsetof(Stage, vs) + 4u * (lane & 1);
-    // bytes of this lane's copy for a complete tile, and the source advance per tile
-    const uint32_t cp_full = lane == 0 ? 512u : lane == 1 ? 1024u : lane < 4 ? 128u : lane < 8 ? 4u : 0u;
-    const int64_t cp_step = lane == 0 ? 512 : lane == 1 ? 1024 : lane < 4 ? 128 : 8;
-    const uint32_t cp_first = (lane >= 4 && (lane & 1)) ? 4u : 0u;    // second block's scale
-    const uint32_t is_bulk = lane < 4 ? 1u : 0u;
-    const uint32_t is_scale = (lane >= 4 && lane < 8) ? 1u : 0u;
-    const uint32_t stage0 = smem_addr(&ws.st[0]);
-    const uint32_t bar0 = smem_addr(&ws.bar[0]);
-
-    int i_t = t0;
-    int64_t i_tile = t_begin;                                // global tile index
-    int i_k = 0;                                             // tile index within the chunk
-    int64_t i_p = t_begin - __ldg(P.pair_prefix + t0);      // tile index within the tensor
-    int64_t i_n = __ldg(P.pair_prefix + t0 + 1) - __ldg(P.pair_prefix + t0);
+    int64_t i_p = t_begin + grp - __ldg(P.pair_prefix + i_t);   // tile index within the tensor
+    int64_t i_n = __ldg(P.pair_prefix + i_t + 1) - __ldg(P.pair_prefix + i_t);
     int64_t i_numel = 0;
     uint32_t i_bytes = 0, i_total = 0;
     bool i_fact = false;
@@ -1179,77 +1186,78 @@ __global__ void __launch_bounds__(kStepThreads, 1) step_kernel(const __grid_cons
         i_fact = is_factored_recipe(RECIPE) && (RECIPE == kRecipeFactoredOnly || (dt->flags & DF_FACTORED));
         const char* base = *reinterpret_cast<const char* const*>(reinterpret_cast<const char*>(dt) + cp_field);
         i_src = base + cp_first + i_p * cp_step;
-        i_bytes = (i_fact && (lane == 3 || lane >= 6)) ? 0u : cp_full;
+        i_bytes = (i_fact && (sl == 3 || sl >= 6)) ? 0u : cp_full;
         i_total = 1536u + 128u + (i_fact ? 0u : 128u);
     };
     load_issue_tensor();
 
-    auto issue = [&](int it) {
-        if (i_k == kChunk) {
-            // next chunk of this warp: seek forward to the tensor holding it
-            i_k = 0;
-            i_tile += chunk_jump;
-            while (i_tile >= __ldg(P.pair_prefix + i_t + 1)) ++i_t;
-            const int64_t pb = __ldg(P.pair_prefix + i_t);
-            i_p = i_tile - pb;
-            i_n = __ldg(P.pair_prefix + i_t + 1) - pb;
-            load_issue_tensor();
-        } else if (i_p == i_n) {
-            do {
-                ++i_t;
-                i_n = __ldg(P.pair_prefix + i_t + 1) - __ldg(P.pair_prefix + i_t);
-            } while (i_n == 0);
-            i_p = 0;
-            load_issue_tensor();
-        }
-        const int s = it & (kStages - 1);
+    // Stage iteration k: the group's tile t_begin + kTilesPerStage k + grp
+    // (absent past the range end); afterwards the cursor moves kTilesPerStage
+    // tiles on.
+    auto issue = [&](int k) {
+        const int s = k % kStageBufs;
         const uint32_t bar = bar0 + 8u * (uint32_t)s;
-        const uint32_t dst = stage0 + (uint32_t)s * (uint32_t)sizeof(Stage) + cp_dst;
-        uint32_t bytes = i_bytes, total = i_total, staged = 1u;
-        if (i_p == i_n - 1) {
+        const uint32_t dst = stage0 + (uint32_t)s * (uint32_t)(kTilesPerStage * sizeof(Stage)) + cp_dst;
+        const bool present = kTilesPerStage * k + grp < n_tiles;
+        uint32_t bytes = i_bytes, total_b = i_total, staged = present ? 1u : 0u;
+        if (present && i_p == i_n - 1) {
             // a tensor's last tile may hold one block and a partial block
             const int64_t left = i_numel - i_p * 2 * kBlock;
             const uint32_t nel = left >= 2 * kBlock ? 2u * kBlock : (uint32_t)left;
             const uint32_t nb = nel > (uint32_t)kBlock ? 2u : 1u;
             staged = (nel & 7u) == 0 ? 1u : 0u;
-            const uint32_t b = lane & 1;
-            bytes = lane < 2   ? nel * (lane == 0 ? 2u : 4u)
-                    : lane < 4 ? ((lane == 3 && i_fact) ? 0u : nb * 64u)
-                               : ((b < nb && (lane < 6 || !i_fact)) ? 4u : 0u);
-            total = nel * 6u + nb * 64u * (i_fact ? 1u : 2u);
+            const uint32_t b = sl & 1;
+            bytes = sl < 2   ? nel * (sl == 0 ? 2u : 4u)
+                    : sl < 4 ? ((sl == 3 && i_fact) ? 0u : nb * 64u)
+                             : ((b < nb && (sl < 6 || !i_fact)) ? 4u : 0u);
+            total_b = nel * 6u + nb * 64u * (i_fact ? 1u : 2u);
         }
-        // lane 0 announces the bulk bytes (or completes its arrival for a ragged
-        // tile, which is then read from global memory) before any copy starts
-        mbar_arrive_expect_tx_if(lane == 0 && staged, bar, total);
-        mbar_arrive_if(lane == 0 && !staged, bar);
+        // each group's lead lane announces its tile's bulk bytes (or arrives
+        // plainly for a ragged or absent tile) before any copy starts
+        mbar_arrive_expect_tx_if(is_lead & staged, bar, total_b);
+        mbar_arrive_if(is_lead & (staged ^ 1u), bar);
         __syncwarp();
         // the warp's earlier reads of this buffer precede the copies into it
         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
         bulk_load_if(staged & is_bulk & (bytes != 0u), dst, i_src, bytes, bar, policy);
         cp_async4_if(staged & is_scale & (bytes != 0u), dst, i_src);
         cp_async_arrive_noinc_if(is_scale, bar);
-        i_src += cp_step;
-        ++i_p;
-        ++i_tile;
-        ++i_k;
+        if (present) {
+            i_p += kTilesPerStage;
+            i_src += kTilesPerStage * cp_step;
+            if (i_p >= i_n) {
+                do {
+                    i_p -= i_n;
+                    if (i_t + 1 >= P.n_tensors) break;
+                    ++i_t;
+                    i_n = __ldg(P.pair_prefix + i_t + 1) - __ldg(P.pair_prefix + i_t);
+                } while (i_p >= i_n);
+                load_issue_tensor();
+            }
+        }
     };
 
-    const int pro = n_it < kStages - 1 ? n_it : kStages - 1;
-    for (int it = 0; it < pro; ++it) issue(it);
+    for (int k = 0; k < kStageBufs - 1 && k < n_st; ++k) issue(k);
     __syncwarp();
 
-    // Compute cursor.
-    int c_t = t0;
-    int64_t c_tile = t_begin;
-    int c_k = 0;
-    int64_t c_p = t_begin - __ldg(P.pair_prefix + t0);
-    int64_t c_n = __ldg(P.pair_prefix + t0 + 1) - __ldg(P.pair_prefix + t0);
+    // Compute cursor: tile c_p of tensor c_t (one tile at a time).
+    int c_t = i_t;
+    {
+        int lo = 0, hi = P.n_tensors - 1;
+        while (lo < hi) {
+            const int mid = (lo + hi + 1) >> 1;
+            if (__ldg(P.pair_prefix + mid) <= t_begin) lo = mid; else hi = mid - 1;
+        }
+        c_t = lo;
+    }
+    int64_t c_p = t_begin - __ldg(P.pair_prefix + c_t);
+    int64_t c_n = __ldg(P.pair_prefix + c_t + 1) - __ldg(P.pair_prefix + c_t);
     reinterpret_cast<uint32_t*>(&ws.desc)[lane] = __ldg(reinterpret_cast<const uint32_t*>(P.tensors + c_t) + lane);
     __syncwarp();
     // factored recipe: (row, column) of the current tile's first element in
     // the parameter's matrix (a shard starts at fbase), for tensors with
-    // DF_CVEC; set by one division per chunk or tensor, then advanced by 256
-    // columns a tile (at most one wrap, as cols >= 256)
+    // DF_CVEC; set by one division per tensor, then advanced by 256 columns a
+    // tile (at most one wrap, as cols >= 256)
     uint32_t f_row = 0, f_col = 0;
     auto fpos = [&]() {
         if (is_factored_recipe(RECIPE) && (ws.desc.flags & DF_CVEC)) {
@@ -1260,56 +1268,52 @@ __global__ void __launch_bounds__(kStepThreads, 1) step_kernel(const __grid_cons
         }
     };
     fpos();
-    for (int it = 0; it < n_it; ++it) {
-        if (it + kStages - 1 < n_it) issue(it + kStages - 1);
-        const int s = it & (kStages - 1);
-        const bool ok =
-            __all_sync(0xffffffffu, mbar_wait_bounded(&ws.bar[s], (uint32_t)((it / kStages) & 1), P.wait_cycles));
+    for (int it = 0; it < n_st; ++it) {
+        if (it + kStageBufs - 1 < n_st) issue(it + kStageBufs - 1);
+        const int s = it % kStageBufs;
+        const bool ok = __all_sync(
+            0xffffffffu, mbar_wait_bounded(&ws.bar[s], (uint32_t)((it / kStageBufs) & 1), P.wait_cycles));
         if (!ok) {
             if (lane == 0) atomicOr(P.status, ST_STAGE_TIMEOUT);
             // drain the copies this warp still has in flight (the late stage
             // included), each with the default bound, then leave
-            const int last = (it + kStages - 1 < n_it) ? it + kStages - 1 : n_it - 1;
+            const int last = it + kStageBufs - 1 < n_st ? it + kStageBufs - 1 : n_st - 1;
             for (int k = it; k <= last; ++k)
-                (void)mbar_wait_bounded(&ws.bar[k & (kStages - 1)], (uint32_t)((k / kStages) & 1),
+                (void)mbar_wait_bounded(&ws.bar[k % kStageBufs], (uint32_t)((k / kStageBufs) & 1),
                                         kDefaultWaitCycles);
             return;
         }
-        if (c_k == kChunk || c_p == c_n) {
-            if (c_k == kChunk) {
-                c_k = 0;
-                c_tile += chunk_jump;
-                while (c_tile >= __ldg(P.pair_prefix + c_t + 1)) ++c_t;
-            } else {
+#pragma unroll 1
+        for (int sub = 0; sub < kTilesPerStage; ++sub) {
+            if (kTilesPerStage * it + sub >= n_tiles) break;
+            if (c_p == c_n) {
                 do {
                     ++c_t;
                 } while (__ldg(P.pair_prefix + c_t + 1) == __ldg(P.pair_prefix + c_t));
+                c_p = 0;
+                c_n = __ldg(P.pair_prefix + c_t + 1) - __ldg(P.pair_prefix + c_t);
+                reinterpret_cast<uint32_t*>(&ws.desc)[lane] =
+                    __ldg(reinterpret_cast<const uint32_t*>(P.tensors + c_t) + lane);
+                __syncwarp();
+                fpos();
             }
-            const int64_t pb = __ldg(P.pair_prefix + c_t);
-            c_p = c_tile - pb;
-            c_n = __ldg(P.pair_prefix + c_t + 1) - pb;
-            reinterpret_cast<uint32_t*>(&ws.desc)[lane] =
-                __ldg(reinterpret_cast<const uint32_t*>(P.tensors + c_t) + lane);
+            Stage& stg = ws.st[s][sub];
+            const bool full = c_p < c_n - 1 || ws.desc.numel - c_p * 2 * kBlock >= 2 * kBlock;
+            if (full && !NEXTR) {
+                compute_tile_full<RECIPE, URTN, MSR>(P, ws.desc, c_p, stg, lane, sm, ws.wt, my_nf4, my_nf4t,
+                                                     my_vl, my_vt, my_vl1, my_mag, clip, f_row, f_col);
+            } else {
+                const int64_t left = ws.desc.numel - c_p * 2 * kBlock;
+                compute_tile<RECIPE, URTN, NEXTR>(P, ws.desc, c_p, (full || (left & 7) == 0) ? &stg : nullptr,
+                                                  lane, sm, ws.wt, my_nf4, my_nf4t, my_vl, my_vt, clip);
+            }
+            ++c_p;
+            if (is_factored_recipe(RECIPE)) {
+                f_col += 2 * kBlock;
+                if (f_col >= (uint32_t)ws.desc.cols) { f_col -= (uint32_t)ws.desc.cols; ++f_row; }
+            }
             __syncwarp();
-            fpos();
         }
-        const bool full = c_p < c_n - 1 || ws.desc.numel - c_p * 2 * kBlock >= 2 * kBlock;
-        if (full && !NEXTR) {
-            compute_tile_full<RECIPE, URTN, MSR>(P, ws.desc, c_p, ws.st[s], lane, sm, ws.wt, my_nf4, my_nf4t,
-                                                 my_vl, my_vt, my_vl1, my_mag, clip, f_row, f_col);
-        } else {
-            const int64_t left = ws.desc.numel - c_p * 2 * kBlock;
-            compute_tile<RECIPE, URTN, NEXTR>(P, ws.desc, c_p, (full || (left & 7) == 0) ? &ws.st[s] : nullptr,
-                                              lane, sm, ws.wt, my_nf4, my_nf4t, my_vl, my_vt, clip);
-        }
-        ++c_p;
-        ++c_tile;
-        ++c_k;
-        if (is_factored_recipe(RECIPE)) {
-            f_col += 2 * kBlock;
-            if (f_col >= (uint32_t)ws.desc.cols) { f_col -= (uint32_t)ws.desc.cols; ++f_row; }
-        }
-        __syncwarp();
     }
 }
 
@@ -1341,16 +1345,8 @@ int step_grid_size(int device, int64_t total_pairs) {
     return (int)(need < full ? (need > 0 ? need : 1) : full);
 }
 
-int launch_step(const StepParams& p_in, int grid, void* stream) {
+int launch_step(const StepParams& p, int grid, void* stream) {
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    // Chunk size: kMaxChunk tiles when every warp gets many chunks (a chunk
-    // switch costs a tensor search; within a chunk copy sources advance by
-    // constants), fewer when the launch is small, so that its tiles spread
-    // over the warps instead of a few warps taking 16 each.
-    StepParams p = p_in;
-    const int64_t warps = (int64_t)grid * kStepWarps;
-    const int64_t per = p.total_pairs / (4 * warps);
-    p.chunk = (int)(per >= kMaxChunk ? kMaxChunk : per < 1 ? 1 : per);
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return (int)e;
