@@ -13,10 +13,14 @@
 //   stats_kernel    persistent CTAs of 8 warps, four per SM, each taking tiles
 //                   of 256 rows x 256 columns of a tensor in turn: g is read
 //                   once, 16 bytes (8 BF16) per lane and row.
-//                   Each lane sums the 8 squares of its row chunk; a warp's 32
-//                   row chunks are reduced across lanes by a transpose tree
-//                   (lane l ends with row l's sum over the 256 columns), giving
-//                   row partials per 256-column segment.  Column sums over the
+//                   Each lane sums the 8 squares of its row chunk; each of a
+//                   warp's 32 rows is summed over the lanes with the pairing of
+//                   an xor butterfly (lane offsets 16, 8, 4, 2, 1), giving row
+//                   partials per 256-column segment.  A strip of 32 rows that
+//                   lies wholly inside the tensor's elements is read as 4
+//                   batches of 8 independent loads per lane; edge strips take a
+//                   per-row checked path with the same pairing (a transpose
+//                   tree, lane l ending with row l's sum).  Column sums over the
 //                   warp's 32 rows are combined over the 8 warps in warp order,
 //                   giving column partials per 256-row slab.
 //   rows_kernel,    a row's partials summed in segment order by one thread, a
@@ -24,8 +28,8 @@
 //                   slab ranges per warp, then the warps in order); mean = sum /
 //                   cols (rows), and the average R_i <- beta2 R_i + (1-beta2)
 //                   mean (C_j likewise).
-//   rbar_kernel     one CTA per factored tensor: mean(R) in a fixed tree order,
-//                   stored with its correctly rounded reciprocal.
+//   rbar_kernel     one 1024-thread CTA per factored tensor: mean(R) in a fixed
+//                   tree order, stored with its correctly rounded reciprocal.
 // The step kernel then forms vhat_ij = R_i * C_j / mean(R) per element (with
 // the global-norm clip factor, when given, applied to g before squaring here).
 #include <cuda_runtime.h>
@@ -67,56 +71,96 @@ __global__ void __launch_bounds__(kStatsWarps * 32, kStatsCtasPerSm) stats_kerne
         const int nc = c0 >= cols ? 0 : (cols - c0 >= 8 ? 8 : (int)(cols - c0));
         const bool vec = nc == 8 && (cols & 7) == 0;
         float col[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-        float rowp[32];
+        float my_row = 0.f;   // the sum of row r0 + lane over this segment
+        // interior strip (warp-uniform): all 32 rows in range, the segment's
+        // 256 columns inside the matrix, every element inside [fbase, fend)
+        const bool interior = (cols & 7) == 0 && seg * kSegCols + kSegCols <= cols && r0 + 32 <= cov &&
+                              (r_first + r0) * cols + seg * kSegCols >= fbase &&
+                              (r_first + r0 + 31) * cols + (seg + 1) * kSegCols <= fend;
+        if (interior) {
+            // 4 batches of 8 independent 16-byte loads per lane; each row's sum
+            // over the 32 lanes by an xor butterfly (offsets 16, 8, 4, 2, 1),
+            // kept by lane (row - r0)
+            const uint16_t* g0 = d.grad + ((r_first + r0) * cols + c0 - fbase);
+#pragma unroll 1
+            for (int b = 0; b < 4; ++b) {
+                uint4 w[8];
 #pragma unroll
-        for (int i = 0; i < 32; ++i) {
-            const int64_t r = r0 + i;
-            float sq[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-            if (r < cov && nc > 0) {
-                const int64_t ge = (r_first + r) * cols + c0;   // matrix index of the lane's first column
-                const uint16_t* g = d.grad + (ge - fbase);
-                if (vec) {
-                    // fbase and cols are multiples of 8: a run of 8 lies wholly inside or outside
-                    if (ge >= fbase && ge < fend) {
-                        const uint4 w = __ldcs(reinterpret_cast<const uint4*>(g));
-                        const uint32_t h[4] = {w.x, w.y, w.z, w.w};
+                for (int i = 0; i < 8; ++i)
+                    w[i] = __ldcs(reinterpret_cast<const uint4*>(g0 + (int64_t)(8 * b + i) * cols));
 #pragma unroll
-                        for (int k = 0; k < 4; ++k) {
-                            const float lo = __fmul_rn(bf16f(h[k] & 0xffffu), clip);
-                            const float hi = __fmul_rn(bf16f(h[k] >> 16), clip);
-                            sq[2 * k] = __fmul_rn(lo, lo);
-                            sq[2 * k + 1] = __fmul_rn(hi, hi);
-                        }
+                for (int i = 0; i < 8; ++i) {
+                    const uint32_t h[4] = {w[i].x, w[i].y, w[i].z, w[i].w};
+                    float sq[8];
+#pragma unroll
+                    for (int k = 0; k < 4; ++k) {
+                        const float lo = __fmul_rn(bf16f(h[k] & 0xffffu), clip);
+                        const float hi = __fmul_rn(bf16f(h[k] >> 16), clip);
+                        sq[2 * k] = __fmul_rn(lo, lo);
+                        sq[2 * k + 1] = __fmul_rn(hi, hi);
                     }
-                } else {
 #pragma unroll
-                    for (int k = 0; k < 8; ++k) {
-                        if (k < nc && ge + k >= fbase && ge + k < fend) {
-                            const float x = __fmul_rn(bf16f(g[k]), clip);
-                            sq[k] = __fmul_rn(x, x);
+                    for (int k = 0; k < 8; ++k) col[k] = __fadd_rn(col[k], sq[k]);
+                    float rs = __fadd_rn(__fadd_rn(__fadd_rn(sq[0], sq[1]), __fadd_rn(sq[2], sq[3])),
+                                         __fadd_rn(__fadd_rn(sq[4], sq[5]), __fadd_rn(sq[6], sq[7])));
+#pragma unroll
+                    for (int o = 16; o >= 1; o >>= 1) rs = __fadd_rn(rs, __shfl_xor_sync(0xffffffffu, rs, o));
+                    if (lane == 8 * b + i) my_row = rs;
+                }
+            }
+        } else {
+            float rowp[32];
+    #pragma unroll
+            for (int i = 0; i < 32; ++i) {
+                const int64_t r = r0 + i;
+                float sq[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+                if (r < cov && nc > 0) {
+                    const int64_t ge = (r_first + r) * cols + c0;   // matrix index of the lane's first column
+                    const uint16_t* g = d.grad + (ge - fbase);
+                    if (vec) {
+                        // fbase and cols are multiples of 8: a run of 8 lies wholly inside or outside
+                        if (ge >= fbase && ge < fend) {
+                            const uint4 w = __ldcs(reinterpret_cast<const uint4*>(g));
+                            const uint32_t h[4] = {w.x, w.y, w.z, w.w};
+    #pragma unroll
+                            for (int k = 0; k < 4; ++k) {
+                                const float lo = __fmul_rn(bf16f(h[k] & 0xffffu), clip);
+                                const float hi = __fmul_rn(bf16f(h[k] >> 16), clip);
+                                sq[2 * k] = __fmul_rn(lo, lo);
+                                sq[2 * k + 1] = __fmul_rn(hi, hi);
+                            }
+                        }
+                    } else {
+    #pragma unroll
+                        for (int k = 0; k < 8; ++k) {
+                            if (k < nc && ge + k >= fbase && ge + k < fend) {
+                                const float x = __fmul_rn(bf16f(g[k]), clip);
+                                sq[k] = __fmul_rn(x, x);
+                            }
                         }
                     }
                 }
+    #pragma unroll
+                for (int k = 0; k < 8; ++k) col[k] = __fadd_rn(col[k], sq[k]);
+                rowp[i] = __fadd_rn(__fadd_rn(__fadd_rn(sq[0], sq[1]), __fadd_rn(sq[2], sq[3])),
+                                    __fadd_rn(__fadd_rn(sq[4], sq[5]), __fadd_rn(sq[6], sq[7])));
             }
-#pragma unroll
-            for (int k = 0; k < 8; ++k) col[k] = __fadd_rn(col[k], sq[k]);
-            rowp[i] = __fadd_rn(__fadd_rn(__fadd_rn(sq[0], sq[1]), __fadd_rn(sq[2], sq[3])),
-                                __fadd_rn(__fadd_rn(sq[4], sq[5]), __fadd_rn(sq[6], sq[7])));
-        }
-        // transpose reduction: afterwards rowp[0] of lane l is the sum over the
-        // 32 lanes of row l (a fixed tree)
-#pragma unroll
-        for (int o = 16; o >= 1; o >>= 1) {
-            const bool upper = (lane & o) != 0;
-#pragma unroll
-            for (int i = 0; i < o; ++i) {
-                const float send = upper ? rowp[i] : rowp[i + o];
-                const float keep = upper ? rowp[i + o] : rowp[i];
-                rowp[i] = __fadd_rn(keep, __shfl_xor_sync(0xffffffffu, send, o));
+            // transpose reduction: afterwards rowp[0] of lane l is the sum over the
+            // 32 lanes of row l (a fixed tree)
+    #pragma unroll
+            for (int o = 16; o >= 1; o >>= 1) {
+                const bool upper = (lane & o) != 0;
+    #pragma unroll
+                for (int i = 0; i < o; ++i) {
+                    const float send = upper ? rowp[i] : rowp[i + o];
+                    const float keep = upper ? rowp[i + o] : rowp[i];
+                    rowp[i] = __fadd_rn(keep, __shfl_xor_sync(0xffffffffu, send, o));
+                }
             }
+            my_row = rowp[0];
         }
         const int64_t nslab = (cov + kSlabRows - 1) / kSlabRows;
-        if (r0 + lane < cov) d.colpart[nslab * cols + (r0 + lane) * nseg + seg] = rowp[0];
+        if (r0 + lane < cov) d.colpart[nslab * cols + (r0 + lane) * nseg + seg] = my_row;
 #pragma unroll
         for (int k = 0; k < 8; ++k) colsum[warp][lane * 8 + k] = col[k];
         __syncthreads();
@@ -216,11 +260,14 @@ __global__ void __launch_bounds__(kColWarps * 32) cols_kernel(const __grid_const
     }
 }
 
-__global__ void __launch_bounds__(256) rbar_kernel(const __grid_constant__ FactoredParams P) {
-    __shared__ float red[256];
+// mean(R) of each factored tensor by one CTA of kRbarThreads threads (the
+// fixed order of block_mean), with its correctly rounded reciprocal.
+constexpr int kRbarThreads = 1024;
+__global__ void __launch_bounds__(kRbarThreads) rbar_kernel(const __grid_constant__ FactoredParams P) {
+    __shared__ float red[kRbarThreads];
     for (int k = blockIdx.x; k < P.n_factored; k += gridDim.x) {
         const DevTensor& d = P.tensors[__ldg(P.factored_ids + k)];
-        const float mean = block_mean(d.vrow, d.rows, red);
+        const float mean = block_mean<kRbarThreads>(d.vrow, d.rows, red);
         if (threadIdx.x == 0) *reinterpret_cast<float2*>(d.rbar) = make_float2(mean, __frcp_rn(mean));
     }
 }
@@ -259,7 +306,7 @@ int launch_factored(const FactoredParams& p, void* stream) {
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     launch_stats(p, s);
     launch_rows_cols<ROWS_FINALIZE>(p, s);
-    rbar_kernel<<<p.n_factored < 1024 ? p.n_factored : 1024, 256, 0, s>>>(p);
+    rbar_kernel<<<p.n_factored < 1024 ? p.n_factored : 1024, kRbarThreads, 0, s>>>(p);
     return (int)cudaGetLastError();
 }
 
@@ -275,7 +322,7 @@ int launch_factored_from_sums(const FactoredParams& p, void* stream) {
     if (p.n_factored == 0) return 0;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     launch_rows_cols<ROWS_FROM_SUMS>(p, s);
-    rbar_kernel<<<p.n_factored < 1024 ? p.n_factored : 1024, 256, 0, s>>>(p);
+    rbar_kernel<<<p.n_factored < 1024 ? p.n_factored : 1024, kRbarThreads, 0, s>>>(p);
     return (int)cudaGetLastError();
 }
 

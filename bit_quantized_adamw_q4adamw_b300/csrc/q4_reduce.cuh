@@ -30,16 +30,18 @@ __device__ __forceinline__ float clip_factor(const float* sqnorm, float max_norm
     return c >= 1.f ? 1.f : c;
 }
 
-// Mean of R[0..rows) by one CTA of exactly 256 threads in a fixed order:
-// thread t sums R[t], R[t+256], ... left to right, then a binary tree over the
-// 256 partials; the sum is divided by rows.  Every CTA that calls it on the
-// same R gets the same bits.  All 256 threads must call it.
+// Mean of R[0..rows) by one CTA of exactly NT threads (a power of two) in a
+// fixed order: thread t sums R[t], R[t+NT], ... left to right, then a binary
+// tree over the NT partials; the sum is divided by rows.  Every CTA that
+// calls it with the same NT on the same R gets the same bits.  All NT threads
+// must call it; red holds NT floats.
+template <int NT = 256>
 __device__ __forceinline__ float block_mean(const float* R, int64_t rows, float* red) {
     float acc = 0.f;
-    for (int64_t i = threadIdx.x; i < rows; i += 256) acc = __fadd_rn(acc, R[i]);
+    for (int64_t i = threadIdx.x; i < rows; i += NT) acc = __fadd_rn(acc, R[i]);
     red[threadIdx.x] = acc;
     __syncthreads();
-    for (int o = 128; o > 0; o >>= 1) {
+    for (int o = NT / 2; o > 0; o >>= 1) {
         if (threadIdx.x < o) red[threadIdx.x] = __fadd_rn(red[threadIdx.x], red[threadIdx.x + o]);
         __syncthreads();
     }
