@@ -151,7 +151,7 @@ Layout make_layout(const q4adamw_tensor_t* t, int n, int recipe, const int64_t* 
     L.desc2 = off; off = round_up(off + (int64_t)n * (int64_t)sizeof(DevTensor), 256);
     L.pairs2 = off; off = round_up(off + (int64_t)(n + 2) * 8, 256);
     L.upload_bytes = off;
-    L.rbar = off;  off = round_up(off + (int64_t)(n > 0 ? n : 1) * 8, 256);   // {mean(R), 1/mean(R)}
+    L.rbar = off;  off = round_up(off + (int64_t)(n > 0 ? n : 1) * 16, 256);   // {mean(R), 1/mean(R), fast, 0}
     L.colpart = off;
     int64_t cp = 0;
     for (int i = 0; i < n; ++i) {
@@ -427,7 +427,7 @@ Image build_image(const q4adamw_tensor_t* t, int n, int recipe, uint32_t flags, 
         cols[i + 1] = cols[i] + (g.fact ? g.cols : 0);
         tiles[i + 1] = tiles[i] + (g.fact ? g.tiles : 0);
         if (g.fact) {
-            desc[i].rbar = reinterpret_cast<float*>(ws + L.rbar) + 2 * im.nf;
+            desc[i].rbar = reinterpret_cast<float*>(ws + L.rbar) + 4 * im.nf;
             desc[i].colpart = reinterpret_cast<float*>(ws + colpart_off);
             colpart_off += g.partials * 4;
             fids[im.nf++] = i;

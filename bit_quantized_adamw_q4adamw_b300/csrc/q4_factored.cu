@@ -40,6 +40,16 @@
 #include "q4_reduce.cuh"
 
 namespace q4 {
+namespace {
+// x >= 0 lies in {0} or [2^-100, 2^100]: the quotient's safe range.
+__device__ __forceinline__ bool quot_range_ok(float x) {
+    const uint32_t b = __float_as_uint(x);
+    return b == 0u || (b - 0x0d800000u) <= (0x71800000u - 0x0d800000u);
+}
+}  // namespace
+}  // namespace q4
+
+namespace q4 {
 
 namespace {
 
@@ -261,14 +271,57 @@ __global__ void __launch_bounds__(kColWarps * 32) cols_kernel(const __grid_const
 }
 
 // mean(R) of each factored tensor by one CTA of kRbarThreads threads (the
-// fixed order of block_mean), with its correctly rounded reciprocal.
+// fixed order of block_mean), with its correctly rounded reciprocal, and
+// whether every quotient R_i C_j / mean(R) of the tensor is in the range
+// where the step's reciprocal-based quotient is exact: from the largest and
+// the smallest nonzero R_i and C_j (on the bit patterns of these non-negative
+// floats: NaN and +inf above every finite value), every nonzero product and
+// quotient lies between the rounded products and quotients of the extremes
+// (rounding is monotone), which must lie in [2^-100, 2^100] (the quotients
+// with a factor-2 margin).  Stored as {mean, 1/mean, 1 or 0, 0}.
 constexpr int kRbarThreads = 1024;
+__device__ __forceinline__ void minmax_bits(const float* x, int64_t n, uint32_t& mx, uint32_t& mn_m1, uint32_t* red) {
+    uint32_t a = 0u, b = 0xffffffffu;
+    for (int64_t i = threadIdx.x; i < n; i += kRbarThreads) {
+        const uint32_t u = __float_as_uint(x[i]);
+        a = max(a, u);
+        b = min(b, u - 1u);   // the smallest nonzero, minus 1 (all ones: none)
+    }
+    a = __reduce_max_sync(0xffffffffu, a);
+    b = __reduce_min_sync(0xffffffffu, b);
+    if ((threadIdx.x & 31) == 0) { red[2 * (threadIdx.x >> 5)] = a; red[2 * (threadIdx.x >> 5) + 1] = b; }
+    __syncthreads();
+    if (threadIdx.x < 32) {
+        a = red[2 * threadIdx.x];
+        b = red[2 * threadIdx.x + 1];
+        a = __reduce_max_sync(0xffffffffu, a);
+        b = __reduce_min_sync(0xffffffffu, b);
+    }
+    mx = a;
+    mn_m1 = b;
+    __syncthreads();
+}
 __global__ void __launch_bounds__(kRbarThreads) rbar_kernel(const __grid_constant__ FactoredParams P) {
     __shared__ float red[kRbarThreads];
+    __shared__ uint32_t redu[64];
     for (int k = blockIdx.x; k < P.n_factored; k += gridDim.x) {
         const DevTensor& d = P.tensors[__ldg(P.factored_ids + k)];
         const float mean = block_mean<kRbarThreads>(d.vrow, d.rows, red);
-        if (threadIdx.x == 0) *reinterpret_cast<float2*>(d.rbar) = make_float2(mean, __frcp_rn(mean));
+        uint32_t rmax, rmin_m1, cmax, cmin_m1;
+        minmax_bits(d.vrow, d.rows, rmax, rmin_m1, redu);
+        minmax_bits(d.vcol, d.cols, cmax, cmin_m1, redu);
+        if (threadIdx.x == 0) {
+            const float y = __frcp_rn(mean);
+            const bool rb_ok = mean != 0.f && quot_range_ok(mean);
+            bool fast = rb_ok;
+            if (rb_ok && rmin_m1 != 0xffffffffu && cmin_m1 != 0xffffffffu) {
+                const float pmax = __fmul_rn(__uint_as_float(rmax), __uint_as_float(cmax));
+                const float pmin = __fmul_rn(__uint_as_float(rmin_m1 + 1u), __uint_as_float(cmin_m1 + 1u));
+                fast = quot_range_ok(pmax) && quot_range_ok(pmin) && pmin != 0.f &&
+                       __fdiv_rn(pmin, mean) >= 0x1p-99f && __fdiv_rn(pmax, mean) <= 0x1p99f;
+            }
+            *reinterpret_cast<float4*>(d.rbar) = make_float4(mean, y, fast ? 1.f : 0.f, 0.f);
+        }
     }
 }
 

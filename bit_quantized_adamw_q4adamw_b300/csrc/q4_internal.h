@@ -37,7 +37,8 @@ struct DevTensor {
     uint64_t elem_offset;
     uint32_t tensor_id;
     uint32_t flags;        // DF_* bits
-    float* rbar;           // factored: {mean(R), RN(1/mean(R))} of this step
+    float* rbar;           // factored: {mean(R), RN(1/mean(R)), 1 when every quotient
+                           // R_i C_j / mean(R) is in the fast quotient's exact range, 0}
     float* colpart;        // factored: column partial sums [n_slabs][cols], then
                            // row partial sums [cov_rows][n_segs] (the rows the
                            // tensor's elements touch, 256-row slabs from the first)

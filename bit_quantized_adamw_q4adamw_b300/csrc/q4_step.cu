@@ -780,6 +780,7 @@ __device__ __forceinline__ void compute_tile_full(const StepParams& P, const Dev
     float f_ri = 0.f;
     float4 f_c0 = make_float4(0.f, 0.f, 0.f, 0.f), f_c1 = f_c0;
     float2 f_rb = make_float2(0.f, 0.f);
+    bool f_fast = false;   // every quotient of the tensor in the fast quotient's exact range
     if (is_factored_recipe(RECIPE) && fvec) {
         const uint32_t cols = (uint32_t)d.cols;
         uint32_t col = f_col + (uint32_t)(half * kBlock + j * 8), row = f_row;
@@ -787,7 +788,9 @@ __device__ __forceinline__ void compute_tile_full(const StepParams& P, const Dev
         f_ri = __ldg(d.vrow + row);
         f_c0 = __ldg(reinterpret_cast<const float4*>(d.vcol + col));
         f_c1 = __ldg(reinterpret_cast<const float4*>(d.vcol + col + 4));
-        f_rb = *reinterpret_cast<const float2*>(d.rbar);
+        const float4 rb4 = *reinterpret_cast<const float4*>(d.rbar);
+        f_rb = make_float2(rb4.x, rb4.y);
+        f_fast = rb4.z != 0.f;
     }
 
     // ---- loads from the stage ---------------------------------------------
@@ -834,8 +837,20 @@ __device__ __forceinline__ void compute_tile_full(const StepParams& P, const Dev
                                    lds_f32(__byte_perm(vhi, tb, 0x7650 + k)));
         } else {
             float vf[8];
-            if (fvec) factored_vhat_pre(f_ri, f_c0, f_c1, f_rb, vf);
-            else factored_vhat(d, e0, 8, vf);
+            if (fvec && f_fast) {
+                const float C[8] = {f_c0.x, f_c0.y, f_c0.z, f_c0.w, f_c1.x, f_c1.y, f_c1.z, f_c1.w};
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                    const float2 p = mul2_rn(make_float2(f_ri, f_ri), make_float2(C[2 * k], C[2 * k + 1]));
+                    const float2 q = div2_rn_by_rcp(p, f_rb.x, f_rb.y);
+                    vf[2 * k] = q.x;
+                    vf[2 * k + 1] = q.y;
+                }
+            } else if (fvec) {
+                factored_vhat_pre(f_ri, f_c0, f_c1, f_rb, vf);
+            } else {
+                factored_vhat(d, e0, 8, vf);
+            }
 #pragma unroll
             for (int k = 0; k < 4; ++k) {
                 v[k] = make_float2(0.f, 0.f);
