@@ -235,8 +235,9 @@ def algorithmic_bytes(st, recipe) -> float:
 def launches_per_step(st, clip: bool = False, flags: int = 0) -> int:
     # step kernel: two launches when one instantiation does not suit every
     # tensor (a factored list with packed 1-D tensors; ZIP-SR / ZE-EDEN with
-    # stochastic m rounding on some tensors only); factored statistics (3
-    # kernels); clipping's sum of squares (3)
+    # stochastic m rounding on some tensors only); factored statistics (4
+    # kernels: the pass over g, rows, columns, mean(R)); clipping's sum of
+    # squares (3)
     live = [s for s in st.slots if s.numel > 0]
     fact = [st.is_factored(s) for s in live]
     if st.recipe in ("zip_sr", "ze_eden"):
@@ -244,7 +245,7 @@ def launches_per_step(st, clip: bool = False, flags: int = 0) -> int:
     else:
         msr = [False]
     split = (any(fact) and not all(fact)) or (any(msr) and not all(msr))
-    return (2 if split else 1) + (3 if any(fact) else 0) + (3 if clip else 0)
+    return (2 if split else 1) + (4 if any(fact) else 0) + (3 if clip else 0)
 
 
 def time_sqnorm(st, stream, iters: int) -> float:

@@ -26,9 +26,9 @@ def test_launches_per_step():
     tao = FakeState("torchao", [(4096, 1, 0), (256 * 8, 256, LM)])
     assert bench.launches_per_step(tao, flags=0x1) == 1               # TorchAO keeps RTN on the head
     fac = FakeState("factored", [(1024 * 64, 64, FACT), (1024, 1, 0)])
-    assert bench.launches_per_step(fac) == 1 + 1 + 3                  # two step launches + statistics
+    assert bench.launches_per_step(fac) == 1 + 1 + 4                  # two step launches + statistics
     fac_only = FakeState("factored", [(1024 * 64, 64, FACT)])
-    assert bench.launches_per_step(fac_only) == 1 + 3
+    assert bench.launches_per_step(fac_only) == 1 + 4
 
 
 def test_strip_comments_keeps_code_and_literals():
