@@ -24,7 +24,8 @@ from ._native import (BLOCK, Q4_LM_HEAD_SR_ACTIVE, Q4_M_SR_ALL, Q4_T_FACTORED, Q
 __all__ = ["q4adamw_version", "q4adamw_strerror", "q4adamw_state_bytes", "q4adamw_workspace_bytes",
            "q4adamw_state_init", "q4adamw_header_check", "q4adamw_step", "q4adamw_step_noalloc",
            "q4adamw_dequant_state", "q4adamw_step_status", "q4adamw_grad_sqnorm", "q4adamw_step_clip", "q4adamw_draws",
-           "q4adamw_codebook", "q4adamw_set_stage_wait_limit", "q4adamw_step_noalloc_status", "Q4State", "Q4Tensor", "Q4Header", "Q4Error", "RECIPES", "Q4_T_LM_HEAD",
+           "q4adamw_codebook", "q4adamw_set_stage_wait_limit", "q4adamw_step_noalloc_status",
+           "q4adamw_grad_nonfinite", "Q4State", "Q4Tensor", "Q4Header", "Q4Error", "RECIPES", "Q4_T_LM_HEAD",
            "Q4_T_FACTORED", "Q4_LM_HEAD_SR_ACTIVE", "Q4_M_SR_ALL", "Q4_V_UPDATE_RTN", "Q4_V_NEXT_R", "BLOCK"]
 
 
@@ -134,6 +135,16 @@ def q4adamw_step_noalloc(tensors, lr, beta1, beta2, eps, weight_decay, step, see
     _check(lib().q4adamw_step_noalloc(arr, n, lr, beta1, beta2, eps, weight_decay, int(step),
                                       int(seed) & (2 ** 64 - 1), _recipe(recipe), int(flags), _stream(stream)),
            "q4adamw_step_noalloc")
+
+
+def q4adamw_grad_nonfinite(tensors, out: torch.Tensor, workspace: torch.Tensor, stream=None) -> None:
+    """Number of NaN / +-inf BF16 gradients of the list into out (a device int64
+    tensor of one element)."""
+    assert out.is_cuda and out.element_size() == 8 and out.numel() >= 1
+    arr, n = _array(tensors)
+    _check(lib().q4adamw_grad_nonfinite(arr, n, ctypes.c_void_p(out.data_ptr()), ctypes.c_void_p(workspace.data_ptr()),
+                                        workspace.numel() * workspace.element_size(), _stream(stream)),
+           "q4adamw_grad_nonfinite")
 
 
 def q4adamw_step_noalloc_status(stream=None) -> int:

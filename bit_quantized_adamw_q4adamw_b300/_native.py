@@ -68,7 +68,7 @@ EXPORTS = ("q4adamw_version", "q4adamw_strerror", "q4adamw_last_cuda_error", "q4
            "q4adamw_grad_sqnorm", "q4adamw_step_clip", "q4adamw_draws", "q4adamw_set_stage_wait_limit",
            "q4adamw_step_noalloc_status", "q4adamw_dp_state_init", "q4adamw_dp_sums_floats",
            "q4adamw_dp_workspace_bytes",
-           "q4adamw_dp_factored_sums", "q4adamw_dp_step")
+           "q4adamw_dp_factored_sums", "q4adamw_dp_step", "q4adamw_grad_nonfinite")
 
 
 def lib():
@@ -106,12 +106,14 @@ def lib():
     L.q4adamw_dp_workspace_bytes.argtypes = [TP, I, I, P, P]
     L.q4adamw_dp_factored_sums.argtypes = [TP, I, I, P, F, P, P, P, I64, P]
     L.q4adamw_dp_step.argtypes = [TP, I, F, F, F, F, F, I64, U64, I, U32, P, P, F, P, P, I64, P]
+    L.q4adamw_grad_nonfinite.argtypes = [TP, I, P, P, I64, P]
     for name in ("q4adamw_state_bytes", "q4adamw_workspace_bytes", "q4adamw_state_init", "q4adamw_header_check",
                  "q4adamw_step", "q4adamw_dequant_state", "q4adamw_codebook", "q4adamw_step_noalloc",
                  "q4adamw_step_status", "q4adamw_grad_sqnorm", "q4adamw_step_clip", "q4adamw_draws",
                  "q4adamw_set_stage_wait_limit", "q4adamw_step_noalloc_status", "q4adamw_dp_state_init",
                  "q4adamw_dp_sums_floats",
-                 "q4adamw_dp_workspace_bytes", "q4adamw_dp_factored_sums", "q4adamw_dp_step"):
+                 "q4adamw_dp_workspace_bytes", "q4adamw_dp_factored_sums", "q4adamw_dp_step",
+                 "q4adamw_grad_nonfinite"):
         getattr(L, name).restype = I
     _lib = L
     return L

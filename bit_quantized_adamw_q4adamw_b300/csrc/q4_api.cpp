@@ -749,6 +749,44 @@ int q4adamw_grad_sqnorm(const q4adamw_tensor_t* t, int n, float* sqnorm, void* w
     return Q4_OK;
 }
 
+int q4adamw_grad_nonfinite(const q4adamw_tensor_t* t, int n, uint64_t* count, void* workspace,
+                           int64_t workspace_bytes, void* stream) {
+    if (n < 0 || (n > 0 && !t) || !count) return Q4_EINVAL;
+    if (!aligned(count, 8)) return Q4_EALIGN;
+    for (int i = 0; i < n; ++i) {
+        if (t[i].numel < 0) return Q4_ESHAPE;
+        if (t[i].numel > 0 && !t[i].grad) return Q4_EINVAL;
+        if (t[i].grad && !aligned(t[i].grad, 16)) return Q4_EALIGN;
+    }
+    // the upload (descriptors and run prefixes) fits the gradient-norm layout
+    const NormLayout L = make_norm_layout(t, n);
+    if (!workspace || !aligned(workspace, 256) || workspace_bytes < L.total) return Q4_EWORKSPACE;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    thread_local std::vector<unsigned char> img;
+    img.assign((size_t)L.upload_bytes, 0);
+    q4::NormTensor* desc = reinterpret_cast<q4::NormTensor*>(img.data() + L.desc);
+    int64_t* prefix = reinterpret_cast<int64_t*>(img.data() + L.prefix);
+    prefix[0] = 0;
+    for (int i = 0; i < n; ++i) {
+        desc[i].grad = t[i].grad;
+        desc[i].numel = t[i].numel;
+        prefix[i + 1] = prefix[i] + (t[i].numel + 7) / 8;
+    }
+    cudaError_t e = cudaMemcpyAsync(workspace, img.data(), (size_t)L.upload_bytes, cudaMemcpyHostToDevice, s);
+    if (e != cudaSuccess) return cuda_fail(e);
+    char* ws = static_cast<char*>(workspace);
+    q4::NonfiniteParams p{};
+    p.tensors = reinterpret_cast<const q4::NormTensor*>(ws + L.desc);
+    p.run_prefix = reinterpret_cast<const int64_t*>(ws + L.prefix);
+    p.n_tensors = n;
+    p.total_runs = prefix[n];
+    p.out = reinterpret_cast<unsigned long long*>(count);
+    int dev = 0;
+    if ((e = cudaGetDevice(&dev)) != cudaSuccess) return cuda_fail(e);
+    if (int ce = q4::launch_nonfinite(p, dev, stream)) return cuda_fail((cudaError_t)ce);
+    return Q4_OK;
+}
+
 int q4adamw_set_stage_wait_limit(int64_t cycles) {
     if (cycles < 0) return Q4_EINVAL;
     g_wait_cycles = cycles == 0 ? q4::kDefaultWaitCycles : (long long)cycles;

@@ -151,6 +151,15 @@ struct NormParams {
     float* out;                   // the sum of squares
 };
 
+// Count of non-finite BF16 gradients: runs of 8 elements per tensor.
+struct NonfiniteParams {
+    const NormTensor* tensors;
+    const int64_t* run_prefix;    // n+1: runs of each tensor
+    int n_tensors;
+    int64_t total_runs;
+    unsigned long long* out;      // the count (zeroed by the launch)
+};
+
 // Kernel-internal recipe value: the factored recipe on a launch whose tensors
 // are all factored (rank >= 2), which compiles without the packed-v code.
 constexpr int kRecipeFactoredOnly = 16;
@@ -184,6 +193,7 @@ int launch_factored(const FactoredParams& p, void* stream);
 int launch_factored_sums(const FactoredParams& p, void* stream);
 int launch_factored_from_sums(const FactoredParams& p, void* stream);
 int launch_grad_sqnorm(const NormParams& p, int device, void* stream);
+int launch_nonfinite(const NonfiniteParams& p, int device, void* stream);
 int launch_draws(uint64_t seed, uint32_t step, uint32_t tensor_id, uint64_t idx0, uint32_t purpose, int64_t n,
                  uint32_t* out, void* stream);
 int launch_dequant(const DevTensor& d, int recipe, const float* nf4, const float* vl, float* m_out, float* v_out,

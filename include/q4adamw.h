@@ -311,6 +311,22 @@ int q4adamw_dp_step(const q4adamw_tensor_t* t, int n, float lr, float beta1, flo
                     void* workspace, int64_t workspace_bytes, void* stream);
 
 /*
+ * Optional check of the gradients (a counter the step itself does not keep, so
+ * that the step pays nothing for it): writes to *count (one device uint64, 8-B
+ * aligned, caller-owned) the number of BF16 gradient elements of t[0..n) that
+ * are NaN, +inf or -inf (exponent bits all ones).  One pass over the gradients
+ * (2 bytes per element).  Reads grad and numel of each tensor only (grad 16-B
+ * aligned, may be NULL when numel is 0).  workspace as for q4adamw_step
+ * (q4adamw_workspace_bytes covers this call; the calls must not overlap on
+ * it).  Asynchronous on stream.  The pages have no counterpart: a caller may
+ * use it to skip the step of a batch whose gradients overflowed.  Q4_EINVAL
+ * for NULL count or n < 0, Q4_EALIGN, Q4_ESHAPE, Q4_EWORKSPACE as for
+ * q4adamw_grad_sqnorm.
+ */
+int q4adamw_grad_nonfinite(const q4adamw_tensor_t* t, int n, uint64_t* count, void* workspace,
+                           int64_t workspace_bytes, void* stream);
+
+/*
  * The stochastic-rounding draws of the step, for checking and reproducing its
  * rounding: writes to out[0..n) (device, 4-B aligned) the 32-bit Philox4x32-10
  * words that q4adamw_step draws for elements idx0 .. idx0+n-1 (global element
