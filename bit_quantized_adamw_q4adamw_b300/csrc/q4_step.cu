@@ -104,6 +104,7 @@ struct __align__(256) SmemAll {
     WarpSmem w[kStepWarps];
     float2 nf4_bucket[64];  // NF4 RTN by linear bucket: {unscaled threshold of the candidate, candidate}
     float4 v_rtn[16];       // v RTN by candidate c: {unscaled threshold t_c, level L_c, level L_{c+1}, 0}
+    float v_thr[16];        // the thresholds t_c alone: 16 words in distinct banks
     float v_next[16];       // ZIP-SR cell search by candidate c: unscaled level L_{c+1}
     float vl[16];     // unscaled v levels (EDEN reconstruction)
     uint8_t lut_nf4_t[64];
@@ -772,26 +773,9 @@ __device__ __forceinline__ void compute_tile_full(const StepParams& P, const Dev
     const bool m_sr = (flags & DF_M_SR) != 0;
     const uint32_t tb = smem_addr(&wt);   // 256-byte aligned
 
-    // factored v (columns a multiple of 8, at least 256): R_i, the lane's 8
-    // C_j and mean(R) are loaded first, so that their latency overlaps the
-    // decoding; the tile starts at (f_row, f_col), the lane's 8 elements lie
-    // in one row
+    // factored v with columns a multiple of 8, at least 256: the tile starts at
+    // (f_row, f_col) and the lane's 8 elements lie in one row
     const bool fvec = fact && (flags & DF_CVEC);
-    float f_ri = 0.f;
-    float4 f_c0 = make_float4(0.f, 0.f, 0.f, 0.f), f_c1 = f_c0;
-    float2 f_rb = make_float2(0.f, 0.f);
-    bool f_fast = false;   // every quotient of the tensor in the fast quotient's exact range
-    if (is_factored_recipe(RECIPE) && fvec) {
-        const uint32_t cols = (uint32_t)d.cols;
-        uint32_t col = f_col + (uint32_t)(half * kBlock + j * 8), row = f_row;
-        if (col >= cols) { col -= cols; ++row; }
-        f_ri = __ldg(d.vrow + row);
-        f_c0 = __ldg(reinterpret_cast<const float4*>(d.vcol + col));
-        f_c1 = __ldg(reinterpret_cast<const float4*>(d.vcol + col + 4));
-        const float4 rb4 = *reinterpret_cast<const float4*>(d.rbar);
-        f_rb = make_float2(rb4.x, rb4.y);
-        f_fast = rb4.z != 0.f;
-    }
 
     // ---- loads from the stage ---------------------------------------------
     const float sm_old = st.ms[half];
@@ -837,6 +821,24 @@ __device__ __forceinline__ void compute_tile_full(const StepParams& P, const Dev
                                    lds_f32(__byte_perm(vhi, tb, 0x7650 + k)));
         } else {
             float vf[8];
+            // R_i, the lane's 8 C_j and mean(R), loaded where the quotient
+            // needs them (loads at the tile's start, for more overlap, measured
+            // slower: longer live ranges)
+            float f_ri = 0.f;
+            float4 f_c0 = make_float4(0.f, 0.f, 0.f, 0.f), f_c1 = f_c0;
+            float2 f_rb = make_float2(0.f, 0.f);
+            bool f_fast = false;   // every quotient of the tensor in the fast quotient's exact range
+            if (is_factored_recipe(RECIPE) && fvec) {
+                const uint32_t cols = (uint32_t)d.cols;
+                uint32_t col = f_col + (uint32_t)(half * kBlock + j * 8), row = f_row;
+                if (col >= cols) { col -= cols; ++row; }
+                f_ri = __ldg(d.vrow + row);
+                f_c0 = __ldg(reinterpret_cast<const float4*>(d.vcol + col));
+                f_c1 = __ldg(reinterpret_cast<const float4*>(d.vcol + col + 4));
+                const float4 rb4 = *reinterpret_cast<const float4*>(d.rbar);
+                f_rb = make_float2(rb4.x, rb4.y);
+                f_fast = rb4.z != 0.f;
+            }
             if (fvec && f_fast) {
                 const float C[8] = {f_c0.x, f_c0.y, f_c0.z, f_c0.w, f_c1.x, f_c1.y, f_c1.z, f_c1.w};
 #pragma unroll
@@ -1030,35 +1032,40 @@ __device__ __forceinline__ void compute_tile_full(const StepParams& P, const Dev
         } else {
             const uint32_t lut = smem_addr(sm.lut_v_t);
             const uint32_t vr_base = smem_addr(sm.v_rtn);
-            float ta[8], tb2[8];
+            const uint32_t vt_base = smem_addr(sm.v_thr);
+            const uint32_t vl_base = smem_addr(sm.vl);
+            // EDEN: each group of 4 consecutive elements (pairs 2h, 2h+1)
+            // summed left to right as its terms appear
+            float pa[2] = {0.f, 0.f}, pb[2] = {0.f, 0.f};
 #pragma unroll
             for (int k = 0; k < 4; ++k) {
                 const float2 y = mul2_rn(v1[k], make_float2(rho, rho));
                 const uint32_t c0 = lds_u8(lut + (__float_as_uint(y.x) >> 19));
                 const uint32_t c1 = lds_u8(lut + (__float_as_uint(y.y) >> 19));
-                // {t_c, L_c, L_{c+1}}; the threshold at the new scale is t_c * s_v
-                const float4 e0v = lds_f32x4(vr_base + c0 * 16u);
-                const float4 e1v = lds_f32x4(vr_base + c1 * 16u);
-                const float2 thr = mul2_rn(make_float2(e0v.x, e1v.x), sv2);
+                // the threshold at the new scale is t_c * s_v; TorchAO reads it from
+                // the {t_c, L_c, L_{c+1}} entry, ZE-EDEN from the 4-byte table (no
+                // bank conflicts) and then the level of the chosen code
+                float2 thr;
+                if (RECIPE == Q4_RECIPE_ZE_EDEN) {
+                    thr = make_float2(lds_f32(vt_base + c0 * 4u), lds_f32(vt_base + c1 * 4u));
+                } else {
+                    thr = make_float2(lds_f32x4(vr_base + c0 * 16u).x, lds_f32x4(vr_base + c1 * 16u).x);
+                }
+                thr = mul2_rn(thr, sv2);
                 const bool up0 = v1[k].x > thr.x, up1 = v1[k].y > thr.y;
                 c[2 * k] = c0 + (up0 ? 1u : 0u);
                 c[2 * k + 1] = c1 + (up1 ? 1u : 0u);
                 if (RECIPE == Q4_RECIPE_ZE_EDEN) {
-                    const float2 yh = make_float2(up0 ? e0v.z : e0v.y, up1 ? e1v.z : e1v.y);
+                    // scalar sums: the terms are paired products
+                    const float2 yh = make_float2(lds_f32(vl_base + c[2 * k] * 4u), lds_f32(vl_base + c[2 * k + 1] * 4u));
                     const float2 a2 = mul2_rn(y, y), b2 = mul2_rn(y, yh);
-                    ta[2 * k] = a2.x; ta[2 * k + 1] = a2.y;
-                    tb2[2 * k] = b2.x; tb2[2 * k + 1] = b2.y;
+                    const int h = k >> 1;
+                    pa[h] = (k & 1) ? __fadd_rn(__fadd_rn(pa[h], a2.x), a2.y) : __fadd_rn(a2.x, a2.y);
+                    pb[h] = (k & 1) ? __fadd_rn(__fadd_rn(pb[h], b2.x), b2.y) : __fadd_rn(b2.x, b2.y);
                 }
             }
             if (RECIPE == Q4_RECIPE_ZE_EDEN) {
-                // groups of 4 consecutive elements left to right, then the two groups
-                // (scalar sums: the terms are paired products)
-                float pa[2], pb[2];
-#pragma unroll
-                for (int h = 0; h < 2; ++h) {
-                    pa[h] = __fadd_rn(__fadd_rn(__fadd_rn(ta[4 * h], ta[4 * h + 1]), ta[4 * h + 2]), ta[4 * h + 3]);
-                    pb[h] = __fadd_rn(__fadd_rn(__fadd_rn(tb2[4 * h], tb2[4 * h + 1]), tb2[4 * h + 2]), tb2[4 * h + 3]);
-                }
+                // then the lane's two groups, then the butterfly over the lanes
                 float A = __fadd_rn(pa[0], pa[1]);
                 float B = __fadd_rn(pb[0], pb[1]);
 #pragma unroll
@@ -1066,7 +1073,10 @@ __device__ __forceinline__ void compute_tile_full(const StepParams& P, const Dev
                     A = __fadd_rn(A, __shfl_xor_sync(0xffffffffu, A, o));
                     B = __fadd_rn(B, __shfl_xor_sync(0xffffffffu, B, o));
                 }
-                sv_store = (B == 0.f) ? 0.f : __fmul_rn(s_v, __fdiv_rn(A, B));
+                // A and B lie in about [1, 128] here (the block's largest element
+                // has y = 1 within an ulp and code 15, level 1), inside the range
+                // where the reciprocal-based quotient is exact: no division call
+                sv_store = (B == 0.f) ? 0.f : __fmul_rn(s_v, div_rn_by_rcp(A, B, rcp_rn_normal<1>(B)));
             }
         }
         cv = pack8(c);
@@ -1100,6 +1110,7 @@ __global__ void __launch_bounds__(kStepThreads, 1) step_kernel(const __grid_cons
         const int c = threadIdx.x, c1 = c < 15 ? c + 1 : 15;
         sm.vl[c] = P.tab.vl[c];
         sm.v_rtn[c] = make_float4(P.tab.vt[c], P.tab.vl[c], P.tab.vl[c1], 0.f);
+        sm.v_thr[c] = P.tab.vt[c];
         sm.v_next[c] = P.tab.vl[c1];
     }
     for (int i = threadIdx.x; i < 64; i += blockDim.x) {

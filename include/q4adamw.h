@@ -388,8 +388,7 @@ int q4adamw_dequant_state(const q4adamw_tensor_t* t, int recipe, float* m_out, f
  *     Q4ADAMW_NOALLOC_SCRATCH_BYTES is rejected with Q4_EWORKSPACE before any
  *     device work.
  *   - The first call on a device looks up the array's device address on that
- *     device (cudaGetSymbolAddress); make that first call before any stream
- *     capture.  A failed lookup returns Q4_ECUDA.
+ *     device (cudaGetSymbolAddress).  A failed lookup returns Q4_ECUDA.
  *   - All calls share the one array and it keeps the previous call's contents;
  *     every byte a step reads from it is written earlier in the same step, so
  *     nothing needs clearing.  Calls whose GPU work overlaps (different streams
