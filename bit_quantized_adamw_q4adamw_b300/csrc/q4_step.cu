@@ -103,6 +103,7 @@ struct __align__(256) WarpSmem {
 struct __align__(256) SmemAll {
     WarpSmem w[kStepWarps];
     float2 nf4_bucket[64];  // NF4 RTN by linear bucket: {unscaled threshold of the candidate, candidate}
+    float nf4_thr[64];      // its thresholds alone (4-byte entries: buckets 0..32 in distinct banks)
     float4 v_rtn[16];       // v RTN by candidate c: {unscaled threshold t_c, level L_c, level L_{c+1}, 0}
     float v_thr[16];        // the thresholds t_c alone: 16 words in distinct banks
     float v_next[16];       // ZIP-SR cell search by candidate c: unscaled level L_{c+1}
@@ -907,16 +908,30 @@ __device__ __forceinline__ void compute_tile_full(const StepParams& P, const Dev
     if (nf4_rtn) {
         const float rho16 = __fmul_rn(16.f, rcp_rn_normal<1>(s_m));
         const uint32_t nb_base = smem_addr(sm.nf4_bucket);
+        const uint32_t nt_base = smem_addr(sm.nf4_thr), nc_base = smem_addr(sm.lut_nf4_t);
         const float2 sm2 = make_float2(s_m, s_m);
         uint32_t c[8];
 #pragma unroll
         for (int k = 0; k < 4; ++k) {
             const float2 z = fma2_rn(m1[k], make_float2(rho16, rho16), make_float2(kMagic + 16.f, kMagic + 16.f));
-            const float2 e0v = lds_f32x2(nb_base + (__float_as_uint(z.x) & 63u) * 8u);
-            const float2 e1v = lds_f32x2(nb_base + (__float_as_uint(z.y) & 63u) * 8u);
-            const float2 thr = mul2_rn(make_float2(e0v.x, e1v.x), sm2);
-            c[2 * k] = __float_as_uint(e0v.y) + (m1[k].x > thr.x ? 1u : 0u);
-            c[2 * k + 1] = __float_as_uint(e1v.y) + (m1[k].y > thr.y ? 1u : 0u);
+            const uint32_t b0 = __float_as_uint(z.x) & 63u, b1 = __float_as_uint(z.y) & 63u;
+            float2 thr;
+            uint32_t q0, q1;
+            if (RECIPE == Q4_RECIPE_ZE_EDEN) {
+                // two 4-byte reads, free of bank conflicts (measured faster here;
+                // one 8-byte read of {t_c, c} is faster for ZIP-SR)
+                thr = make_float2(lds_f32(nt_base + b0 * 4u), lds_f32(nt_base + b1 * 4u));
+                q0 = lds_u8(nc_base + b0);
+                q1 = lds_u8(nc_base + b1);
+            } else {
+                const float2 e0v = lds_f32x2(nb_base + b0 * 8u), e1v = lds_f32x2(nb_base + b1 * 8u);
+                thr = make_float2(e0v.x, e1v.x);
+                q0 = __float_as_uint(e0v.y);
+                q1 = __float_as_uint(e1v.y);
+            }
+            thr = mul2_rn(thr, sm2);
+            c[2 * k] = q0 + (m1[k].x > thr.x ? 1u : 0u);
+            c[2 * k + 1] = q1 + (m1[k].y > thr.y ? 1u : 0u);
         }
         cm = pack8(c);
     }
@@ -1117,6 +1132,7 @@ __global__ void __launch_bounds__(kStepThreads, 1) step_kernel(const __grid_cons
         sm.lut_nf4_t[i] = P.tab.lut_nf4_t[i];
         sm.lut_nf4_l[i] = P.tab.lut_nf4_l[i];
         sm.nf4_bucket[i] = P.tab.nf4_bucket[i];
+        sm.nf4_thr[i] = P.tab.nf4_bucket[i].x;
     }
     for (int i = threadIdx.x; i < kVLut / 4; i += blockDim.x) {
         reinterpret_cast<uint32_t*>(sm.lut_v_l)[i] = reinterpret_cast<const uint32_t*>(P.tab.lut_v_l)[i];
