@@ -163,25 +163,25 @@ def test_factored_wide_rows():
         assert r["rc"] == 0 and r["theta"] == 0 and r["bf16"] == 0, (t, r)
 
 
-def test_sharded_tensor_matches_whole():
-    # Two block-aligned shards with elem_offset produce the bits of the whole tensor.
+@pytest.mark.parametrize("recipe", ["zip_sr", "ze_eden", "torchao"])
+def test_sharded_tensor_matches_whole(recipe):
+    # Two block-aligned shards with elem_offset produce the bits of the whole
+    # tensor (the draws are keyed by the global element index; EDEN and the
+    # scales are block-local), LM-head SR included.
     n, cut = 128 * 9 + 31, 128 * 4
-    w = W.custom("shard", [(n,)], "zip_sr", flags=[W.T_LM_HEAD])
+    w = W.custom("shard", [(n,)], recipe, flags=[W.T_LM_HEAD])
     th = W.init_param(w.tensors[0], 0)
-    whole = Pair(w.tensors, "zip_sr", theta0=[th], tensor_ids=[4])
-    parts = W.custom("shard2", [(cut,), (n - cut,)], "zip_sr", flags=[W.T_LM_HEAD, W.T_LM_HEAD])
-    split = Pair(parts.tensors, "zip_sr", theta0=[th[:cut], th[cut:]], tensor_ids=[4, 4], elem_offsets=[0, cut])
+    whole = Pair(w.tensors, recipe, theta0=[th], tensor_ids=[4])
+    parts = W.custom("shard2", [(cut,), (n - cut,)], recipe, flags=[W.T_LM_HEAD, W.T_LM_HEAD])
+    split = Pair(parts.tensors, recipe, theta0=[th[:cut], th[cut:]], tensor_ids=[4, 4], elem_offsets=[0, cut])
     for t in range(1, 5):
         g = W.draw_grad(w, w.tensors[0], 0, t)
         whole.step(t, [g], seed=9, flags=1)
         split.step(t, [g[:cut], g[cut:]], seed=9, flags=1)
-        a = whole.gpu.view(0, "param").cpu()
-        b = torch.cat([split.gpu.view(0, "param").cpu(), split.gpu.view(1, "param").cpu()])
-        assert torch.equal(a, b)
-        assert torch.equal(whole.gpu.view(0, "m_codes").cpu(),
-                           torch.cat([split.gpu.view(0, "m_codes").cpu(), split.gpu.view(1, "m_codes").cpu()]))
-        assert torch.equal(whole.gpu.view(0, "v_codes").cpu(),
-                           torch.cat([split.gpu.view(0, "v_codes").cpu(), split.gpu.view(1, "v_codes").cpu()]))
+        for name in ("param", "param_bf16", "m_codes", "v_codes", "m_scale", "v_scale"):
+            a = whole.gpu.view(0, name).cpu()
+            b = torch.cat([split.gpu.view(0, name).cpu(), split.gpu.view(1, name).cpu()])
+            assert torch.equal(a.view(torch.uint8), b.view(torch.uint8)), (recipe, t, name)
 
 
 @pytest.mark.parametrize("recipe", ["zip_sr", "ze_eden", "factored", "torchao"])
