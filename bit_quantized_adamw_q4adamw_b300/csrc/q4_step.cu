@@ -882,7 +882,7 @@ __device__ __forceinline__ void compute_tile_full(const StepParams& P, const Dev
     const float s_m = half_max(amax, half);
     const float s_v = fact ? 0.f : half_max(vmax_lane, half);
 
-    const bool fast = !URTN && __all_sync(0xffffffffu, (MSR || !m_sr) && scale_in_fast_range(s_m) &&
+    const bool fast = __all_sync(0xffffffffu, (MSR || !m_sr) && scale_in_fast_range(s_m) &&
                                                           (fact || scale_in_fast_range(s_v)));
     if (!fast) {
         float m1s[8], v1s[8], rs[8];
@@ -952,12 +952,13 @@ __device__ __forceinline__ void compute_tile_full(const StepParams& P, const Dev
     if (RECIPE == Q4_RECIPE_ZIP_SR && !fact) {
         // a_k = level k at the new scale, r_k its preconditioner, d_k =
         // (r_k - r_{k+1}) 2^-24: after the cell search (from the constant
-        // levels) the SR decision reads (r_k, d_k) by cell.
+        // levels) the SR decision reads (r_k, d_k) by cell; Update-RTN reads
+        // (r_k, r_{k+1}) instead (r_15 twice: cell 15 keeps code 15).
         const float a = __fmul_rn(my_vl, s_v);
         const float rk = P.fast_math ? precond<true>(P, a) : precond<false>(P, a);
         const float rk1 = __shfl_down_sync(0xffffffffu, rk, 1);
-        const float dk = j < 15 ? __fmul_rn(__fsub_rn(rk, rk1), kTwoM24) : 0.f;
-        wt.rdv[half][j] = make_float2(rk, dk);  // (r_k, d_k) by cell
+        const float dk = URTN ? (j < 15 ? rk1 : rk) : j < 15 ? __fmul_rn(__fsub_rn(rk, rk1), kTwoM24) : 0.f;
+        wt.rdv[half][j] = make_float2(rk, dk);
     }
     // the v RTN codes (ZE-EDEN, TorchAO, factored 1-D) and the NF4 RTN m codes
     // read constant tables only: no per-block table to wait for
@@ -1023,7 +1024,7 @@ __device__ __forceinline__ void compute_tile_full(const StepParams& P, const Dev
             const uint32_t lut = smem_addr(sm.lut_v_l);
             const uint32_t vn_base = smem_addr(sm.v_next);
             uint32_t w[8];
-            draws8(d.elem_offset + (uint64_t)e0, 1u, d.tensor_id, P.step, P.round_keys, w);
+            if (!URTN) draws8(d.elem_offset + (uint64_t)e0, 1u, d.tensor_id, P.step, P.round_keys, w);
 #pragma unroll
             for (int k = 0; k < 4; ++k) {
                 const float2 y = mul2_rn(v1[k], make_float2(rho, rho));
@@ -1038,11 +1039,18 @@ __device__ __forceinline__ void compute_tile_full(const StepParams& P, const Dev
                 const float2 e1v = lds_f32x2(rd_base + k1 * 8u);
                 const float2 rk = make_float2(e0v.x, e1v.x);
                 const float2 dk = make_float2(e0v.y, e1v.y);
-                // u (r_k - r_{k+1}) with u = (w >> 8) 2^-24, as (w >> 8) ((r_k - r_{k+1}) 2^-24)
-                const float2 t = mul2_rn(make_float2((float)(w[2 * k] >> 8), (float)(w[2 * k + 1] >> 8)), dk);
                 const float2 gap = add2_rn(rk, neg2(r[k]));
-                c[2 * k] = k0 + (t.x < gap.x ? 1u : 0u);
-                c[2 * k + 1] = k1 + (t.y < gap.y ? 1u : 0u);
+                if (URTN) {
+                    // Update-RTN: up when r - r_{k+1} < r_k - r (a tie keeps k)
+                    const float2 below = add2_rn(r[k], neg2(dk));
+                    c[2 * k] = k0 + (below.x < gap.x ? 1u : 0u);
+                    c[2 * k + 1] = k1 + (below.y < gap.y ? 1u : 0u);
+                } else {
+                    // u (r_k - r_{k+1}) with u = (w >> 8) 2^-24, as (w >> 8) ((r_k - r_{k+1}) 2^-24)
+                    const float2 t = mul2_rn(make_float2((float)(w[2 * k] >> 8), (float)(w[2 * k + 1] >> 8)), dk);
+                    c[2 * k] = k0 + (t.x < gap.x ? 1u : 0u);
+                    c[2 * k + 1] = k1 + (t.y < gap.y ? 1u : 0u);
+                }
             }
         } else {
             const uint32_t lut = smem_addr(sm.lut_v_t);
