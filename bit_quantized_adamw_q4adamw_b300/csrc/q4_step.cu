@@ -97,6 +97,7 @@ struct __align__(256) WarpSmem {
     WarpTables wt;
     Stage st[kStageBufs][kTilesPerStage];   // stage buffers of kTilesPerStage tiles each
     DevTensor desc;                         // descriptor of the tensor being computed
+    float4 rbv;                             // factored: its {mean(R), 1/mean(R), fast flag, 0}
     unsigned long long bar[kStageBufs];     // one mbarrier per stage buffer
 };
 
@@ -765,7 +766,8 @@ __device__ __forceinline__ void compute_tile_full(const StepParams& P, const Dev
                                                   const Stage& st, int lane, SmemAll& sm, WarpTables& wt,
                                                   const float my_nf4, const float my_nf4t, const float my_vl,
                                                   const float my_vt, const float my_vl1, const float my_mag,
-                                                  const float clip, const uint32_t f_row, const uint32_t f_col) {
+                                                  const float clip, const uint32_t f_row, const uint32_t f_col,
+                                                  const float4& rbv) {
     const int half = lane >> 4, j = lane & 15, hb = half * 16;
     const int64_t blk = pair * 2 + half;
     const int64_t e0 = blk * kBlock + j * 8;
@@ -836,7 +838,7 @@ __device__ __forceinline__ void compute_tile_full(const StepParams& P, const Dev
                 f_ri = __ldg(d.vrow + row);
                 f_c0 = __ldg(reinterpret_cast<const float4*>(d.vcol + col));
                 f_c1 = __ldg(reinterpret_cast<const float4*>(d.vcol + col + 4));
-                const float4 rb4 = *reinterpret_cast<const float4*>(d.rbar);
+                const float4 rb4 = rbv;
                 f_rb = make_float2(rb4.x, rb4.y);
                 f_fast = rb4.z != 0.f;
             }
@@ -1315,6 +1317,7 @@ __global__ void __launch_bounds__(kStepThreads, 1) step_kernel(const __grid_cons
             const int64_t r = e / ws.desc.cols;
             f_row = (uint32_t)r;
             f_col = (uint32_t)(e - r * ws.desc.cols);
+            if (lane < 4) reinterpret_cast<float*>(&ws.rbv)[lane] = __ldg(ws.desc.rbar + lane);
         }
     };
     fpos();
@@ -1351,7 +1354,7 @@ __global__ void __launch_bounds__(kStepThreads, 1) step_kernel(const __grid_cons
             const bool full = c_p < c_n - 1 || ws.desc.numel - c_p * 2 * kBlock >= 2 * kBlock;
             if (full && !NEXTR) {
                 compute_tile_full<RECIPE, URTN, MSR>(P, ws.desc, c_p, stg, lane, sm, ws.wt, my_nf4, my_nf4t,
-                                                     my_vl, my_vt, my_vl1, my_mag, clip, f_row, f_col);
+                                                     my_vl, my_vt, my_vl1, my_mag, clip, f_row, f_col, ws.rbv);
             } else {
                 const int64_t left = ws.desc.numel - c_p * 2 * kBlock;
                 compute_tile<RECIPE, URTN, NEXTR>(P, ws.desc, c_p, (full || (left & 7) == 0) ? &stg : nullptr,
