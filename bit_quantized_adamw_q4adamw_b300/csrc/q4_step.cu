@@ -272,6 +272,31 @@ __device__ __forceinline__ float precond_next(const StepParams& P, float x) {
     return __frcp_rn(__fadd_rn(__fmul_rn(__fsqrt_rn(__fmul_rn(P.beta2, x)), P.c2_next), P.eps));
 }
 
+// precond_next through the correctly rounded fast square root and reciprocal
+// where their domains hold (beta2 x is +0 or in [2^-100, inf), the divisor
+// below 2^126; the divisor is at least eps >= 2^-100 under fast_math), else
+// the IEEE operations: the same value either way.
+__device__ __forceinline__ float precond_next_fast(const StepParams& P, float x) {
+    const float bx = __fmul_rn(P.beta2, x);
+    if (P.fast_math && sqrt_fast_domain(bx)) {
+        const float d = __fadd_rn(__fmul_rn(sqrt_rn_normal<0>(bx), P.c2_next), P.eps);
+        if (d < 0x1p126f) return rcp_rn_normal<1>(d);
+    }
+    return precond_next(P, x);
+}
+
+// The same on a pair.
+__device__ __forceinline__ float2 precond_next_fast2(const StepParams& P, float2 x) {
+    const float2 bx = mul2_rn(P.x2_beta2, x);
+    if (P.fast_math && sqrt_fast_domain(bx.x) && sqrt_fast_domain(bx.y)) {
+        // the paired product feeds scalar adds only
+        const float2 sc = mul2_rn(sqrt2_rn_normal(bx), make_float2(P.c2_next, P.c2_next));
+        const float2 d = make_float2(__fadd_rn(sc.x, P.eps), __fadd_rn(sc.y, P.eps));
+        if (d.x < 0x1p126f && d.y < 0x1p126f) return rcp2_rn_normal(d);
+    }
+    return make_float2(precond_next(P, x.x), precond_next(P, x.y));
+}
+
 // The update of 8 elements: r_i and theta'_i.
 template <bool FAST>
 __device__ __forceinline__ void update8(const StepParams& P, const float m1[8], const float v1[8], float th[8],
@@ -761,7 +786,7 @@ __device__ __forceinline__ void compute_tile(const StepParams& P, const DevTenso
 // when neither block needs the general requantisation (LM-head stochastic
 // rounding, or a new scale outside the fast range) the codes come from
 // per-bucket entries that carry everything one comparison needs.
-template <int RECIPE, bool URTN, bool MSR>
+template <int RECIPE, bool URTN, bool MSR, bool NEXTR>
 __device__ __forceinline__ void compute_tile_full(const StepParams& P, const DevTensor& d, int64_t pair,
                                                   const Stage& st, int lane, SmemAll& sm, WarpTables& wt,
                                                   const float my_nf4, const float my_nf4t, const float my_vl,
@@ -957,7 +982,7 @@ __device__ __forceinline__ void compute_tile_full(const StepParams& P, const Dev
         // levels) the SR decision reads (r_k, d_k) by cell; Update-RTN reads
         // (r_k, r_{k+1}) instead (r_15 twice: cell 15 keeps code 15).
         const float a = __fmul_rn(my_vl, s_v);
-        const float rk = P.fast_math ? precond<true>(P, a) : precond<false>(P, a);
+        const float rk = NEXTR ? precond_next_fast(P, a) : P.fast_math ? precond<true>(P, a) : precond<false>(P, a);
         const float rk1 = __shfl_down_sync(0xffffffffu, rk, 1);
         const float dk = URTN ? (j < 15 ? rk1 : rk) : j < 15 ? __fmul_rn(__fsub_rn(rk, rk1), kTwoM24) : 0.f;
         wt.rdv[half][j] = make_float2(rk, dk);
@@ -1041,10 +1066,12 @@ __device__ __forceinline__ void compute_tile_full(const StepParams& P, const Dev
                 const float2 e1v = lds_f32x2(rd_base + k1 * 8u);
                 const float2 rk = make_float2(e0v.x, e1v.x);
                 const float2 dk = make_float2(e0v.y, e1v.y);
-                const float2 gap = add2_rn(rk, neg2(r[k]));
+                // the r being rounded: the update's, or the next step's
+                const float2 ri = NEXTR ? precond_next_fast2(P, v1[k]) : r[k];
+                const float2 gap = add2_rn(rk, neg2(ri));
                 if (URTN) {
                     // Update-RTN: up when r - r_{k+1} < r_k - r (a tie keeps k)
-                    const float2 below = add2_rn(r[k], neg2(dk));
+                    const float2 below = add2_rn(ri, neg2(dk));
                     c[2 * k] = k0 + (below.x < gap.x ? 1u : 0u);
                     c[2 * k + 1] = k1 + (below.y < gap.y ? 1u : 0u);
                 } else {
@@ -1352,8 +1379,8 @@ __global__ void __launch_bounds__(kStepThreads, 1) step_kernel(const __grid_cons
             }
             Stage& stg = ws.st[s][sub];
             const bool full = c_p < c_n - 1 || ws.desc.numel - c_p * 2 * kBlock >= 2 * kBlock;
-            if (full && !NEXTR) {
-                compute_tile_full<RECIPE, URTN, MSR>(P, ws.desc, c_p, stg, lane, sm, ws.wt, my_nf4, my_nf4t,
+            if (full) {
+                compute_tile_full<RECIPE, URTN, MSR, NEXTR>(P, ws.desc, c_p, stg, lane, sm, ws.wt, my_nf4, my_nf4t,
                                                      my_vl, my_vt, my_vl1, my_mag, clip, f_row, f_col, ws.rbv);
             } else {
                 const int64_t left = ws.desc.numel - c_p * 2 * kBlock;
