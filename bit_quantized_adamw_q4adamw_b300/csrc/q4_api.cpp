@@ -437,7 +437,7 @@ Image build_image(const q4adamw_tensor_t* t, int n, int recipe, uint32_t flags, 
     // the factored recipe the factored tensors run on an instantiation without
     // the packed-v code and the 1-D ones on the general factored one; under
     // ZIP-SR / ZE-EDEN the tensors whose first moment is rounded
-    // stochastically (the LM head in the final phase) run on the m-SR
+    // stochastically (the LM head during its SR phase) run on the m-SR
     // instantiation and the rest on the plain one.  desc2 holds the
     // descriptors of the first group first; pairs2 the two groups' prefix sums.
     im.split_bit = recipe == Q4_RECIPE_FACTORED ? (uint32_t)q4::DF_FACTORED

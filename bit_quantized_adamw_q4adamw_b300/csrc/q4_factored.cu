@@ -1,12 +1,12 @@
 // Factored second-moment statistics for rank >= 2 tensors (AReno docs
-// "4-bit AdamW", section "State representation": Adafactor-style row and
-// column means of g^2 over the [shape[0], -1] view, kept as exponential
-// averages; 1-D tensors keep packed 4-bit v).
+// "4-bit AdamW", section "State representation": as in Adafactor, means of
+// g^2 over the rows and over the columns of the [shape[0], -1] view, kept as
+// exponential averages; 1-D tensors keep packed 4-bit v).
 //
 // Three launches, all multi-tensor and deterministic (fixed summation order,
 // no atomics).  A tensor may be one data-parallel shard of its parameter (the
-// same page: partial row and column sums are combined across the group before
-// their exponential update): its elements are [fbase, fbase + numel) of the
+// same page: each rank's row and column sums of g^2 are added over the group,
+// and R and C take their exponential update from the totals): its elements are [fbase, fbase + numel) of the
 // whole [rows, cols] matrix, the pass covers the rows they touch, and the
 // rows/cols kernels either write the shard's row and column sums for the
 // caller to add over the ranks, or update R and C from the added sums.

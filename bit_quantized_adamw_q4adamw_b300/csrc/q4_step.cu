@@ -964,7 +964,7 @@ __device__ __forceinline__ void compute_tile_full(const StepParams& P, const Dev
     }
 
     // ---- fast tables at the new scales ------------------------------------
-    // State-SR (LM head in the final phase): a_k = level k at the new scale;
+    // State-SR (LM head during its SR phase): a_k = level k at the new scale;
     // the cell search reads a_{c+1} (floats 0..15 of mt[half]), then
     // (a_k, d_k) with d_k = (a_{k+1} - a_k) 2^-24 (float2 8..23).
     if (RECIPE == Q4_RECIPE_TORCHAO) {
@@ -1145,7 +1145,7 @@ __device__ __forceinline__ void compute_tile_full(const StepParams& P, const Dev
 
 // ----------------------------------------------------------------- the kernel
 // URTN: the Update-RTN rounding variant of ZIP-SR; MSR: some tensor rounds
-// its first moment stochastically (the LM head in the final phase), which the
+// its first moment stochastically (the LM head during its SR phase), which the
 // fast path then handles too.  Separate instantiations, so that the main
 // kernels carry none of that code.
 // NEXTR (the next-step ZIP-SR variant) runs every tile on the general path.

@@ -10,8 +10,8 @@ pieces); it moves no data.
 Factored parameters (rank >= 2 under the factored recipe) are the exception:
 their row and column statistics span the whole parameter, so a shard of one
 cannot be stepped on its own.  AReno docs "4-bit AdamW", section "State
-representation": the partial row and column sums are combined across the
-data-parallel group before their exponential update.  With the library that
+representation": under data parallelism each rank's row and column sums of
+g^2 are added over the group, and R and C are updated from the totals.  With the library that
 is q4adamw_dp_factored_sums on every rank, a SUM all-reduce of the sums
 buffers, then q4adamw_dp_step (include/q4adamw.h).  The buffers line up only
 if every rank passes every factored parameter, in the same order, even where

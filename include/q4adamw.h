@@ -9,8 +9,8 @@
  *              chosen in preconditioner space r = 1/(sqrt(v_hat)+eps);
  *   ZE-EDEN -- NF4 first moment (RTN), zero-excluding dynamic-exponent 4-bit
  *              second moment (RTN) with an EDEN rescale of each block;
- * both with NF4 stochastic rounding of the LM-head first moment during the
- * final 10% of training (Table 2 note).  The AReno docs page "4-bit AdamW",
+ * both round the LM head's first moment stochastically on the NF4 grid in
+ * the last tenth of the training steps (Table 2 note).  The AReno docs page "4-bit AdamW",
  * section "State representation", adds the factored mode (Adafactor row and
  * column means over [shape[0], -1] for rank >= 2, packed zero-excluding v for
  * 1-D tensors) and fixes the 128-element parameter-local block.  The news page
@@ -226,8 +226,8 @@ int q4adamw_step(const q4adamw_tensor_t* t, int n, float lr, float beta1, float 
 
 /*
  * Global gradient-norm clipping (AReno docs "4-bit AdamW", section "State
- * representation": gradient norm and clipping operate directly on the BF16
- * gradient shards), in two calls on one stream:
+ * representation": the norm is taken, and the clip applied, on the BF16
+ * gradients themselves, shard by shard), in two calls on one stream:
  *
  * q4adamw_grad_sqnorm writes to *sqnorm (one device float, 4-B aligned,
  * caller-owned) the FP32 sum of squares of the BF16 gradients of t[0..n):
@@ -257,9 +257,9 @@ int q4adamw_step_clip(const q4adamw_tensor_t* t, int n, float lr, float beta1, f
 
 /*
  * Data-parallel shards of factored parameters (AReno docs "4-bit AdamW",
- * section "State representation": for data-parallel training the partial
- * row and column sums are combined across the group before their
- * exponential update).  Each rank passes its own shards; a shard of a
+ * section "State representation": under data parallelism each rank's sums
+ * of g^2 over rows and over columns are added over the group, and only the
+ * totals enter the exponential update of R and C).  Each rank passes its own shards; a shard of a
  * factored parameter i is the elements [elem_offset, elem_offset + numel)
  * of the parameter's row-major matrix [rows, full_numel[i] / rows]
  * (elem_offset a multiple of 128, as for every tensor; numel may be 0).

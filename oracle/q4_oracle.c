@@ -217,8 +217,9 @@ static float block_absmax(const float* x, int n) {
     return s;
 }
 
-/* ZE-EDEN calibration of one block (listing page Abstract: "rescales the
- * quantized second-moment block"; Table 2 EDEN column).  Reading: the EDEN
+/* ZE-EDEN calibration of one block (listing page Abstract: after its RTN
+ * codes are chosen, the block's second-moment scale is recalibrated; Table 2
+ * EDEN column).  Reading: the EDEN
  * scale |y|^2 / <y, yhat> (Vargaftik et al., EDEN, ICML 2022) with
  * y = v * (1/s) and yhat = L[q], folded into the stored block scale.
  * Sums run in one fixed order: 32 groups of 4 consecutive elements, each
@@ -592,7 +593,7 @@ static int step_tensor(const oracle_codebooks* cb, const oracle_tensor* T, float
             r[i] = rr;
         }
         /* 4-6: m requantisation (NF4, State-RTN; State-SR on the LM head
-         * in the final phase: listing page Table 2 note). */
+         * during its SR phase: listing page Table 2 note). */
         uint8_t qm[OB], qv[OB];
         memset(qm, 0, sizeof qm);
         memset(qv, 0, sizeof qv);

@@ -1,8 +1,8 @@
 """Data-parallel shards of factored parameters on the GPU, through the C ABI.
 
-AReno docs "4-bit AdamW", section "State representation": for data-parallel
-training the partial row and column sums are combined across the group
-before their exponential update.  The library's three-call protocol
+AReno docs "4-bit AdamW", section "State representation": under data
+parallelism each rank's row and column sums of g^2 are added over the group,
+and R and C are updated from the totals.  The library's three-call protocol
 (q4adamw_dp_factored_sums -> the caller adds the sums over the ranks ->
 q4adamw_dp_step) is checked here on one GPU, with the ranks' buffers side by
 side and their sums added on the device (the addition an all-reduce makes):

@@ -234,9 +234,9 @@ def test_factored_1d_tensor_stores_nearest_zero_excluding_level():
 
 
 # ------------------------------------------------- data-parallel shards
-# AReno docs "State representation": for data-parallel training the partial
-# row and column sums are combined across the group before the exponential
-# update.  A shard is a block-aligned run of the flattened parameter (it may
+# AReno docs "State representation": under data parallelism each rank's row
+# and column sums of g^2 are added over the group, and R and C are updated
+# from the totals.  A shard is a block-aligned run of the flattened parameter (it may
 # start and end inside a row); every rank keeps the whole R and C.
 
 def _exact_grad(n, rng, scale=2.0 ** -12):
