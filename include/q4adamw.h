@@ -138,8 +138,9 @@ typedef struct q4adamw_tensor {
 /*
  * State header: what a checkpoint of the 4-bit state must carry so that it is
  * resumed only by this optimizer in this representation (AReno docs,
- * "Requirements and errors": a saved 4-bit state resumes only with the 4-bit
- * optimizer; earlier representations are incompatible).  Host memory.
+ * "Requirements and errors": a checkpoint of the 4-bit state can be resumed
+ * by this optimizer alone, and states of older formats are rejected).  Host
+ * memory.
  */
 typedef struct q4adamw_header {
     uint32_t magic;       /* Q4ADAMW_MAGIC */

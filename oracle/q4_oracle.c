@@ -22,8 +22,8 @@
  *    packed values plus block scales = 1.0625 bytes/param).
  *  - AReno docs "4-bit AdamW", section "State representation" (parameter-
  *    local 128-element blocks, zero-excluding map for 1-D v, Adafactor row /
- *    column means over [shape[0], -1]) and "Requirements and errors" (fused
- *    kernel, bounded block-local FP32 work).
+ *    column means over [shape[0], -1]) and "Requirements and errors" (one
+ *    fused kernel whose FP32 work per block is local and of fixed size).
  * Where those pages are silent, the reading taken is stated at the function.
  *
  * Parity status of each function is given in oracle/oracle.py's header.
@@ -340,10 +340,10 @@ void oracle_adamw_fp32(float* theta, const float* grad, float* m, float* v, int6
 /* tensors viewed as [rows, cols] keep row means R and column means C of */
 /* g^2 as exponential averages; vhat_ij = R_i * C_j / mean_i(R_i).        */
 /* Sums run in double (exact per-term g^2 of BF16 inputs), rounded once. */
-/* For data-parallel training the same page has each rank's partial row  */
-/* and column sums combined across the group before the exponential      */
-/* update: factored_partials adds one shard's sums, factored_finalize    */
-/* applies the update from the sums over the whole parameter.            */
+/* Under data parallelism the same page adds each rank's row and column  */
+/* sums over the group, and R and C are updated from the totals:         */
+/* factored_partials adds one shard's sums, factored_finalize applies    */
+/* the update from the sums over the whole parameter.                    */
 /* ------------------------------------------------------------------ */
 static double clipped(uint16_t h, float clip) {
     float g = bf16_to_f32(h);

@@ -263,8 +263,9 @@ def _factored_worker(rank, world, port, q):
 
 
 def test_two_rank_factored_statistics_exchange():
-    # AReno docs "State representation": partial row and column sums combined
-    # across the data-parallel group before their exponential update.  Two
+    # AReno docs "State representation": under data parallelism each rank's
+    # row and column sums are added over the group, and R and C are updated
+    # from the totals.  Two
     # gloo ranks hold block-aligned shards (cut inside rows, one rank holding
     # no element of a parameter); after three steps every rank's R and C and
     # the union of the shards equal the single-rank step bit for bit.
