@@ -47,7 +47,7 @@ VARIANT_FLAGS = {"none": 0, "m_sr_all": 0x2, "v_update_rtn": 0x4, "v_next_r": 0x
 def parse():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--steps", type=int, default=50)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--workload", default="llama8b_zipsr")
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
@@ -63,7 +63,21 @@ def parse():
                     help="keep only the first N tensors of the workload (small cases for profiling)")
     ap.add_argument("--tensor-slice", default="",
                     help="keep tensors a:b of the workload (e.g. 1:10 = the first decoder layer of the 8B set)")
+    ap.add_argument("--companion", default="auto",
+                    help="a second workload timed after the first and reported under 'companion' "
+                         "('auto': the 8B ZE-EDEN step beside the default 8B ZIP-SR one; 'none': skip)")
     return ap.parse_args()
+
+
+def companion_workload(args):
+    """The workload timed beside the main one: the 8B model is specified with
+    both second-moment recipes, each timed over the same number of steps."""
+    if args.companion == "none":
+        return None
+    if args.companion != "auto":
+        return args.companion
+    plain = not args.tensors and not args.tensor_slice and args.variant == "none" and args.max_grad_norm is None
+    return "llama8b_zeeden" if plain and args.workload == "llama8b_zipsr" else None
 
 
 def dist_env():
@@ -387,6 +401,8 @@ def run_ours(args, rank, world, local):
         one_step(t)
         t += 1
     torch.cuda.synchronize()
+    main_alg = algorithmic_bytes(st, w.recipe)
+    main_launches = launches_per_step(st, mgn is not None, flags)
 
     sampler = ClockSampler(local) if rank == 0 else None
     if sampler:
@@ -417,9 +433,16 @@ def run_ours(args, rank, world, local):
         t += args.e2e_steps + 1
 
     sq_ms = time_sqnorm(st, stream, max(3, args.steps)) if mgn is not None else None
+    comp = None
+    cname = companion_workload(args)
+    if cname:
+        # the main state is released first: both 8B states do not need to be resident
+        st = None
+        torch.cuda.empty_cache()
+        comp = time_companion(args, W.WORKLOADS[cname], dev, stream, rank)
     if rank != 0:
         return
-    alg = algorithmic_bytes(st, w.recipe) + (2.0 * w.numel if mgn is not None else 0.0)
+    alg = main_alg + (2.0 * w.numel if mgn is not None else 0.0)
     peak, peak_kind = peaks()
     mean_ms = statistics.mean(per)
     achieved = alg / (mean_ms / 1e3) / 1e9
@@ -438,7 +461,7 @@ def run_ours(args, rank, world, local):
                      "traffic_source": tr["measured_on"] if tr else "no ncu record for this kernel source",
                      "algorithmic_bytes": alg, "kernel": "step_kernel (one launch per step)",
                      "frac_of_nominal_8tbs": achieved / NOMINAL_HBM_GBS},
-        "gpu_launches": launches_per_step(st, mgn is not None, flags) * args.steps,
+        "gpu_launches": main_launches * args.steps,
         "clocks": clocks,
     }
     if args.variant != "none":
@@ -457,11 +480,58 @@ def run_ours(args, rank, world, local):
                                "frac": 2.0 * w.numel / (sq_ms / 1e3) / 1e9 / peak}
     if e2e:
         line["e2e"] = e2e
+    if comp:
+        line["companion"] = comp
     if not args.no_cpu_baseline:
         v, desc, n, secs = oracle_sample(w, args.cpu_seconds)
         line["cpu_baseline"] = {"value": v, "unit": "params/s", "cores": 1, "host_cores": os.cpu_count(),
                                 "kind": "oracle", "sample": f"{desc}; {secs:.1f} s single-threaded"}
     print(json.dumps(line), flush=True)
+
+
+def time_companion(args, w, dev, stream, rank):
+    """The companion workload timed like the main one (W warm-up steps, then K
+    steps between CUDA events, clocks sampled); its own roofline and launch
+    count.  Called on every rank; rank 0's figures are reported."""
+    import torch
+    h = W_HYPER()
+    flags = 1 if w.lm_head_sr else 0
+    st = build_state(w, dev)
+    t = w.first_step
+    for _ in range(args.warmup):
+        st.step(t, h["lr"], h["beta1"], h["beta2"], h["eps"], h["weight_decay"], 0, flags, stream)
+        t += 1
+    torch.cuda.synchronize()
+    sampler = ClockSampler(torch.cuda.current_device()) if rank == 0 else None
+    if sampler:
+        sampler.start()
+        time.sleep(0.5)
+    evs = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps + 1)]
+    evs[0].record(stream)
+    for k in range(args.steps):
+        st.step(t, h["lr"], h["beta1"], h["beta2"], h["eps"], h["weight_decay"], 0, flags, stream)
+        t += 1
+        evs[k + 1].record(stream)
+    torch.cuda.synchronize()
+    clocks = sampler.stop() if sampler else None
+    per = [evs[k].elapsed_time(evs[k + 1]) for k in range(args.steps)]
+    mean_ms = statistics.mean(per)
+    alg = algorithmic_bytes(st, w.recipe)
+    peak, _ = peaks()
+    achieved = alg / (mean_ms / 1e3) / 1e9
+    tr = traffic_record(w.name)
+    out = {"config": workload_config(w, 1), "steps": args.steps, "warmup": args.warmup,
+           "ms_per_step": evs[0].elapsed_time(evs[-1]) / args.steps, "value": w.numel / (mean_ms / 1e3),
+           "unit": "params/s",
+           "step_ms": {"median": statistics.median(per), "p10": sorted(per)[len(per) // 10],
+                       "p90": sorted(per)[min(len(per) - 1, (9 * len(per)) // 10)]},
+           "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
+                        "traffic": (tr["dram_bytes_per_param"] * w.numel) if tr else None,
+                        "algorithmic_bytes": alg},
+           "gpu_launches": launches_per_step(st, False, flags) * args.steps, "clocks": clocks}
+    del st
+    torch.cuda.empty_cache()
+    return out
 
 
 def run_e2e(args, st, w, dev, stream, t0):

@@ -42,3 +42,18 @@ def test_strip_comments_keeps_code_and_literals():
 def test_kernel_source_hash_is_stable():
     h = bench.kernel_source_hash()
     assert len(h) == 16 and h == bench.kernel_source_hash()
+
+
+def test_companion_workload_only_beside_the_plain_default():
+    def args(**kw):
+        base = dict(companion="auto", workload="llama8b_zipsr", tensors=0, tensor_slice="", variant="none",
+                    max_grad_norm=None)
+        base.update(kw)
+        return SimpleNamespace(**base)
+    assert bench.companion_workload(args()) == "llama8b_zeeden"
+    assert bench.companion_workload(args(companion="none")) is None
+    assert bench.companion_workload(args(workload="llama8b_zeeden")) is None
+    assert bench.companion_workload(args(tensor_slice="1:10")) is None
+    assert bench.companion_workload(args(variant="m_sr_all")) is None
+    assert bench.companion_workload(args(max_grad_norm=1.0)) is None
+    assert bench.companion_workload(args(companion="gpt1p4b_zipsr", workload="qwen0p6b_factored")) == "gpt1p4b_zipsr"
