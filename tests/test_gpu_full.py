@@ -154,6 +154,17 @@ def test_gpt1p4b_torchao_sampled_blocks():
     assert n >= STEPS * 4 * 100
 
 
+@pytest.mark.parametrize("variant", ["m_sr_all", "v_update_rtn", "v_next_r", "v_next_r_update_rtn"])
+def test_gpt1p4b_rounding_variants_sampled_blocks(variant):
+    # the rounding variants at the full 1.4B size, on the same launch path as
+    # bench.py --variant (their full tiles take the fast path)
+    fl = {"m_sr_all": q4.Q4_M_SR_ALL, "v_update_rtn": q4.Q4_V_UPDATE_RTN, "v_next_r": q4.Q4_V_NEXT_R,
+          "v_next_r_update_rtn": q4.Q4_V_NEXT_R | q4.Q4_V_UPDATE_RTN}[variant]
+    w = W.WORKLOADS["gpt1p4b_zipsr"]
+    n = _run_packed(w, 3, q4.Q4_LM_HEAD_SR_ACTIVE | fl)
+    assert n >= 3 * 4 * 100
+
+
 @pytest.mark.parametrize("name", ["llama8b_zipsr", "llama8b_zeeden"])
 def test_llama8b_sampled_blocks(name):
     w = W.WORKLOADS[name]
