@@ -439,7 +439,7 @@ def run_ours(args, rank, world, local):
         # the main state is released first: both 8B states do not need to be resident
         st = None
         torch.cuda.empty_cache()
-        comp = time_companion(args, W.WORKLOADS[cname], dev, stream, rank)
+        comp = time_companion(args, W.WORKLOADS[cname], dev, stream, rank, local)
     if rank != 0:
         return
     alg = main_alg + (2.0 * w.numel if mgn is not None else 0.0)
@@ -489,7 +489,7 @@ def run_ours(args, rank, world, local):
     print(json.dumps(line), flush=True)
 
 
-def time_companion(args, w, dev, stream, rank):
+def time_companion(args, w, dev, stream, rank, gpu_index):
     """The companion workload timed like the main one (W warm-up steps, then K
     steps between CUDA events, clocks sampled); its own roofline and launch
     count.  Called on every rank; rank 0's figures are reported."""
@@ -502,7 +502,7 @@ def time_companion(args, w, dev, stream, rank):
         st.step(t, h["lr"], h["beta1"], h["beta2"], h["eps"], h["weight_decay"], 0, flags, stream)
         t += 1
     torch.cuda.synchronize()
-    sampler = ClockSampler(torch.cuda.current_device()) if rank == 0 else None
+    sampler = ClockSampler(gpu_index) if rank == 0 else None
     if sampler:
         sampler.start()
         time.sleep(0.5)
