@@ -247,3 +247,44 @@ def test_mat4096_zeeden_full_size_hundred_steps():
             checked.append(t)
     print(f"mat4096_zeeden: 100 steps, {w.tensors[0].numel} elements compared at steps {checked}, "
           f"excepted elements: 0")
+
+
+def test_tensor_beyond_2_pow_31_elements_sampled_blocks():
+    # one 1-D tensor of 2^31 + 2^20 + 37 elements (64-bit element offsets in
+    # the tile list, the copy sources and the Philox counters; a ragged last
+    # block), flagged as the LM head with its SR phase active, so both draw
+    # purposes run at element indices above 2^31.  Blocks on both sides of
+    # element 2^31, the first and the last block are stepped by the oracle for
+    # 3 steps and compared bit for bit.
+    n = 2 ** 31 + 2 ** 20 + 37
+    w = W.custom("big", [(n,)], "zip_sr", flags=[W.T_LM_HEAD])
+    dev = torch.device("cuda", 0)
+    st = _build(w, dev)
+    nb = (n + BLOCK - 1) // BLOCK
+    edge = 2 ** 31 // BLOCK
+    blocks = [0, edge - 1, edge, edge + 1, nb - 1]
+    th = st.view(0, "param")
+    ora = {b: O.OracleTensor.zeros_state(th[b * BLOCK:min(b * BLOCK + BLOCK, n)].cpu().numpy(), 0, rows=1,
+                                         flags=W.T_LM_HEAD, elem_offset=b * BLOCK, recipe="zip_sr")
+           for b in blocks}
+    h = HYPER
+    for t in range(1, 4):
+        _draw(w, st, t, dev)
+        g = st.view(0, "grad")
+        host_g = {b: bf16_bits(g[b * BLOCK:b * BLOCK + o.param.size]) for b, o in ora.items()}
+        st.step(t, h["lr"], h["beta1"], h["beta2"], h["eps"], h["weight_decay"], seed=0,
+                flags=q4.Q4_LM_HEAD_SR_ACTIVE)
+        torch.cuda.synchronize()
+        assert st.status() == 0
+        for b, o in ora.items():
+            o.step(host_g[b], h["lr"], h["beta1"], h["beta2"], h["eps"], h["weight_decay"], t, 0, "zip_sr",
+                   q4.Q4_LM_HEAD_SR_ACTIVE)
+            lo, k = b * BLOCK, o.param.size
+            assert not neq_f32(st.view(0, "param")[lo:lo + k].cpu().numpy(), o.param).any(), (b, t)
+            assert np.array_equal(bf16_bits(st.view(0, "param_bf16")[lo:lo + k]), o.param_bf16), (b, t)
+            assert np.array_equal(st.view(0, "m_codes")[b * 64:(b + 1) * 64].cpu().numpy(), o.m_codes), (b, t)
+            assert np.array_equal(st.view(0, "v_codes")[b * 64:(b + 1) * 64].cpu().numpy(), o.v_codes), (b, t)
+            assert not neq_f32(st.view(0, "m_scale")[b:b + 1].cpu().numpy(), o.m_scale).any(), (b, t)
+            assert not neq_f32(st.view(0, "v_scale")[b:b + 1].cpu().numpy(), o.v_scale).any(), (b, t)
+    _free(st)
+    print(f"big tensor of {n} elements: 3 steps, {len(blocks)} blocks per step bit-identical, excepted elements: 0")
