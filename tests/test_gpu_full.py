@@ -288,3 +288,54 @@ def test_tensor_beyond_2_pow_31_elements_sampled_blocks():
             assert not neq_f32(st.view(0, "v_scale")[b:b + 1].cpu().numpy(), o.v_scale).any(), (b, t)
     _free(st)
     print(f"big tensor of {n} elements: 3 steps, {len(blocks)} blocks per step bit-identical, excepted elements: 0")
+
+
+def test_factored_tensor_beyond_2_pow_31_elements_closed_form():
+    # a factored [65537, 32768] parameter (2^31 + 32768 elements: 64-bit matrix
+    # positions in the statistics pass, 257 column slabs, mean(R) over 65537
+    # rows, the step's (row, column) tracking past element 2^31) with every
+    # gradient 2^-4 (exact in BF16).  Closed forms after one step from zero
+    # state: every row and column mean of g^2 is 2^-8 exactly, so every R_i
+    # and C_j is omb2 * 2^-8 exactly; every m' is omb1 * 2^-4, so every NF4
+    # code is 15 and every m scale m'; theta follows AdamW with vhat = R_i C_j
+    # / mean(R) = omb2 * 2^-8 (up to the rounding of mean(R)), checked within
+    # the factored tolerance on blocks around element 2^31 and at both ends.
+    rows, cols = 65537, 32768
+    n = rows * cols
+    w = W.custom("bigf", [(rows, cols)], "factored", flags=[W.T_FACTORED])
+    dev = torch.device("cuda", 0)
+    st = _build(w, dev)
+    g = 2.0 ** -4
+    st.view(0, "grad").fill_(g)
+    nb = n // BLOCK
+    edge = 2 ** 31 // BLOCK
+    blocks = [0, edge - 1, edge, edge + 1, nb - 1]
+    th0 = {b: st.view(0, "param")[b * BLOCK:(b + 1) * BLOCK].cpu().numpy().astype(np.float64) for b in blocks}
+    h = HYPER
+    st.step(1, h["lr"], h["beta1"], h["beta2"], h["eps"], h["weight_decay"], seed=0)
+    torch.cuda.synchronize()
+    assert st.status() == 0
+    # the host scalars as the library forms them: from the FP32 arguments, in
+    # double, each rounded once to FP32
+    f32 = np.float32
+    lr, b1, b2, eps, wd = (float(f32(h[k])) for k in ("lr", "beta1", "beta2", "eps", "weight_decay"))
+    omb1, omb2 = f32(1.0 - b1), f32(1.0 - b2)
+    x = f32(omb2 * f32(2.0 ** -8))
+    R = st.view(0, "v_row").cpu().numpy()
+    C = st.view(0, "v_col").cpu().numpy()
+    assert R.shape == (rows,) and C.shape == (cols,)
+    assert (R == x).all() and (C == x).all(), (R.min(), R.max(), C.min(), C.max(), x)
+    m1 = f32(omb1 * f32(g))
+    c2 = f32(1.0 / np.sqrt(1.0 - b2))
+    step_size = f32(lr / (1.0 - b1))
+    decay = f32(1.0 - lr * wd)
+    r = 1.0 / (np.sqrt(float(x)) * float(c2) + eps)
+    for b in blocks:
+        th = st.view(0, "param")[b * BLOCK:(b + 1) * BLOCK].cpu().numpy().astype(np.float64)
+        want = th0[b] * float(decay) - float(step_size) * float(m1) * r
+        assert (np.abs(th - want) <= 1e-6 * np.maximum(1.0, np.abs(want))).all(), (b, np.abs(th - want).max())
+        assert (st.view(0, "m_codes")[b * 64:(b + 1) * 64].cpu().numpy() == 0xFF).all(), b
+        assert st.view(0, "m_scale")[b:b + 1].cpu().numpy()[0] == m1, b
+    _free(st)
+    print(f"factored tensor of {n} elements: R, C exact on all {rows} rows and {cols} columns; "
+          f"{len(blocks)} blocks within the factored tolerance")
